@@ -1,0 +1,205 @@
+"""Seeded synthetic inputs for the attention forward pass.
+
+This module only draws inputs; it holds none of the attention arithmetic.  The
+CUDA path's tests, the benchmark and the CPU oracle's tests all take their
+inputs from here, so every side sees the same 16-bit values.
+
+Recipe (all draws on the CPU, ``torch.Generator().manual_seed(seed)``):
+
+* packed variable-length workloads first draw their sequence lengths, then
+  Q, K, V;
+* Q, K, V are drawn in fp32 as N(0, sigma^2) and cast (round to nearest) to the
+  16-bit dtype; the oracle reads those same rounded values;
+* the rising-bias workload reserves channel D-1 of Q and K to carry a per-key
+  bias b(j) in log2 units: q[..., D-1] = 1 and k[j, ..., D-1] =
+  b(j) * ln2 / scale, so scale * <q_i, k_j> gains exactly b(j) * ln2 (natural
+  units), i.e. b(j) log2 units.  b is constant within a 128-key block and grows
+  by 0.5 * (blk mod 25) log2 units at block blk >= 1, so successive block maxima
+  rise by 0 .. 12 log2 units and both skipped and performed lazy rescales occur
+  when the keys are walked in ascending order.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+DTYPE_CODE = {"fp16": 0, "bf16": 1}
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One attention forward problem, described by its sizes and draw recipe."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    S: int                 # Sq = Sk for dense problems; unused for packed ones
+    D: int
+    dtype: str
+    causal: bool
+    sigma: float = 1.0
+    rising_bias: bool = False
+    varlen_count: int = 0  # >0: packed problem with this many sequences
+    varlen_min: int = 0
+    varlen_max: int = 0
+    seed: int = 0
+
+
+# The five workloads the method is validated and measured on.  Seeds are
+# 1000 + index.  ``attention fwd`` throughput is quoted on the second one.
+WORKLOADS = [
+    Workload("b1_h2_s128_d64_fp16_noncausal", 1, 2, 2, 128, 64, "fp16", False,
+             seed=1000),
+    Workload("b4_h16_s2048_d128_bf16_causal", 4, 16, 16, 2048, 128, "bf16", True,
+             seed=1001),
+    Workload("b2_hq32_hkv8_s4096_d128_bf16_causal_risingbias", 2, 32, 8, 4096, 128,
+             "bf16", True, rising_bias=True, seed=1002),
+    Workload("varlen16_l64to8192_h16_d64_fp16_causal", 16, 16, 16, 0, 64, "fp16",
+             True, varlen_count=16, varlen_min=64, varlen_max=8192, seed=1003),
+    Workload("b1_h8_s32768_d128_bf16_noncausal_sigma2", 1, 8, 8, 32768, 128, "bf16",
+             False, sigma=math.sqrt(2.0), seed=1004),
+]
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+@dataclass
+class Case:
+    """Drawn inputs plus the C-ABI size arguments that describe them."""
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int              # dense: rows per sequence; packed: total_q
+    Sk: int              # dense: keys per sequence; packed: total_k
+    D: int
+    scale: float
+    causal: bool
+    dtype: str
+    cu_seqlens_q: Optional[torch.Tensor] = None   # int32 [B + 1] (CPU)
+    cu_seqlens_k: Optional[torch.Tensor] = None
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def varlen(self) -> bool:
+        return self.cu_seqlens_q is not None
+
+    def seq_lengths(self):
+        """(Lq, Lk) per sequence."""
+        if not self.varlen:
+            return [(self.Sq, self.Sk)] * self.B
+        cq = self.cu_seqlens_q.tolist()
+        ck = self.cu_seqlens_k.tolist()
+        return [(cq[b + 1] - cq[b], ck[b + 1] - ck[b]) for b in range(self.B)]
+
+    def lse_rows(self) -> int:
+        """Number of query rows (= LSE entries)."""
+        return self.Hq * (self.Sq if self.varlen else self.B * self.Sq)
+
+
+def rising_bias_log2(n_keys: int, block: int = 128, period: int = 25,
+                     step: float = 0.5) -> torch.Tensor:
+    """Per-key bias b(j) in log2 units (constant within each key block)."""
+    nblk = (n_keys + block - 1) // block
+    rise = torch.tensor([0.0] + [step * (i % period) for i in range(1, nblk)],
+                        dtype=torch.float64)
+    per_block = torch.cumsum(rise, 0)
+    return per_block.repeat_interleave(block)[:n_keys]
+
+
+def _draw(shape, sigma, dtype, g):
+    x = torch.randn(shape, generator=g, dtype=torch.float32)
+    if sigma != 1.0:
+        x = x * sigma
+    return x.to(DTYPES[dtype])
+
+
+def make_case(B, Hq, Hkv, Sq, Sk, D, dtype="bf16", causal=False, seed=0,
+              sigma=1.0, rising_bias=False, seqlens_q=None, seqlens_k=None,
+              scale=None, zero_q=False) -> Case:
+    """Draw one problem.
+
+    Dense when ``seqlens_q`` is None (q [B, Sq, Hq, D], k/v [B, Sk, Hkv, D]);
+    packed otherwise (q [sum Lq, Hq, D], k/v [sum Lk, Hkv, D], B = number of
+    sequences, Sq / Sk = the packed totals).
+    """
+    g = torch.Generator().manual_seed(int(seed))
+    scale = (1.0 / math.sqrt(D)) if scale is None else float(scale)
+    cu_q = cu_k = None
+    if seqlens_q is not None:
+        seqlens_k = seqlens_q if seqlens_k is None else seqlens_k
+        lq = [int(x) for x in seqlens_q]
+        lk = [int(x) for x in seqlens_k]
+        B = len(lq)
+        cu_q = torch.tensor([0] + lq, dtype=torch.int64).cumsum(0).to(torch.int32)
+        cu_k = torch.tensor([0] + lk, dtype=torch.int64).cumsum(0).to(torch.int32)
+        Sq, Sk = int(cu_q[-1]), int(cu_k[-1])
+        q_shape, kv_shape = (Sq, Hq, D), (Sk, Hkv, D)
+    else:
+        q_shape, kv_shape = (B, Sq, Hq, D), (B, Sk, Hkv, D)
+    q = _draw(q_shape, sigma, dtype, g)
+    k = _draw(kv_shape, sigma, dtype, g)
+    v = _draw(kv_shape, sigma, dtype, g)
+    if zero_q:
+        q.zero_()
+    if rising_bias:
+        # channel D-1 carries b(j) log2 units: scale * q . k gains b(j) * ln2
+        q[..., D - 1] = 1.0
+        if cu_k is None:
+            bias = rising_bias_log2(Sk) * math.log(2.0) / scale
+            k[..., D - 1] = bias.view(1, Sk, 1).to(k.dtype)
+        else:
+            for b in range(B):
+                s0, s1 = int(cu_k[b]), int(cu_k[b + 1])
+                bias = rising_bias_log2(s1 - s0) * math.log(2.0) / scale
+                k[s0:s1, :, D - 1] = bias.view(-1, 1).to(k.dtype)
+    return Case(q, k, v, B, Hq, Hkv, Sq, Sk, D, scale, bool(causal), dtype, cu_q, cu_k)
+
+
+def make_workload(w: Workload) -> Case:
+    """Draw the inputs of one named workload."""
+    if w.varlen_count:
+        g = torch.Generator().manual_seed(int(w.seed))
+        lens = torch.randint(w.varlen_min, w.varlen_max + 1, (w.varlen_count,),
+                             generator=g).tolist()
+        case = make_case(w.varlen_count, w.Hq, w.Hkv, 0, 0, w.D, w.dtype, w.causal,
+                         seed=w.seed + 7919, sigma=w.sigma,
+                         rising_bias=w.rising_bias, seqlens_q=lens)
+    else:
+        case = make_case(w.B, w.Hq, w.Hkv, w.S, w.S, w.D, w.dtype, w.causal,
+                         seed=w.seed, sigma=w.sigma, rising_bias=w.rising_bias)
+    case.meta["workload"] = w.name
+    return case
+
+
+def visible_pairs(case: Case) -> int:
+    """Number of (query, key) pairs the mask leaves visible, summed over the
+    sequences of one head (bottom-right aligned causal mask)."""
+    total = 0
+    for lq, lk in case.seq_lengths():
+        if not case.causal:
+            total += lq * lk
+            continue
+        off = lk - lq
+        # row i sees min(lk, max(0, i + off + 1)) keys
+        for_rows = torch.arange(lq, dtype=torch.int64) + off + 1
+        total += int(for_rows.clamp(min=0, max=lk).sum())
+    return total
+
+
+def attention_flops(case: Case) -> int:
+    """FLOPs of the two contractions (QK^T and PV): 4 * D * Hq * visible pairs."""
+    pairs = visible_pairs(case)
+    return 4 * case.D * case.Hq * pairs
+
+
+def algorithmic_bytes(case: Case) -> int:
+    """Q, K, V read once plus O written (16-bit) and LSE written (fp32)."""
+    el = 2
+    return (case.q.numel() + case.k.numel() + case.v.numel() + case.q.numel()) * el \
+        + case.lse_rows() * 4

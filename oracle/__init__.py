@@ -1,0 +1,173 @@
+"""fp64 CPU oracle for the exact attention forward pass.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the
+benchmark's CPU-baseline / reference leg are the only callers.  The product
+path (the CUDA library and its Python binding) never imports this package, and
+this package imports nothing from the product.
+
+The arithmetic lives in ``attention_oracle.c`` (plain C, fp64, OpenMP over
+independent rows); this module only builds it with gcc and marshals arrays.
+
+* :func:`attention` — the plain definition (full score row, softmax, O, LSE).
+* :func:`attention_online` — the streaming restatement with the lazy-rescale
+  threshold and max lagging of the fork's v1.7 release notes (section 1.2),
+  plus its skip / rescale counters and the largest P.
+
+Both take the 16-bit inputs as exact float32 copies and address rows by their
+LSE index (dense: ``(b * Hq + h) * Sq + i``; packed: ``h * total_q + t``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attention_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` with gcc + OpenMP (no GPU needed)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        f32p = ctypes.POINTER(ctypes.c_float)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        c_int = ctypes.c_int
+        common = [f32p, f32p, f32p, f64p, f64p,
+                  c_int, c_int, c_int, c_int, c_int, c_int,
+                  ctypes.c_double, c_int, i32p, i32p, i64p, ctypes.c_int64]
+        lib.oracle_attention.argtypes = common + [c_int]
+        lib.oracle_attention.restype = c_int
+        lib.oracle_attention_online.argtypes = common + [
+            c_int, ctypes.c_double, c_int, i64p, i64p, f64p, c_int]
+        lib.oracle_attention_online.restype = c_int
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = c_int
+        _lib = lib
+        return lib
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def _as_f32(x):
+    if hasattr(x, "detach"):  # torch tensor: upcast exactly on the CPU
+        x = x.detach().to("cpu").float().numpy()
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def _ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _prep(q, k, v, B, Hq, Hkv, Sq, Sk, D, cu_seqlens_q, cu_seqlens_k, rows):
+    q, k, v = _as_f32(q), _as_f32(k), _as_f32(v)
+    varlen = cu_seqlens_q is not None
+    if varlen:
+        cu_q = np.ascontiguousarray(np.asarray(
+            cu_seqlens_q.cpu() if hasattr(cu_seqlens_q, "cpu") else cu_seqlens_q),
+            dtype=np.int32)
+        cu_k = np.ascontiguousarray(np.asarray(
+            cu_seqlens_k.cpu() if hasattr(cu_seqlens_k, "cpu") else cu_seqlens_k),
+            dtype=np.int32)
+        total_rows = Hq * int(cu_q[B])
+    else:
+        cu_q = cu_k = None
+        total_rows = B * Hq * Sq
+    if rows is None:
+        rows = np.arange(total_rows, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    return q, k, v, cu_q, cu_k, rows
+
+
+def attention(q, k, v, B, Hq, Hkv, Sq, Sk, D, scale, causal,
+              cu_seqlens_q=None, cu_seqlens_k=None, rows=None, nthreads=0):
+    """Plain-definition attention in fp64 for the requested rows.
+
+    Returns ``(o_rows [nrows, D] float64, lse_rows [nrows] float64)``; with
+    ``rows=None`` every row, in LSE-index order.
+    """
+    lib = _load()
+    q, k, v, cu_q, cu_k, rows = _prep(q, k, v, B, Hq, Hkv, Sq, Sk, D,
+                                      cu_seqlens_q, cu_seqlens_k, rows)
+    n = rows.shape[0]
+    o = np.zeros((n, D), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    i32n = ctypes.POINTER(ctypes.c_int32)()
+    rc = lib.oracle_attention(
+        _ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float), _ptr(v, ctypes.c_float),
+        _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+        B, Hq, Hkv, Sq, Sk, D, float(scale), int(bool(causal)),
+        _ptr(cu_q, ctypes.c_int32) if cu_q is not None else i32n,
+        _ptr(cu_k, ctypes.c_int32) if cu_k is not None else i32n,
+        _ptr(rows, ctypes.c_int64), n, int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention failed with status {rc}")
+    return o, lse
+
+
+def attention_online(q, k, v, B, Hq, Hkv, Sq, Sk, D, scale, causal,
+                     cu_seqlens_q=None, cu_seqlens_k=None, rows=None,
+                     block_n=128, threshold=8.0, lagging=True, nthreads=0):
+    """Online-softmax restatement (fp64) with the lazy-rescale rule.
+
+    Returns ``(o_rows, lse_rows, stats)`` where ``stats`` holds the number of
+    skipped and performed rescales and the largest P seen.
+    """
+    lib = _load()
+    q, k, v, cu_q, cu_k, rows = _prep(q, k, v, B, Hq, Hkv, Sq, Sk, D,
+                                      cu_seqlens_q, cu_seqlens_k, rows)
+    n = rows.shape[0]
+    o = np.zeros((n, D), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    n_skip = ctypes.c_int64(0)
+    n_rescale = ctypes.c_int64(0)
+    max_p = ctypes.c_double(0.0)
+    i32n = ctypes.POINTER(ctypes.c_int32)()
+    rc = lib.oracle_attention_online(
+        _ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float), _ptr(v, ctypes.c_float),
+        _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+        B, Hq, Hkv, Sq, Sk, D, float(scale), int(bool(causal)),
+        _ptr(cu_q, ctypes.c_int32) if cu_q is not None else i32n,
+        _ptr(cu_k, ctypes.c_int32) if cu_k is not None else i32n,
+        _ptr(rows, ctypes.c_int64), n, int(block_n), float(threshold),
+        int(bool(lagging)), ctypes.byref(n_skip), ctypes.byref(n_rescale),
+        ctypes.byref(max_p), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_online failed with status {rc}")
+    return o, lse, {"skips": n_skip.value, "rescales": n_rescale.value,
+                    "max_p": max_p.value}
+
+
+def row_index_dense(b, h, i, Hq, Sq):
+    """LSE index of dense row (b, h, i)."""
+    return (np.asarray(b, dtype=np.int64) * Hq + h) * Sq + i
+
+
+def row_index_packed(h, t, total_q):
+    """LSE index of packed row (h, global token t)."""
+    return np.asarray(h, dtype=np.int64) * total_q + t
