@@ -1,0 +1,164 @@
+"""GB300 (sm_103a) exact attention forward — thin Python binding over libfa.so.
+
+Every function here only marshals arguments into the C ABI declared in
+``include/fa.h``; all of the computation runs in the library's CUDA kernel.
+PyTorch is used for device memory and streams only.  There is no fallback:
+if ``libfa.so`` has not been built, every call raises :class:`LibraryMissing`.
+
+Functions with the C names (``fa_fwd``, ``fa_get_device_error``, ...) take
+tensors or raw integer addresses.  :func:`attention_forward` is a convenience
+wrapper that allocates O and LSE with PyTorch and checks the status.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = [
+    "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
+    "FA_ERR_BAD_SEQLENS", "FA_DTYPE_FP16", "FA_DTYPE_BF16", "LibraryMissing", "FaError",
+    "library_path", "load_library", "fa_fwd", "fa_get_device_error", "fa_debug_wait_timeout",
+    "fa_status_string", "fa_version", "attention_forward", "EXPORTED_SYMBOLS",
+]
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+FA_ERR_BAD_SEQLENS = 5
+FA_DTYPE_FP16 = 0
+FA_DTYPE_BF16 = 1
+
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_get_device_error", "fa_debug_wait_timeout",
+                    "fa_status_string", "fa_version")
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+_lock = threading.Lock()
+
+
+class LibraryMissing(RuntimeError):
+    """libfa.so is not built (run ``__graft_entry__.build()``)."""
+
+
+class FaError(RuntimeError):
+    def __init__(self, status, where="fa_fwd"):
+        self.status = status
+        super().__init__(f"{where} failed: {status} ({fa_status_string(status)})")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libfa.so")
+
+
+def load_library():
+    """Load libfa.so (once) and declare the C signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise LibraryMissing(
+                f"{path} is missing: build it with __graft_entry__.build() "
+                "(nvcc, sm_103a); there is no fallback implementation")
+        lib = ctypes.CDLL(path)
+        vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
+                               vp, vp, vp, i32]
+        lib.fa_fwd.restype = i32
+        lib.fa_get_device_error.argtypes = [vp]
+        lib.fa_get_device_error.restype = i32
+        lib.fa_debug_wait_timeout.argtypes = [ctypes.c_longlong, vp]
+        lib.fa_debug_wait_timeout.restype = i32
+        lib.fa_status_string.argtypes = [i32]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _addr(x):
+    """Device / host address of a tensor, an int address, or None (NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream  # torch.cuda.Stream
+
+
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal,
+           cu_seqlens_q, cu_seqlens_k, stream, dtype) -> int:
+    """Call the C ``fa_fwd``; returns its status code (see include/fa.h)."""
+    lib = load_library()
+    return lib.fa_fwd(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(Hq),
+                      int(Hkv), int(Sq), int(Sk), int(D), float(scale), int(causal),
+                      _addr(cu_seqlens_q), _addr(cu_seqlens_k), _stream(stream), int(dtype))
+
+
+def fa_get_device_error(stream=None) -> int:
+    return load_library().fa_get_device_error(_stream(stream))
+
+
+def fa_debug_wait_timeout(limit_cycles, stream=None) -> int:
+    return load_library().fa_debug_wait_timeout(int(limit_cycles), _stream(stream))
+
+
+def fa_status_string(status) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def fa_version() -> int:
+    return load_library().fa_version()
+
+
+def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens_q=None,
+                      cu_seqlens_k=None, out=None, lse=None, stream=None):
+    """Exact attention forward on CUDA tensors; returns ``(out, lse)``.
+
+    Dense: q [B, Sq, Hq, D], k/v [B, Sk, Hkv, D] -> out like q, lse [B, Hq, Sq].
+    Packed: q [total_q, Hq, D], k/v [total_k, Hkv, D] with int32 cu_seqlens of
+    B + 1 offsets -> out like q, lse [Hq, total_q].
+    """
+    import torch
+
+    dtype = {torch.float16: FA_DTYPE_FP16, torch.bfloat16: FA_DTYPE_BF16}.get(q.dtype)
+    if dtype is None:
+        raise FaError(FA_ERR_UNSUPPORTED, "attention_forward (dtype)")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise FaError(FA_ERR_INVALID_ARG, "attention_forward (contiguity)")
+    if cu_seqlens_q is None:
+        B, Sq, Hq, D = q.shape
+        Sk, Hkv = k.shape[1], k.shape[2]
+        lse_shape = (B, Hq, Sq)
+    else:
+        Sq, Hq, D = q.shape
+        Sk, Hkv = k.shape[0], k.shape[1]
+        B = cu_seqlens_q.numel() - 1
+        lse_shape = (Hq, Sq)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = fa_fwd(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, D, scale, int(bool(causal)),
+                cu_seqlens_q, cu_seqlens_k, stream, dtype)
+    if st != FA_OK:
+        raise FaError(st)
+    return out, lse

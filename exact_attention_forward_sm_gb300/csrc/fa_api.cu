@@ -1,0 +1,217 @@
+// C ABI of libfa.so: argument checks, TMA tensor maps, kernel dispatch and the
+// per-device status word.  See include/fa.h for the contract of each call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_launch.cuh"
+
+// Status word written by kernels on a device-side error (first error wins).
+// Host code only ever uses its device address, fetched per device below.
+__device__ int g_fa_status;
+
+namespace fa {
+
+// Kernel used only to exercise the bounded wait: nothing arrives on the barrier.
+static __global__ void fa_wait_timeout_kernel(long long limit, int *status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_bar(smem_u32(&bar), 0, &abort_flag, limit, status);
+  __syncthreads();
+}
+
+}  // namespace fa
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr long long kDefaultWaitLimit = 1ll << 33;  // ~4 s of SM clock
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+std::mutex g_status_mu;
+int *g_status_ptr[kMaxDevices] = {};
+
+// Device address of g_fa_status on the current device.
+int *status_ptr(int device) {
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status_ptr[device]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fa_status) != cudaSuccess) return nullptr;
+    g_status_ptr[device] = static_cast<int *>(ptr);
+  }
+  return g_status_ptr[device];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tensor map over a [batch, rows, heads, D] (or packed [rows, heads, D]) buffer,
+// box = 128 rows x 64 elements of one head, 128-byte swizzle.  Out-of-range
+// rows read as zero.
+bool make_map(CUtensorMap *m, const void *base, bool bf16, int D, int heads, int64_t rows,
+              int64_t batch) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows,
+                              (cuuint64_t)batch};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2,
+                                 (cuuint64_t)rows * heads * D * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+             const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }  // 0.1.0
+
+const char *fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case FA_ERR_BAD_SEQLENS: return "cu_seqlens inconsistent with Sq / Sk";
+    default: return "unknown status";
+  }
+}
+
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+           int Hkv, int Sq, int Sk, int D, float scale, int causal,
+           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, fa_stream_t stream,
+           int dtype) {
+  // ---------------------------------------------------------- argument checks
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  const bool varlen = cu_seqlens_q != nullptr;
+  if (varlen != (cu_seqlens_k != nullptr)) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || Sq == 0) return FA_OK;  // no query rows
+  if (!q || !o) return FA_ERR_INVALID_ARG;
+  if (Sk > 0 && (!k || !v)) return FA_ERR_INVALID_ARG;  // k / v unused when there are no keys
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;
+  if (varlen && ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) ||
+                 (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u)))
+    return FA_ERR_INVALID_ARG;
+
+  const int group = Hq / Hkv;
+  const bool pair_heads = (group % 2) == 0;
+  const int head_units = pair_heads ? Hq / 2 : Hq;
+  const int rows_per_unit = pair_heads ? fa::kBlockM : 2 * fa::kBlockM;
+  const int64_t row_units = (Sq + rows_per_unit - 1) / rows_per_unit;
+  const int64_t grid = varlen ? (row_units + B) * head_units : row_units * B * head_units;
+  if (grid <= 0 || grid > 0x7fffffffll) return FA_ERR_UNSUPPORTED;
+
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
+  int *status = status_ptr(device);
+  if (!status) return FA_ERR_CUDA;
+
+  fa::LaunchArgs a;
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  const int64_t q_rows = Sq, k_rows = Sk;
+  const int64_t q_batch = varlen ? 1 : B, k_batch = varlen ? 1 : B;
+  if (!make_map(&a.tm_q, q, bf16, D, Hq, q_rows, q_batch)) return FA_ERR_CUDA;
+  if (Sk > 0) {
+    if (!make_map(&a.tm_k, k, bf16, D, Hkv, k_rows, k_batch)) return FA_ERR_CUDA;
+    if (!make_map(&a.tm_v, v, bf16, D, Hkv, k_rows, k_batch)) return FA_ERR_CUDA;
+  } else {
+    a.tm_k = a.tm_q;  // never read: no query tile visits a key tile
+    a.tm_v = a.tm_q;
+  }
+  fa::FwdParams &p = a.p;
+  p.o = o;
+  p.lse = lse;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.group = group;
+  p.pair_heads = pair_heads ? 1 : 0;
+  p.head_units = head_units;
+  p.rows_per_unit = rows_per_unit;
+  p.dense_row_units = (int)row_units;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.threshold = 8.0f;
+  p.wait_limit = kDefaultWaitLimit;
+  p.status = status;
+  a.grid = (int)grid;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  a.device = device;
+
+  cudaError_t e;
+  if (D == 64)
+    e = bf16 ? fa::launch_d64_bf16(a, causal, varlen) : fa::launch_d64_fp16(a, causal, varlen);
+  else
+    e = bf16 ? fa::launch_d128_bf16(a, causal, varlen) : fa::launch_d128_fp16(a, causal, varlen);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_get_device_error(fa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
+  int *status = status_ptr(device);
+  if (!status) return FA_ERR_CUDA;
+  int value = 0;
+  if (cudaMemcpy(&value, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (value != 0 && cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  return value;
+}
+
+int fa_debug_wait_timeout(long long limit_cycles, fa_stream_t stream) {
+  if (limit_cycles < 1 || limit_cycles > (1ll << 34)) return FA_ERR_INVALID_ARG;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
+  int *status = status_ptr(device);
+  if (!status) return FA_ERR_CUDA;
+  fa::fa_wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_cycles,
+                                                                                   status);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

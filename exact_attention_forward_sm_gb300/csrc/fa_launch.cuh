@@ -1,0 +1,51 @@
+// Host-side launcher for one instantiation of the attention kernel.
+#pragma once
+
+#include <atomic>
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+struct LaunchArgs {
+  CUtensorMap tm_q, tm_k, tm_v;
+  FwdParams p;
+  int grid;
+  cudaStream_t stream;
+  int device;
+};
+
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
+cudaError_t launch_fwd(const LaunchArgs &a) {
+  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN>;
+  // opt in to the large dynamic shared memory once per device
+  static std::atomic<unsigned long long> configured{0};
+  const unsigned long long bit = 1ull << (a.device & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Smem<D>::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  kern<<<a.grid, kThreads, Smem<D>::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
+  return cudaGetLastError();
+}
+
+// One translation unit per (head dim, dtype) instantiates the four
+// (causal, packed) variants.
+#define FA_DEFINE_LAUNCHER(NAME, D, BF16)                                       \
+  cudaError_t NAME(const LaunchArgs &a, bool causal, bool varlen) {            \
+    if (causal) {                                                               \
+      return varlen ? launch_fwd<D, BF16, true, true>(a)                        \
+                    : launch_fwd<D, BF16, true, false>(a);                      \
+    }                                                                           \
+    return varlen ? launch_fwd<D, BF16, false, true>(a)                         \
+                  : launch_fwd<D, BF16, false, false>(a);                       \
+  }
+
+cudaError_t launch_d64_fp16(const LaunchArgs &a, bool causal, bool varlen);
+cudaError_t launch_d64_bf16(const LaunchArgs &a, bool causal, bool varlen);
+cudaError_t launch_d128_fp16(const LaunchArgs &a, bool causal, bool varlen);
+cudaError_t launch_d128_bf16(const LaunchArgs &a, bool causal, bool varlen);
+
+}  // namespace fa

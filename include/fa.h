@@ -1,0 +1,125 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) exact attention forward library, libfa.so.
+ *
+ * The library computes, for every query row i of every (sequence b, query head
+ * h), the exact softmax attention over the keys visible to that row:
+ *
+ *     s_ij  = scale * <q_i, k_j>
+ *     O_i   = sum_j softmax(s_i)_j * v_j
+ *     LSE_i = ln sum_j exp(s_ij)
+ *
+ * in one fused pass that streams K/V tiles through an online softmax with the
+ * lazy rescale of the flash-attention fork's v1.7 release notes, section 1.2:
+ * the running O and row_sum are rescaled only when the row max rises by more
+ * than 8 log2 units, and on a skipped rescale the max stays at its previous
+ * value ("max lagging"), so O, row_sum and P share one base and the result is
+ * exact.  The upstream forward API it mirrors (flash_attn_func /
+ * flash_attn_varlen_func with causal masking and grouped K/V heads) is listed
+ * in the same notes, section 4.1; LSE is the [B, H, S] fp32 output of section
+ * 4.6 (natural log).
+ *
+ * Every call is asynchronous on the given CUDA stream, allocates no device or
+ * host memory, and is deterministic: two calls on the same inputs give
+ * bit-identical O and LSE.
+ *
+ * All pointers are DEVICE pointers unless stated otherwise; the caller owns
+ * every buffer.  A stream of NULL means the legacy default stream.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t from cuda_runtime.h. */
+typedef struct CUstream_st *fa_stream_t;
+
+/* Status codes returned by the calls below. */
+enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* a size, pointer, flag or alignment is invalid; nothing launched */
+  FA_ERR_UNSUPPORTED = 2,  /* valid but not built (e.g. head dim other than 64 / 128)      */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime / driver call failed (no device, launch error) */
+  FA_ERR_TIMEOUT = 4,      /* device: a pipeline wait exceeded its limit; outputs invalid    */
+  FA_ERR_BAD_SEQLENS = 5   /* device: cu_seqlens not monotone or beyond Sq / Sk; rows skipped */
+};
+
+/* Element type of q, k, v and o. */
+enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 };
+
+/*
+ * fa_fwd — exact attention forward (O and LSE).
+ *
+ * Layouts (row-major, contiguous, element type `dtype`):
+ *   dense  (cu_seqlens_q == cu_seqlens_k == NULL):
+ *     q, o  [B, Sq, Hq, D]     k, v  [B, Sk, Hkv, D]     lse [B, Hq, Sq] fp32
+ *   packed variable-length (both cu_seqlens non-NULL):
+ *     q, o  [Sq, Hq, D]        k, v  [Sk, Hkv, D]        lse [Hq, Sq]   fp32
+ *     where Sq / Sk are the packed row counts (total query / key tokens) and
+ *     cu_seqlens_q / cu_seqlens_k are int32 device arrays of B + 1 prefix
+ *     offsets: sequence b owns q rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) and
+ *     k/v rows [cu_seqlens_k[b], cu_seqlens_k[b+1]).  Rows of q/o that belong
+ *     to no sequence are neither read for any output nor written.  Every k/v row
+ *     inside [0, Sk) must hold finite values (a tile of one sequence may read
+ *     the first rows of the next one; those keys are masked, their values are
+ *     multiplied by an exact zero weight).
+ *
+ * Arguments:
+ *   q, k, v     inputs (16-byte aligned); k and v may be NULL when Sk == 0.
+ *   o           output, same layout as q (16-byte aligned).
+ *   lse         output log-sum-exp in natural-log units over the scaled scores,
+ *               or NULL to skip it.  A row with no visible key gets O = 0 and
+ *               LSE = -inf.
+ *   B           batch size (dense) or number of sequences (packed); B = 0 is a
+ *               no-op.
+ *   Hq, Hkv     query / key-value heads; Hq % Hkv == 0 (grouped-query
+ *               attention: query head h reads K/V head h / (Hq / Hkv)).
+ *   Sq, Sk      sequence lengths (dense) or packed totals (packed), >= 0.
+ *   D           head dimension: 64 or 128.
+ *   scale       score scale (commonly 1 / sqrt(D)); finite and > 0.
+ *   causal      0 or 1.  With causal = 1 key j is visible to query i iff
+ *               j <= i + (Lk - Lq) (diagonal aligned to the bottom-right; for
+ *               Lq == Lk this is j <= i).
+ *   stream      CUDA stream the work is queued on.
+ *   dtype       FA_DTYPE_FP16 or FA_DTYPE_BF16.
+ *
+ * Returns FA_OK once the kernel is queued, or FA_ERR_INVALID_ARG /
+ * FA_ERR_UNSUPPORTED (nothing queued) / FA_ERR_CUDA.  Errors found on the
+ * device (FA_ERR_TIMEOUT, FA_ERR_BAD_SEQLENS) are recorded in a per-device
+ * status word read by fa_get_device_error().
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
+           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+           fa_stream_t stream, int dtype);
+
+/*
+ * fa_get_device_error — synchronize `stream`, then return and clear the status
+ * word that kernels on the current device set on a device-side error
+ * (FA_OK if none).  Returns FA_ERR_CUDA if the synchronization itself fails.
+ */
+int fa_get_device_error(fa_stream_t stream);
+
+/*
+ * fa_debug_wait_timeout — self-test of the bounded pipeline waits.  Launches
+ * one block that waits on a shared-memory barrier nothing will ever arrive on,
+ * with a wait limit of `limit_cycles` SM clock cycles (1 .. 2^34).  The wait
+ * gives up, records FA_ERR_TIMEOUT in the device status word and the kernel
+ * returns normally; the context stays usable.  Returns the launch status.
+ */
+int fa_debug_wait_timeout(long long limit_cycles, fa_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *fa_status_string(int status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

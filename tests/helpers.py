@@ -33,5 +33,6 @@ def lse_max_abs(lse, ref):
     lse = np.asarray(lse, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     both_inf = np.isneginf(lse) & np.isneginf(ref)
-    d = np.where(both_inf, 0.0, np.abs(lse - ref))
+    with np.errstate(invalid="ignore"):
+        d = np.where(both_inf, 0.0, np.abs(lse - ref))
     return float(np.max(d)) if d.size else 0.0

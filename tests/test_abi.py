@@ -1,0 +1,92 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+libfa.so must load on a machine without a GPU, export every function that
+include/fa.h declares, and reject invalid arguments before touching CUDA.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_forward_sm_gb300 as fa
+from exact_attention_forward_sm_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return fa.load_library()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_exports():
+    assert _declared_functions() == sorted(fa.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert fa.fa_version() >= 100
+    for code in range(6):
+        assert fa.fa_status_string(code) not in ("", "unknown status")
+    assert fa.fa_status_string(99) == "unknown status"
+
+
+def _call(**kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=None, B=1, Hq=2, Hkv=2, Sq=8, Sk=8, D=64,
+                scale=0.125, causal=0, cu_seqlens_q=None, cu_seqlens_k=None, stream=None,
+                dtype=fa.FA_DTYPE_BF16)
+    args.update(kw)
+    return fa.fa_fwd(**args)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(B=-1), dict(Hq=0), dict(Hkv=0), dict(Hq=3, Hkv=2), dict(Sq=-1), dict(Sk=-5),
+    dict(D=0), dict(causal=2), dict(dtype=7), dict(scale=0.0), dict(scale=float("nan")),
+    dict(scale=float("inf")), dict(cu_seqlens_q=64), dict(q=0), dict(o=0),
+    dict(q=8), dict(v=24), dict(lse=2),
+])
+def test_invalid_arguments_rejected_without_launch(lib, bad):
+    assert _call(**bad) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("D", [32, 96, 256])
+def test_unbuilt_head_dims_unsupported(lib, D):
+    assert _call(D=D) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_k_v_may_be_null_only_without_keys(lib):
+    assert _call(k=0, v=0, Sk=4) == fa.FA_ERR_INVALID_ARG
+
+
+def test_empty_problems_are_noops(lib):
+    assert _call(B=0) == fa.FA_OK
+    assert _call(Sq=0) == fa.FA_OK
+
+
+def test_binding_raises_when_library_missing(tmp_path, monkeypatch):
+    monkeypatch.setattr(fa, "_lib", None)
+    monkeypatch.setattr(fa, "library_path", lambda: str(tmp_path / "libfa.so"))
+    with pytest.raises(fa.LibraryMissing):
+        fa.load_library()
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "exact_attention_forward_sm_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in src and "oracle." not in src.replace(
+                    "the oracle", ""), f

@@ -1,0 +1,198 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small shapes are compared row by row over every output (several tiles plus a
+ragged tail); the five named workloads run at full size in the launch
+configuration the benchmark times, with a spread of sampled rows checked
+against the oracle.  Gates: O rel_Linf <= 2e-2 (fp16) / 1e-2 (bf16), cosine
+>= 0.9995, LSE max abs error <= 1e-3.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines too
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import exact_attention_forward_sm_gb300 as fa  # noqa: E402
+from exact_attention_forward_sm_gb300 import workloads as wl  # noqa: E402
+from tests.gpu_util import check, run_gpu, sample_rows, to_device  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from exact_attention_forward_sm_gb300 import _build
+    _build.build()
+    fa.load_library()
+
+
+# ------------------------------------------------------------- small shapes
+
+SMALL = [
+    # B, Hq, Hkv, S, D, dtype, causal
+    (1, 1, 1, 128, 64, "fp16", False),
+    (1, 1, 1, 128, 128, "bf16", False),
+    (1, 2, 2, 256, 128, "bf16", True),
+    (2, 4, 4, 300, 64, "fp16", True),
+    (1, 4, 2, 129, 128, "bf16", True),    # GQA 2:1, ragged tail
+    (1, 8, 2, 513, 128, "bf16", True),    # GQA 4:1
+    (2, 6, 2, 200, 64, "fp16", False),    # odd group (3:1)
+    (1, 4, 1, 385, 64, "bf16", True),     # MQA
+    (1, 2, 2, 1, 128, "bf16", True),      # S = 1
+    (1, 2, 2, 2, 64, "fp16", False),      # S = 2
+    (1, 1, 1, 127, 128, "fp16", True),
+    (3, 3, 3, 640, 128, "fp16", False),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "b{}_hq{}_hkv{}_s{}_d{}_{}_{}".format(
+    *s[:6], "causal" if s[6] else "full"))
+def test_small_shapes_all_rows(shape):
+    B, Hq, Hkv, S, D, dtype, causal = shape
+    case = wl.make_case(B, Hq, Hkv, S, S, D, dtype, causal, seed=hash(shape) % 1000)
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag=str(shape))
+
+
+@pytest.mark.parametrize("sq,sk", [(100, 300), (300, 100), (128, 512), (257, 129)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_unequal_lengths(sq, sk, causal):
+    case = wl.make_case(2, 4, 2, sq, sk, 128, "bf16", causal, seed=sq + sk)
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag=f"sq{sq}_sk{sk}")
+
+
+def test_rising_bias_small_exercises_rescale():
+    case = wl.make_case(1, 4, 1, 1024, 1024, 128, "bf16", True, seed=31, rising_bias=True)
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag="rising_bias")
+
+
+def test_sigma2_scores():
+    case = wl.make_case(1, 2, 2, 700, 700, 128, "bf16", False, seed=32, sigma=math.sqrt(2.0))
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag="sigma2")
+
+
+@pytest.mark.parametrize("D,dtype", [(64, "fp16"), (128, "bf16")])
+def test_packed_sequences(D, dtype):
+    lens = [1, 5, 127, 128, 129, 300, 64, 700]
+    case = wl.make_case(0, 4, 4, 0, 0, D, dtype, True, seed=33, seqlens_q=lens)
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag="varlen")
+
+
+def test_packed_gqa_unequal_lengths_noncausal():
+    case = wl.make_case(0, 8, 2, 0, 0, 128, "bf16", False, seed=34,
+                        seqlens_q=[17, 300, 1, 129], seqlens_k=[200, 5, 300, 129])
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag="varlen_gqa")
+
+
+# ----------------------------------------------------------- named workloads
+
+@pytest.mark.parametrize("idx", range(len(wl.WORKLOADS)), ids=[w.name for w in wl.WORKLOADS])
+def test_named_workload_full_size(idx):
+    w = wl.WORKLOADS[idx]
+    case = wl.make_workload(w)
+    o, lse = run_gpu(case)
+    if case.lse_rows() <= 300_000 and case.Sq <= 4096 and w.D * case.lse_rows() < 2e8 \
+            and idx <= 1:
+        check(case, o, lse, tag=w.name)  # every row
+    else:
+        heads = range(case.Hq) if case.Hq <= 8 else [0, 1, case.Hq // 2, case.Hq - 1]
+        rows = sample_rows(case, per_head=96, heads=heads, seed=idx)
+        check(case, o, lse, rows=rows, tag=w.name)
+
+
+# ---------------------------------------------------------- properties / edges
+
+def test_deterministic_bit_identical():
+    case = wl.make_case(2, 8, 2, 777, 777, 128, "bf16", True, seed=40)
+    o1, l1 = run_gpu(case)
+    o2, l2 = run_gpu(case)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_null_lse_pointer():
+    case = wl.make_case(1, 2, 2, 256, 256, 64, "fp16", True, seed=41)
+    o, _ = run_gpu(case, with_lse=False)
+    o2, lse = run_gpu(case)
+    assert torch.equal(o, o2)
+
+
+def test_no_keys_gives_zero_and_neg_inf():
+    case = wl.make_case(1, 2, 2, 100, 0, 64, "bf16", False, seed=42)
+    o, lse = run_gpu(case)
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_rows_without_visible_keys():
+    # causal with Sq > Sk: the first Sq - Sk rows see no key
+    case = wl.make_case(1, 2, 2, 300, 100, 128, "bf16", True, seed=43)
+    o, lse = run_gpu(case)
+    assert torch.all(o[:, :200] == 0) and torch.all(torch.isneginf(lse[:, :, :200]))
+    check(case, o, lse, tag="masked_rows")
+
+
+def test_nan_canary_outside_tensors_and_sequences():
+    """Memory past every tensor and rows of no sequence hold NaN; outputs of the
+    sequences stay exact and rows of no sequence are not written."""
+    lens = [100, 250, 129]
+    case = wl.make_case(0, 2, 2, 0, 0, 128, "fp16", True, seed=44, seqlens_q=lens)
+    dev = "cuda:0"
+    pad = 4096
+    tot = case.Sq
+    gap = 37  # rows after the last sequence that belong to no sequence
+    def padded(t, rows):
+        buf = torch.full((rows + gap) * t[0].numel() + pad, float("nan"), dtype=t.dtype,
+                         device=dev)
+        view = buf[: (rows + gap) * t[0].numel()].view(rows + gap, *t.shape[1:])
+        view[:rows] = t.to(dev)
+        return view
+    q = padded(case.q, tot)
+    k = padded(case.k, tot)
+    v = padded(case.v, tot)
+    o = torch.full_like(q, 7.0)
+    lse = torch.full((2, tot + gap), 7.0, dtype=torch.float32, device=dev)
+    cu = case.cu_seqlens_q.to(dev)
+    st = fa.fa_fwd(q, k, v, o, lse, 3, 2, 2, tot + gap, tot, 128, case.scale, 1, cu, cu,
+                   torch.cuda.current_stream(), fa.FA_DTYPE_FP16)
+    assert st == fa.FA_OK
+    assert fa.fa_get_device_error() == fa.FA_OK
+    assert torch.all(o[tot:] == 7.0) and torch.all(lse[:, tot:] == 7.0)
+    check(case, o[:tot].contiguous(), lse[:, :tot].contiguous(), tag="canary")
+
+
+def test_bad_seqlens_reported_and_context_survives():
+    case = wl.make_case(0, 2, 2, 0, 0, 64, "fp16", False, seed=45, seqlens_q=[64, 64])
+    q, k, v, cu_q, cu_k = to_device(case)
+    bad = torch.tensor([0, 64, 999], dtype=torch.int32, device="cuda:0")
+    o = torch.empty_like(q)
+    st = fa.fa_fwd(q, k, v, o, None, 2, 2, 2, case.Sq, case.Sk, 64, case.scale, 0, bad, cu_k,
+                   torch.cuda.current_stream(), fa.FA_DTYPE_FP16)
+    assert st == fa.FA_OK
+    assert fa.fa_get_device_error() == fa.FA_ERR_BAD_SEQLENS
+    o2, lse2 = run_gpu(case)
+    check(case, o2, lse2, tag="after_bad_seqlens")
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    assert fa.fa_debug_wait_timeout(200_000) == fa.FA_OK
+    assert fa.fa_get_device_error() == fa.FA_ERR_TIMEOUT
+    assert fa.fa_get_device_error() == fa.FA_OK  # cleared
+    case = wl.make_case(1, 2, 2, 200, 200, 128, "bf16", True, seed=46)
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag="after_timeout")
+
+
+def test_side_stream():
+    s = torch.cuda.Stream()
+    case = wl.make_case(1, 4, 4, 512, 512, 64, "bf16", True, seed=47)
+    with torch.cuda.stream(s):
+        o, lse = run_gpu(case, stream=s)
+    s.synchronize()
+    check(case, o, lse, tag="side_stream")
