@@ -1,0 +1,434 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact attention forward pass on GB300.
+
+One step = one fa_fwd launch over the whole workload (every query row of every
+head), inputs resident in HBM, L2 flushed (256 MiB write) before each step.
+Prints ONE JSON line (rank 0):
+
+  value     attention TFLOP/s over all ranks (4 * D * Hq * visible pairs per
+            step; the two contractions QK^T and PV), kernel time from CUDA
+            events on the launching stream, max over ranks;
+  roofline  the kernel against the measured dense bf16 tensor peak;
+  e2e       the same metric through the public API with the inputs copied
+            from pinned host memory and O / LSE copied back inside each step;
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload.
+
+``--impl reference`` times the oracle itself (host cores) as the reference arm.
+Under torchrun each rank runs its own copy of the workload (independent
+problems, no collective on the data path): weak scaling.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_attention_forward_sm_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (1×GB300) and % of dense bf16/fp16 tensor-core peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = wl.WORKLOADS[1].name   # hdim-128 bf16 causal, B4 H16 S2048
+L2_FLUSH_BYTES = 256 << 20
+PEAK_FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+KERNEL_SOURCES = ["fa_fwd_kernel.cuh", "fa_ptx.cuh", "fa_launch.cuh"]
+
+
+# --------------------------------------------------------------- host helpers
+
+def dist_env():
+    """(rank, local_rank, world) from the torchrun environment (1 GPU default)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def rank_seed(base_seed, rank):
+    """Each rank draws its own independent problem of the same shape."""
+    return int(base_seed) + 7919 * int(rank)
+
+
+def max_over_ranks(value, world):
+    """Max of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(PEAK_FALLBACK), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "exact_attention_forward_sm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"fa_fwd_kernel_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return int(float(fields["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fa_bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for name, flag in zip(names, parts[5:9]):
+                    if flag.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons)}
+        loaded = [x for x in sm if x >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(case, seconds, seed=0):
+    """Time the fp64 oracle on a sample of rows sized to about `seconds` of work.
+
+    Rows are drawn uniformly over every (sequence, head, row), so the sample has
+    the workload's mix of causal row lengths; FLOPs are counted exactly for the
+    sampled rows (4 * D per visible key)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    n_rows = case.lse_rows()
+    vis = _visible_per_row(case)
+    # convert the 16-bit inputs once; the conversion is not timed
+    q, k, v = (t.float().numpy() for t in (case.q, case.k, case.v))
+    threads = len(os.sched_getaffinity(0))
+
+    def run(rows):
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D,
+                         case.scale, case.causal, case.cu_seqlens_q, case.cu_seqlens_k,
+                         rows=rows, nthreads=threads)
+        return time.perf_counter() - t0, 4.0 * case.D * float(vis[rows].sum())
+
+    calib = np.sort(rng.choice(n_rows, size=min(n_rows, 256), replace=False))
+    dt, fl = run(calib)
+    rate = fl / max(dt, 1e-6)
+    want = int(min(n_rows, max(256, seconds * rate / max(fl / len(calib), 1.0))))
+    rows = np.sort(rng.choice(n_rows, size=want, replace=False))
+    dt, fl = run(rows)
+    return {"tflops": fl / dt / 1e12, "seconds": dt, "rows": int(len(rows)),
+            "rows_total": int(n_rows), "flops": fl, "threads": threads}
+
+
+def _visible_per_row(case):
+    """Visible keys of every row in LSE-index order."""
+    out = []
+    lens = case.seq_lengths()
+    if case.varlen:
+        for _h in range(case.Hq):
+            for lq, lk in lens:
+                out.append(_vis_rows(lq, lk, case.causal))
+    else:
+        for lq, lk in lens:
+            for _h in range(case.Hq):
+                out.append(_vis_rows(lq, lk, case.causal))
+    return np.concatenate(out) if out else np.zeros(0)
+
+
+def _vis_rows(lq, lk, causal):
+    i = np.arange(lq, dtype=np.int64)
+    if not causal:
+        return np.full(lq, lk, dtype=np.int64)
+    return np.clip(i + lk - lq + 1, 0, lk)
+
+
+# --------------------------------------------------------------- GPU benchmark
+
+def run_gpu_arm(args, rank, local_rank, world):
+    import exact_attention_forward_sm_gb300 as fa
+    from exact_attention_forward_sm_gb300 import _build
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    _build.build()
+    fa.load_library()
+    w = wl.BY_NAME[args.workload]
+    w_rank = wl.Workload(**{**w.__dict__, "seed": rank_seed(w.seed, rank)})
+    case = wl.make_workload(w_rank)
+    flops = wl.attention_flops(case)
+    dtype_code = wl.DTYPE_CODE[case.dtype]
+    stream = torch.cuda.current_stream(dev)
+
+    q, k, v = (t.to(dev) for t in (case.q, case.k, case.v))
+    cu_q = case.cu_seqlens_q.to(dev) if case.varlen else None
+    cu_k = case.cu_seqlens_k.to(dev) if case.varlen else None
+    o = torch.empty_like(q)
+    lse_shape = (case.Hq, case.Sq) if case.varlen else (case.B, case.Hq, case.Sq)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def launch(qq, kk, vv, oo, ll):
+        st = fa.fa_fwd(qq, kk, vv, oo, ll, case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D,
+                       case.scale, int(case.causal), cu_q, cu_k, stream, dtype_code)
+        if st != fa.FA_OK:
+            raise RuntimeError(f"fa_fwd: {fa.fa_status_string(st)}")
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        launch(q, k, v, o, lse)
+    torch.cuda.synchronize()
+    status = fa.fa_get_device_error(stream)
+    if status != fa.FA_OK:
+        raise RuntimeError(f"device status after warm-up: {fa.fa_status_string(status)}")
+
+    # ------------------------------------------------ timed region: kernel only
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))             # evict L2 (outside the kernel's events)
+            starts[i].record(stream)
+            launch(q, k, v, o, lse)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall
+    barrier(world)
+    status = fa.fa_get_device_error(stream)
+    if status != fa.FA_OK:
+        raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(status)}")
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = statistics.mean(times_ms)
+    kernel_ms_max = max_over_ranks(kernel_ms, world)
+    clock = clocks.summary()
+
+    # -------------------------------------- end to end through the public API
+    h_q, h_k, h_v = (t.pin_memory() for t in (case.q, case.k, case.v))
+    h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h_l = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
+    d2h = h_o.numel() * h_o.element_size() + h_l.numel() * h_l.element_size()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup + args.steps):
+        if i == args.warmup:
+            torch.cuda.synchronize()
+            barrier(world)
+            e_start.record(stream)
+        q.copy_(h_q, non_blocking=True)
+        k.copy_(h_k, non_blocking=True)
+        v.copy_(h_v, non_blocking=True)
+        launch(q, k, v, o, lse)
+        h_o.copy_(o, non_blocking=True)
+        h_l.copy_(lse, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, world)
+    barrier(world)
+
+    peaks, peak_src = load_peaks()
+    dense_key = "bf16_tflops"
+    peak = float(peaks.get(dense_key, PEAK_FALLBACK[dense_key]))
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(world * flops / (kernel_ms_max * 1e-3) / 1e12, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(kernel_ms_max, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": case.dtype,
+        "data": "synthetic (seeded N(0, sigma^2) draws cast to 16-bit; no dataset)",
+        "config": {
+            "workload": w.name, "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv,
+            "Sq": case.Sq, "Sk": case.Sk, "D": case.D, "causal": case.causal,
+            "varlen": case.varlen, "flops_per_step_per_gpu": flops,
+            "l2": "flushed before every step (256 MiB write, outside the kernel events)",
+            "parallelism": f"replicas x{world} (independent problems, no collective)",
+            "wall_ms_per_step_incl_flush": round(wall * 1e3 / args.steps, 4),
+        },
+        "roofline": {
+            "bound": "tensor",
+            "achieved": round(achieved, 3),
+            "peak": peak,
+            "unit": UNIT,
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(w.name),
+            "peak_source": f"{peak_src} {dense_key} (burst, cuBLAS bf16)",
+            "kernel": "fa_fwd_kernel",
+            "kernel_ms_mean": round(kernel_ms, 5),
+            "kernel_ms_min": round(min(times_ms), 5),
+        },
+        "e2e": {
+            "value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3),
+            "unit": UNIT,
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_ms, 4),
+        },
+        "gpu_launches": args.steps,
+        "clocks": clock,
+    }
+    if "bf16_tflops_sustained" in peaks:
+        line["roofline"]["frac_of_sustained"] = round(
+            achieved / float(peaks["bf16_tflops_sustained"]), 4)
+    return line, case
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference_arm(args):
+    """The fp64 oracle as the reference arm: each step times a bounded sample."""
+    w = wl.BY_NAME[args.workload]
+    case = wl.make_workload(w)
+    per_step = max(0.5, min(8.0, args.reference_budget_s / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        oracle_sample(case, per_step, seed=1000 + i)
+    results = [oracle_sample(case, per_step, seed=i) for i in range(args.steps)]
+    fl = sum(r["flops"] for r in results)
+    secs = sum(r["seconds"] for r in results)
+    value = fl / secs / 1e12
+    rows = results[0]["rows"]
+    sample = (f"{rows} of {results[0]['rows_total']} query rows per step, drawn uniformly "
+              f"(workload {w.name}); TFLOP/s = 4*D*visible keys of the sampled rows / time")
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded inputs as the CUDA arm)", "impl": "reference",
+        "config": {"workload": w.name, "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv,
+                   "Sq": case.Sq, "Sk": case.Sk, "D": case.D, "causal": case.causal,
+                   "varlen": case.varlen},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": results[0]["threads"],
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.BY_NAME))
+    ap.add_argument("--cpu-baseline-s", type=float, default=12.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--reference-budget-s", type=float, default=90.0,
+                    help="total oracle seconds for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, local_rank, world = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference_arm(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line, case = run_gpu_arm(args, rank, local_rank, world)
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = oracle_sample(case, args.cpu_baseline_s, seed=12345)
+        line["cpu_baseline"] = {
+            "value": cb["tflops"], "unit": UNIT, "cores": cb["threads"], "kind": "oracle",
+            "sample": (f"{cb['rows']} of {cb['rows_total']} query rows drawn uniformly from "
+                       f"the same workload ({cb['seconds']:.1f} s of fp64 work)")}
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

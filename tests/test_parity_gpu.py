@@ -104,7 +104,7 @@ def test_named_workload_full_size(idx):
         check(case, o, lse, tag=w.name)  # every row
     else:
         heads = range(case.Hq) if case.Hq <= 8 else [0, 1, case.Hq // 2, case.Hq - 1]
-        rows = sample_rows(case, per_head=96, heads=heads, seed=idx)
+        rows = sample_rows(case, per_head=512, heads=heads, seed=idx)
         check(case, o, lse, rows=rows, tag=w.name)
 
 
@@ -148,7 +148,7 @@ def test_nan_canary_outside_tensors_and_sequences():
     tot = case.Sq
     gap = 37  # rows after the last sequence that belong to no sequence
     def padded(t, rows):
-        buf = torch.full((rows + gap) * t[0].numel() + pad, float("nan"), dtype=t.dtype,
+        buf = torch.full(((rows + gap) * t[0].numel() + pad,), float("nan"), dtype=t.dtype,
                          device=dev)
         view = buf[: (rows + gap) * t[0].numel()].view(rows + gap, *t.shape[1:])
         view[:rows] = t.to(dev)
