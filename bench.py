@@ -223,7 +223,8 @@ def run_gpu_arm(args, rank, local_rank, world):
 
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
-    _build.build()
+    if not os.environ.get("FA_AB_NOBUILD"):
+        _build.build(variant=args.variant)
     fa.load_library()
     w = wl.BY_NAME[args.workload]
     w_rank = wl.Workload(**{**w.__dict__, "seed": rank_seed(w.seed, rank)})
@@ -325,6 +326,7 @@ def run_gpu_arm(args, rank, local_rank, world):
             "l2": "flushed before every step (256 MiB write, outside the kernel events)",
             "parallelism": f"replicas x{world} (independent problems, no collective)",
             "wall_ms_per_step_incl_flush": round(wall * 1e3 / args.steps, 4),
+            **({"ablation_variant": args.variant} if args.variant else {}),
         },
         "roofline": {
             "bound": "tensor",
@@ -401,7 +403,11 @@ def main():
     ap.add_argument("--reference-budget-s", type=float, default=90.0,
                     help="total oracle seconds for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", choices=["unfused", "threshold0"], default=None,
+                    help="time an ablation build instead of the product library")
     args = ap.parse_args()
+    if args.variant:
+        os.environ["FA_LIB_VARIANT"] = args.variant
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, local_rank, world = dist_env()

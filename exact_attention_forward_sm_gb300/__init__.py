@@ -20,6 +20,7 @@ __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
     "FA_ERR_BAD_SEQLENS", "FA_DTYPE_FP16", "FA_DTYPE_BF16", "LibraryMissing", "FaError",
     "library_path", "load_library", "fa_fwd", "fa_get_device_error", "fa_debug_wait_timeout",
+    "fa_debug_trace_read",
     "fa_status_string", "fa_version", "attention_forward", "EXPORTED_SYMBOLS",
 ]
 
@@ -33,7 +34,7 @@ FA_DTYPE_FP16 = 0
 FA_DTYPE_BF16 = 1
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_get_device_error", "fa_debug_wait_timeout",
-                    "fa_status_string", "fa_version")
+                    "fa_debug_trace_read", "fa_status_string", "fa_version")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -51,7 +52,10 @@ class FaError(RuntimeError):
 
 
 def library_path() -> str:
-    return os.path.join(_HERE, "libfa.so")
+    """In-tree libfa.so, or an ablation / debug build named by FA_LIB_VARIANT
+    ("unfused", "threshold0", "trace")."""
+    variant = os.environ.get("FA_LIB_VARIANT")
+    return os.path.join(_HERE, f"libfa_{variant}.so" if variant else "libfa.so")
 
 
 def load_library():
@@ -74,6 +78,8 @@ def load_library():
         lib.fa_get_device_error.restype = i32
         lib.fa_debug_wait_timeout.argtypes = [ctypes.c_longlong, vp]
         lib.fa_debug_wait_timeout.restype = i32
+        lib.fa_debug_trace_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i32]
+        lib.fa_debug_trace_read.restype = i32
         lib.fa_status_string.argtypes = [i32]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_version.argtypes = []
@@ -114,6 +120,13 @@ def fa_get_device_error(stream=None) -> int:
 
 def fa_debug_wait_timeout(limit_cycles, stream=None) -> int:
     return load_library().fa_debug_wait_timeout(int(limit_cycles), _stream(stream))
+
+
+def fa_debug_trace_read(n=2048):
+    """(status, list of n clock stamps) from a trace build's buffer."""
+    buf = (ctypes.c_ulonglong * n)()
+    st = load_library().fa_debug_trace_read(buf, n)
+    return st, list(buf)
 
 
 def fa_status_string(status) -> str:

@@ -14,6 +14,11 @@
 // Host code only ever uses its device address, fetched per device below.
 __device__ int g_fa_status;
 
+#ifdef FA_TRACE
+// Pipeline trace buffer of trace builds (see FA_TRACE_AT in the kernel).
+__device__ unsigned long long g_fa_trace[fa::kTraceEntries];
+#endif
+
 namespace fa {
 
 // Kernel used only to exercise the bounded wait: nothing arrives on the barrier.
@@ -31,6 +36,12 @@ static __global__ void fa_wait_timeout_kernel(long long limit, int *status) {
 }
 
 }  // namespace fa
+
+// Lazy-rescale threshold in log2 units (8 for 16-bit inputs); a build-time
+// define so the threshold-0 ablation is a separate library.
+#ifndef FA_RESCALE_THRESHOLD
+#define FA_RESCALE_THRESHOLD 8.0f
+#endif
 
 namespace {
 
@@ -59,6 +70,18 @@ EncodeTiledFn encode_fn() {
 
 std::mutex g_status_mu;
 int *g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+// Streaming multiprocessors of `device` (the persistent grid has one CTA each).
+int sm_count(int device) {
+  if (device < 0 || device >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_sm_count[device] &&
+      cudaDeviceGetAttribute(&g_sm_count[device], cudaDevAttrMultiProcessorCount, device) !=
+          cudaSuccess)
+    g_sm_count[device] = 0;
+  return g_sm_count[device];
+}
 
 // Device address of g_fa_status on the current device.
 int *status_ptr(int device) {
@@ -138,19 +161,27 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   const int head_units = pair_heads ? Hq / 2 : Hq;
   const int rows_per_unit = pair_heads ? fa::kBlockM : 2 * fa::kBlockM;
   const int64_t row_units = (Sq + rows_per_unit - 1) / rows_per_unit;
-  const int64_t grid = varlen ? (row_units + B) * head_units : row_units * B * head_units;
-  if (grid <= 0 || grid > 0x7fffffffll) return FA_ERR_UNSUPPORTED;
+  // packed problems: each sequence rounds its row count up once, so this
+  // bounds the number of units; the kernel skips the ones past the last
+  const int64_t units = varlen ? (row_units + B) * head_units : row_units * B * head_units;
+  if (units <= 0 || units > 0x7fffffffll) return FA_ERR_UNSUPPORTED;
 
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
   int *status = status_ptr(device);
-  if (!status) return FA_ERR_CUDA;
+  const int sms = sm_count(device);
+  if (!status || sms <= 0) return FA_ERR_CUDA;
+  // dense: persistent, one CTA per SM walking a snake over the heavy-first
+  // unit order; packed: unit costs follow the sequence lengths, so one CTA per
+  // unit and the hardware's in-order CTA dispatch balances them
+  const int64_t grid = varlen ? units : (units < sms ? units : sms);
 
   fa::LaunchArgs a;
   const bool bf16 = dtype == FA_DTYPE_BF16;
   const int64_t q_rows = Sq, k_rows = Sk;
   const int64_t q_batch = varlen ? 1 : B, k_batch = varlen ? 1 : B;
   if (!make_map(&a.tm_q, q, bf16, D, Hq, q_rows, q_batch)) return FA_ERR_CUDA;
+  if (!make_map(&a.tm_o, o, bf16, D, Hq, q_rows, q_batch)) return FA_ERR_CUDA;
   if (Sk > 0) {
     if (!make_map(&a.tm_k, k, bf16, D, Hkv, k_rows, k_batch)) return FA_ERR_CUDA;
     if (!make_map(&a.tm_v, v, bf16, D, Hkv, k_rows, k_batch)) return FA_ERR_CUDA;
@@ -173,10 +204,19 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   p.head_units = head_units;
   p.rows_per_unit = rows_per_unit;
   p.dense_row_units = (int)row_units;
+  p.total_units = (int)units;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.threshold = 8.0f;
+  p.threshold = FA_RESCALE_THRESHOLD;
   p.wait_limit = kDefaultWaitLimit;
   p.status = status;
+  p.trace = nullptr;
+#ifdef FA_TRACE
+  {
+    void *tr = nullptr;
+    if (cudaGetSymbolAddress(&tr, g_fa_trace) != cudaSuccess) return FA_ERR_CUDA;
+    p.trace = static_cast<unsigned long long *>(tr);
+  }
+#endif
   a.grid = (int)grid;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.device = device;
@@ -201,6 +241,22 @@ int fa_get_device_error(fa_stream_t stream) {
     return FA_ERR_CUDA;
   if (value != 0 && cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
   return value;
+}
+
+int fa_debug_trace_read(unsigned long long *host_out, int n) {
+#ifdef FA_TRACE
+  if (!host_out || n < 0 || n > fa::kTraceEntries) return FA_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(host_out, g_fa_trace, n * sizeof(unsigned long long)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  static const unsigned long long zeros[fa::kTraceEntries] = {};
+  if (cudaMemcpyToSymbol(g_fa_trace, zeros, sizeof(zeros)) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+#else
+  (void)host_out;
+  (void)n;
+  return FA_ERR_UNSUPPORTED;
+#endif
 }
 
 int fa_debug_wait_timeout(long long limit_cycles, fa_stream_t stream) {

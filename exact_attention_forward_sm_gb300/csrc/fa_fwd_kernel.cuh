@@ -1,11 +1,18 @@
-// Fused exact attention forward for sm_103a (GB300): TMA + mbarrier pipeline,
-// tcgen05 MMAs with TMEM accumulators, lazy-rescale online softmax.
+// Fused exact attention forward for sm_103a (GB300): persistent CTAs, TMA +
+// mbarrier pipeline, tcgen05 MMAs with TMEM accumulators, lazy-rescale online
+// softmax.
 //
-// One CTA owns two 128-row query tiles that share every K/V tile it loads:
+// Work unit: two 128-row query tiles that share every K/V tile loaded for them:
 //   * grouped-query attention with an even group size: two query heads of one
 //     K/V head, same rows (GQA head packing: each K/V tile serves both);
 //   * otherwise: query rows [256 r, 256 r + 128) and [256 r + 128, 256 r + 256)
 //     of one head.
+// Units are numbered heaviest first (causal: last row blocks first).  The grid
+// has at most one CTA per SM; CTA b takes units b, 2G-1-b, 2G+b, 4G-1-b, ...
+// (G = grid size): a snake over the heavy-first order, which balances causal
+// problems like a greedy longest-first schedule without any global counter.
+// Barriers, tensor memory and the K/V ring live across units, so one unit's
+// epilogue overlaps the next unit's loads and first Q K^T.
 //
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3   softmax + epilogue for tile 0 (thread = query row = TMEM lane)
@@ -14,19 +21,23 @@
 //   warp  9     lane 0 issues every TMA load
 //   warps 10-11 idle
 // After set-up the third warpgroup gives registers back (setmaxnreg) so the
-// softmax warpgroups can hold a full 128-column score row: 2 x 128 x 208 +
-// 128 x 56 = 60416 <= 384 x 168 registers granted at launch.
+// softmax warpgroups can hold a full 128-column score row: 2 x 128 x 192 +
+// 128 x 96 = 61440 <= 384 x 168 registers granted at launch.
 //
 // Tensor memory (512 columns):  S0 [0,128)  S1 [128,256)  O0 [256,256+D)
 // O1 [256+D, 256+2D).  P_t (16-bit pairs) overwrites columns [0,64) of S_t
 // once the softmax has read S_t into registers, and is the A operand of
 // O_t += P_t V taken straight from tensor memory.
 //
-// Per K/V tile j and query tile t the MMA warp issues, in this order,
+// Per K/V tile j and query tile t the MMA thread issues, in this order,
 //   O_t += P_t(j-1) V(j-1)   then   S_t = Q_t K(j)^T,
-// and the tensor pipe executes one CTA's MMAs in issue order, so the S_t write
-// of step j happens after the P_t read of step j-1 (the same ordering the
-// pages' FA4 Blackwell kernel relies on for its S/P aliasing).
+// alternating tiles, so tile 0's softmax runs while the tensor pipe works on
+// tile 1 and vice versa.  The tensor pipe executes one CTA's MMAs in issue
+// order, so the S_t write of step j happens after the P_t read of step j-1
+// (the same ordering the pages' FA4 Blackwell kernel relies on for its S/P
+// aliasing).  Descriptors are built once and each MMA adds a compile-time
+// offset: the single issuing thread must emit an MMA every ~64 cycles to keep
+// the tensor pipe busy, so the issue stream is kept branch-free.
 //
 // Online softmax (release notes v1.7 section 1.2, v1.2 sections 1-2): row max
 // m in raw score units, scale_log2 = scale * log2(e).  First K/V tile: m = its
@@ -44,6 +55,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "fa_ptx.cuh"
 
@@ -66,13 +78,36 @@ struct FwdParams {
   int group;                // Hq / Hkv
   int pair_heads;           // 1: the two tiles are query heads 2u and 2u+1
   int head_units;           // head slots per sequence: Hq / 2 or Hq
-  int rows_per_unit;        // query rows per CTA and head slot: 128 or 256
+  int rows_per_unit;        // query rows per unit and head slot: 128 or 256
   int dense_row_units;      // dense problems: ceil(Sq / rows_per_unit)
+  int total_units;          // units to process (packed: an upper bound)
   float scale_log2;         // scale * log2(e)
   float threshold;          // lazy-rescale threshold, log2 units
   long long wait_limit;     // bounded-wait limit in SM clock cycles
   int *status;              // device status word (first error wins)
+  unsigned long long *trace;  // clock64 pipeline trace (trace builds only)
 };
+
+// Pipeline trace (compiled in with -DFA_TRACE): CTA 0 records SM clock stamps
+// of the K/V steps of its first unit into a 2048-entry buffer.
+//   softmax tile t, step j < 63:  (t * 64 + j) * 8 + e   e: 0 S ready, 1 S in
+//       registers, 2 max / rescale decided, 3 P stores issued, 4 P ready
+//       signalled; (t * 64 + 63) * 8 + 5 / 6: epilogue start / end
+//   MMA thread, tile t, step j:  1024 + j * 8 + 2 t + e   e: 0 P(j-1) ready,
+//       1 O += P(j-1) V(j-1) and S = Q K(j)^T issued
+//   TMA load idx < 256:           1536 + idx  (issue time)
+//   2047: kernel start
+constexpr int kTraceEntries = 2048;
+#ifdef FA_TRACE
+#define FA_TRACE_AT(cond, idx)                                               \
+  do {                                                                       \
+    if ((cond) && blockIdx.x == 0 && p.trace) p.trace[(idx)] = clock64();    \
+  } while (0)
+#else
+#define FA_TRACE_AT(cond, idx) \
+  do {                         \
+  } while (0)
+#endif
 
 template <int D>
 struct Smem {
@@ -81,11 +116,15 @@ struct Smem {
   static constexpr int kStages = (D == 128) ? 4 : 8;         // K/V ring depth
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKVOff = 2 * kTileBytes;
-  static constexpr uint32_t kBarOff = kKVOff + kStages * kTileBytes;
-  // barriers: q_full[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_ready[2], drain
-  static constexpr int kNumBars = 2 + 2 * kStages + 7;
+  // output staging for the TMA store of the epilogue: 128 rows x 64 columns
+  // (128B-swizzled) per query tile
+  static constexpr uint32_t kStageOff = kKVOff + kStages * kTileBytes;
+  static constexpr uint32_t kBarOff = kStageOff + 2 * kChunkBytes;
+  // barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2],
+  //           p_full[2], o_ready[2], o_free[2], drain
+  static constexpr int kNumBars = 4 + 2 * kStages + 9;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr uint32_t kBytes = kMiscOff + 128;
+  static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
@@ -136,13 +175,20 @@ __device__ __forceinline__ int tile_kv_count(int m0, int lq, int lk) {
   return min(full, last_key / kBlockN + 1);
 }
 
-// Decode this CTA's work unit.  Dense: row-unit index (heaviest causal rows
-// first) is the slowest-varying part of blockIdx.x.  Packed: units are numbered
-// sequence by sequence; warp 0 scans cu_seqlens cooperatively.
+// The i-th unit of this CTA (snake over the heavy-first unit order).
+__device__ __forceinline__ int unit_of(int i) {
+  const int G = gridDim.x;
+  return i * G + ((i & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+}
+
+// Decode work unit `unit`; every lane of the calling warp gets the same record.
+// Dense: the row-unit index (heaviest causal rows first) is the slowest-varying
+// part of the unit index.  Packed: units are numbered sequence by sequence
+// (heaviest rows of a sequence first); the warp scans cu_seqlens cooperatively.
 template <bool CAUSAL, bool VARLEN>
-__device__ void decode_work(const FwdParams &p, Work &w, int lane) {
+__device__ Work decode_work(const FwdParams &p, int unit, int lane) {
+  Work w;
   w.valid = 0;
-  const int unit = blockIdx.x;
   const int hu = unit % p.head_units;
   int b = 0, ru = 0, n_ru = 0;
   if (!VARLEN) {
@@ -150,7 +196,7 @@ __device__ void decode_work(const FwdParams &p, Work &w, int lane) {
     ru = unit / per_ru;
     b = (unit % per_ru) / p.head_units;
     n_ru = p.dense_row_units;
-    if (ru >= n_ru) return;
+    if (ru >= n_ru) return w;
     w.lq = p.Sq;
     w.lk = p.Sk;
     w.q_row0 = 0;
@@ -184,13 +230,13 @@ __device__ void decode_work(const FwdParams &p, Work &w, int lane) {
       }
       base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (found < 0) return;
+    if (found < 0) return w;
     b = found;
     const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
     const int k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
     if (q0 < 0 || q1 < q0 || q1 > p.Sq || k0 < 0 || k1 < k0 || k1 > p.Sk) {
       if (lane == 0) record_status(p.status, 5);
-      return;
+      return w;
     }
     w.lq = q1 - q0;
     w.lk = k1 - k0;
@@ -217,12 +263,55 @@ __device__ void decode_work(const FwdParams &p, Work &w, int lane) {
   w.n_kv[1] = tile_kv_count<CAUSAL>(w.m0[1], w.lq, w.lk);
   w.n_max = max(w.n_kv[0], w.n_kv[1]);
   w.valid = 1;
+  return w;
+}
+
+// 16-bit pair of P values (low half = first key).
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+}
+
+// Max of 32 scores (three-input max tree, depth 4).
+__device__ __forceinline__ float max32(const float *x) {
+  float a[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float *y = x + 8 * q;
+    a[q] = fmax3(fmax3(y[0], y[1], y[2]), fmax3(y[3], y[4], y[5]), fmaxf(y[6], y[7]));
+  }
+  return fmax3(a[0], a[1], fmaxf(a[2], a[3]));
+}
+
+// P for 32 keys: exp2(s * scale_log2 - m * scale_log2) with the subtraction as
+// packed FMAs, summed (fp32, before rounding) into four packed accumulators,
+// rounded to 16-bit pairs and stored as 16 TMEM columns at `p_addr`.
+template <bool BF16>
+__device__ __forceinline__ void softmax_chunk(const float *x, float scale_log2, float ms,
+                                              float2 (&acc)[4], uint32_t p_addr) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float y0, y1;
+    fma_f32x2(y0, y1, x[2 * i], x[2 * i + 1], scale_log2, scale_log2, -ms, -ms);
+    const float p0 = ex2(y0), p1 = ex2(y1);
+    add_f32x2(acc[i & 3].x, acc[i & 3].y, p0, p1);
+    pk[i] = pack_p<BF16>(p0, p1);
+  }
+  tmem_st16(p_addr, pk);
 }
 
 template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdParams p) {
   using L = Smem<D>;
   using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -231,37 +320,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::kBarOff;
   auto q_full = [&](int t) { return bar0 + 8u * t; };
-  auto kv_full = [&](int s) { return bar0 + 8u * (2 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (2 + L::kStages + s); };
-  auto s_full = [&](int t) { return bar0 + 8u * (2 + 2 * L::kStages + t); };
-  auto p_full = [&](int t) { return bar0 + 8u * (4 + 2 * L::kStages + t); };
-  auto o_ready = [&](int t) { return bar0 + 8u * (6 + 2 * L::kStages + t); };
-  const uint32_t drain_bar = bar0 + 8u * (8 + 2 * L::kStages);
+  auto q_empty = [&](int t) { return bar0 + 8u * (2 + t); };
+  auto kv_full = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (4 + L::kStages + s); };
+  auto s_full = [&](int t) { return bar0 + 8u * (4 + 2 * L::kStages + t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (6 + 2 * L::kStages + t); };
+  auto o_ready = [&](int t) { return bar0 + 8u * (8 + 2 * L::kStages + t); };
+  auto o_free = [&](int t) { return bar0 + 8u * (10 + 2 * L::kStages + t); };
+  const uint32_t drain_bar = bar0 + 8u * (12 + 2 * L::kStages);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
-  Work *work_s = reinterpret_cast<Work *>(smem + L::kMiscOff + 8);
-  static_assert(sizeof(Work) <= 120, "work record does not fit");
+  static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-
-  if (warp == 0) {
-    Work w;
-    decode_work<CAUSAL, VARLEN>(p, w, lane);
-    if (lane == 0) *work_s = w;
-  }
-  if (tid == 32) *abort_flag = 0;
-  __syncthreads();
-  const Work w = *work_s;
-  if (!w.valid) return;
+  FA_TRACE_AT(tid == 0, 2047);
 
   if (tid == 0) {
+    *abort_flag = 0;
     for (int t = 0; t < 2; ++t) {
       mbar_init(q_full(t), 1);
+      mbar_init(q_empty(t), 1);
       mbar_init(s_full(t), 1);
-      mbar_init(p_full(t), 4);
+      mbar_init(p_full(t), 4);   // one arrival per softmax warp
       mbar_init(o_ready(t), 1);
+      mbar_init(o_free(t), 4);
     }
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(kv_full(s), 1);
@@ -278,277 +362,367 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const long long limit = p.wait_limit;
+  auto wait = [&](uint32_t bar, uint32_t par) {
+    return wait_bar(bar, par, abort_flag, limit, p.status);
+  };
 
   if (warp >= 8) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
-  if (warp == kTmaWarp) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
+    if (warp == kTmaWarp) {
+      // ---------------------------------------------------------- TMA producer
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      int issued = 0;  // K/V loads issued (ring index)
+      int issued = 0;                  // K/V loads issued (ring index, across units)
+      int q_loads0 = 0, q_loads1 = 0;  // Q loads per tile buffer
       bool ok = true;
-      for (int t = 0; t < 2; ++t) {
-        if (w.n_kv[t] == 0) continue;
-        mbar_arrive_expect_tx(q_full(t), L::kTileBytes);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sbase + L::kQOff + t * L::kTileBytes + c * kChunkBytes, &tm_q, q_full(t),
-                      c * 64, w.head[t], w.q_row0 + w.m0[t], w.map_b, pol_q);
-      }
-      for (int j = 0; j < w.n_max && ok; ++j) {
-        for (int which = 0; which < 2; ++which) {
-          const int idx = 2 * j + which;
-          const int s = idx % L::kStages;
-          if (idx >= L::kStages &&
-              !wait_bar(kv_empty(s), ((idx / L::kStages) + 1) & 1, abort_flag, limit, p.status)) {
-            ok = false;
-            break;
+      for (int i = 0; ok; ++i) {
+        const int unit = unit_of(i);
+        if (unit >= p.total_units) break;
+        const Work w = decode_work<CAUSAL, VARLEN>(p, unit, lane);
+        if (!w.valid) continue;
+        if (lane == 0) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            int &q_loads = t ? q_loads1 : q_loads0;
+            if (w.n_kv[t] == 0 || !ok) continue;
+            // the previous unit's Q_t is free once its last S_t = Q_t K^T is done
+            if (q_loads > 0 && !wait(q_empty(t), (q_loads - 1) & 1)) {
+              ok = false;
+              continue;
+            }
+            mbar_arrive_expect_tx(q_full(t), L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_4d(sbase + L::kQOff + t * L::kTileBytes + c * kChunkBytes, &tm_q,
+                          q_full(t), c * 64, w.head[t], w.q_row0 + w.m0[t], w.map_b, pol_q);
+            ++q_loads;
           }
-          const CUtensorMap *tm = which == 0 ? &tm_k : &tm_v;
-          mbar_arrive_expect_tx(kv_full(s), L::kTileBytes);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_4d(sbase + L::kKVOff + s * L::kTileBytes + c * kChunkBytes, tm, kv_full(s),
-                        c * 64, w.hkv, w.k_row0 + j * kBlockN, w.map_b, pol_kv);
-          issued = idx + 1;
+          for (int j = 0; j < w.n_max && ok; ++j) {
+            for (int which = 0; which < 2; ++which) {
+              const int idx = issued;
+              const int s = idx % L::kStages;
+              if (idx >= L::kStages && !wait(kv_empty(s), ((idx / L::kStages) + 1) & 1)) {
+                ok = false;
+                break;
+              }
+              const CUtensorMap *tm = which == 0 ? &tm_k : &tm_v;
+              FA_TRACE_AT(idx < 256, 1536 + idx);
+              mbar_arrive_expect_tx(kv_full(s), L::kTileBytes);
+              for (int c = 0; c < L::kChunks; ++c)
+                tma_load_4d(sbase + L::kKVOff + s * L::kTileBytes + c * kChunkBytes, tm,
+                            kv_full(s), c * 64, w.hkv, w.k_row0 + j * kBlockN, w.map_b, pol_kv);
+              issued = idx + 1;
+            }
+          }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         // drain copies still in flight into the ring before the CTA exits
         for (int idx = max(0, issued - L::kStages); idx < issued; ++idx)
-          wait_bar(kv_full(idx % L::kStages), (idx / L::kStages) & 1, abort_flag, limit, p.status,
-                   false);
+          wait_bar(kv_full(idx % L::kStages), (idx / L::kStages) & 1, abort_flag, limit,
+                   p.status, false);
+        if (q_loads0 > 0)
+          wait_bar(q_full(0), (q_loads0 - 1) & 1, abort_flag, limit, p.status, false);
+        if (q_loads1 > 0)
+          wait_bar(q_full(1), (q_loads1 - 1) & 1, abort_flag, limit, p.status, false);
       }
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------- MMA issuer
-    if (lane == 0 && w.n_max > 0) {
+    } else if (warp == kMmaWarp) {
+      // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t idesc_qk = make_idesc_f16(BF16, kBlockM, kBlockN, false);
       constexpr uint32_t idesc_pv = make_idesc_f16(BF16, kBlockM, D, true);
-      bool ok = true;
-      auto wait_kv = [&](int idx) {
-        return wait_bar(kv_full(idx % L::kStages), (idx / L::kStages) & 1, abort_flag, limit, p.status);
-      };
+      const uint64_t q_desc0 = make_sdesc_sw128(sbase + L::kQOff, 16, 1024);
+      const uint64_t kv_desc0 = make_sdesc_sw128(sbase + L::kKVOff, 16, 1024);
+      const uint64_t v_desc0 = make_sdesc_sw128(sbase + L::kKVOff, kChunkBytes, 1024);
       auto issue_qk = [&](int t, int kidx) {
-        const uint32_t qa = sbase + L::kQOff + t * L::kTileBytes;
-        const uint32_t kb = sbase + L::kKVOff + (kidx % L::kStages) * L::kTileBytes;
+        const uint64_t qd = q_desc0 + ((t * L::kTileBytes) >> 4);
+        const uint64_t kd = kv_desc0 + (((kidx % L::kStages) * L::kTileBytes) >> 4);
+        const uint32_t d = tmem + t * 128;
+        mma_ss(d, qd, kd, idesc_qk, 0u);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + t * 128, make_sdesc_sw128(qa + off, 16, 1024),
-                 make_sdesc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+        for (int kk = 1; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss_acc(d, qd + off, kd + off, idesc_qk);
         }
       };
       auto issue_pv = [&](int t, int vidx, bool first) {
-        const uint32_t vb = sbase + L::kKVOff + (vidx % L::kStages) * L::kTileBytes;
+        const uint64_t vd = v_desc0 + (((vidx % L::kStages) * L::kTileBytes) >> 4);
+        const uint32_t d = tmem + 256 + t * D;
+        const uint32_t a = tmem + t * 128;
+        mma_ts(d, a, vd, idesc_pv, first ? 0u : 1u);
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
-                 make_sdesc_sw128(vb + kk * 2048, kChunkBytes, 1024), idesc_pv,
-                 (!first || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 1; kk < kBlockN / 16; ++kk)
+          mma_ts_acc(d, a + kk * 8, vd + ((kk * 2048) >> 4), idesc_pv);
       };
-      // step 0: S_t = Q_t K(0)^T
-      ok = wait_kv(0);
-      for (int t = 0; t < 2 && ok; ++t) {
-        if (w.n_kv[t] == 0) continue;
-        ok = wait_bar(q_full(t), 0, abort_flag, limit, p.status);
-        if (!ok) break;
+      auto kv_par = [&](int idx) { return (uint32_t)((idx / L::kStages) & 1); };
+      int used = 0;                 // K/V loads consumed (ring index, across units)
+      // per-tile phase counters kept in scalars (tile index is a compile-time
+      // constant below, so nothing is indexed at run time)
+      int q_used0 = 0, q_used1 = 0;    // Q tiles consumed
+      int p_seen0 = 0, p_seen1 = 0;    // P tiles consumed (p_full phases)
+      int o_done0 = 0, o_done1 = 0;    // finished O accumulations (o_ready / o_free)
+      bool ok = true;
+      // step 0 of tile T: S_T = Q_T K(0)^T
+      auto first_qk = [&](auto tc, int n, int k0idx) {
+        constexpr int T = decltype(tc)::value;
+        int &q_used = T ? q_used1 : q_used0;
+        if (n == 0 || !ok) return;
+        ok = wait(q_full(T), q_used & 1);
+        if (!ok) return;
+        ++q_used;
         tc_fence_after();
-        issue_qk(t, 0);
-        tc_commit(s_full(t));
-      }
-      if (ok) tc_commit(kv_empty(0));
-      for (int j = 1; j < w.n_max && ok; ++j) {
-        const int kidx = 2 * j, vidx = 2 * j - 1;
-        ok = wait_kv(kidx) && wait_kv(vidx);
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j - 1 < w.n_kv[t]) {
-            ok = wait_bar(p_full(t), (j - 1) & 1, abort_flag, limit, p.status);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(t, vidx, j - 1 == 0);
-            tc_commit(o_ready(t));
+        issue_qk(T, k0idx);
+        tc_commit(s_full(T));
+        if (n == 1) tc_commit(q_empty(T));  // last S_T of this unit issued
+      };
+      // bracket of tile T at step j: O_T += P_T(j-1) V(j-1), then S_T = Q_T K(j)^T
+      auto bracket = [&](auto tc, int n, int j, int vidx, int kidx, int i) {
+        constexpr int T = decltype(tc)::value;
+        int &p_seen = T ? p_seen1 : p_seen0;
+        int &o_done = T ? o_done1 : o_done0;
+        if (!ok) return;
+        if (j - 1 < n) {
+          ok = wait(p_full(T), p_seen & 1);
+          if (!ok) return;
+          ++p_seen;
+          // the first O += P V of a unit overwrites O_T: the previous unit's
+          // epilogue must have read it out
+          if (j == 1 && o_done > 0) {
+            ok = wait(o_free(T), (o_done - 1) & 1);
+            if (!ok) return;
           }
-          if (j < w.n_kv[t]) {
-            issue_qk(t, kidx);
-            tc_commit(s_full(t));
-          }
-        }
-        if (ok) {
-          tc_commit(kv_empty(vidx % L::kStages));
-          tc_commit(kv_empty(kidx % L::kStages));
-        }
-      }
-      if (ok) {
-        const int j = w.n_max;
-        const int vidx = 2 * j - 1;
-        ok = wait_kv(vidx);
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j - 1 < w.n_kv[t]) {
-            ok = wait_bar(p_full(t), (j - 1) & 1, abort_flag, limit, p.status);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(t, vidx, j - 1 == 0);
-            tc_commit(o_ready(t));
+          FA_TRACE_AT(i == 0 && j < 64, 1024 + j * 8 + 2 * T);
+          tc_fence_after();
+          issue_pv(T, vidx, j == 1);
+          if (j == n) {
+            tc_commit(o_ready(T));  // tile T of this unit is complete
+            ++o_done;
           }
         }
-        if (ok) tc_commit(kv_empty(vidx % L::kStages));
+        if (j < n) {
+          issue_qk(T, kidx);
+          tc_commit(s_full(T));
+          if (j == n - 1) tc_commit(q_empty(T));
+        }
+        FA_TRACE_AT(i == 0 && j < 64, 1024 + j * 8 + 2 * T + 1);
+      };
+      using T0 = std::integral_constant<int, 0>;
+      using T1 = std::integral_constant<int, 1>;
+      for (int i = 0; ok; ++i) {
+        const int unit = unit_of(i);
+        if (unit >= p.total_units) break;
+        const Work w = decode_work<CAUSAL, VARLEN>(p, unit, lane);
+        if (!w.valid || w.n_max == 0) continue;
+        if (lane == 0) {
+          const int n0 = w.n_kv[0], n1 = w.n_kv[1];
+          const int k0idx = used;
+          ok = wait(kv_full(k0idx % L::kStages), kv_par(k0idx));
+          first_qk(T0{}, n0, k0idx);
+          first_qk(T1{}, n1, k0idx);
+          if (ok) tc_commit(kv_empty(k0idx % L::kStages));
+          for (int j = 1; j <= w.n_max && ok; ++j) {
+            const int vidx = used + 2 * j - 1, kidx = used + 2 * j;
+            const bool last = j == w.n_max;  // only O += P V remains
+            ok = wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
+                 (last || wait(kv_full(kidx % L::kStages), kv_par(kidx)));
+            bracket(T0{}, n0, j, vidx, kidx, i);
+            bracket(T1{}, n1, j, vidx, kidx, i);
+            if (ok) {
+              tc_commit(kv_empty(vidx % L::kStages));
+              if (!last) tc_commit(kv_empty(kidx % L::kStages));
+            }
+          }
+          used += 2 * w.n_max;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      // make sure no MMA is still running when tensor memory is released
-      tc_commit(drain_bar);
-      wait_bar(drain_bar, 0, abort_flag, limit, p.status, false);
+      if (lane == 0) {
+        // make sure no MMA is still running when tensor memory is released
+        tc_commit(drain_bar);
+        wait_bar(drain_bar, 0, abort_flag, limit, p.status, false);
+      }
     }
-  }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
     // ------------------------------------------------------ softmax + epilogue
     const int t = warp >> 2;        // query tile of this warpgroup
     const int quarter = warp & 3;   // TMEM lane quarter
     const int row = quarter * 32 + lane;
-    const int qi = w.m0[t] + row;   // query row within its sequence
-    const int n_kv = w.n_kv[t];
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t s_addr = lane_base + t * 128;
     const uint32_t o_addr = lane_base + 256 + t * D;
     const float scale_log2 = p.scale_log2;
     const float neg_thr = -p.threshold;
-    const int diag = qi + w.lk - w.lq;  // last visible key of this row (causal)
     // every lane of a warp must agree before the warp-wide tcgen05.ld / st
     auto warp_wait = [&](uint32_t bar, uint32_t parity) {
-      const bool got = wait_bar(bar, parity, abort_flag, limit, p.status);
+      const bool got = wait(bar, parity);
       return __all_sync(0xffffffffu, got);
     };
-    float m = -INFINITY, l = 0.f;
+    int s_seen = 0;   // S tiles consumed (s_full phases, across units)
+    int o_seen = 0;   // finished units of this tile (o_ready phases)
+    const bool elected = quarter == 0 && lane == 0;  // issues this tile's TMA stores
+    const uint32_t stage = sbase + L::kStageOff + t * kChunkBytes;
+    // The warpgroup meets at named barrier 1 + t in the epilogue.  To keep every
+    // barrier complete, the role never leaves its unit loop early: after a
+    // failed wait (ok == false) it keeps walking the same units and barriers
+    // but skips every wait, tensor-memory access and store.
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!warp_wait(s_full(t), j & 1)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld128_wait(s_addr, sr);
-      float *s = reinterpret_cast<float *>(sr);
-      const int k0 = j * kBlockN;
-      const bool need_mask =
-          (k0 + kBlockN > w.lk) || (CAUSAL && (k0 + kBlockN - 1 > w.m0[t] + w.lk - w.lq));
-      if (need_mask) {
-        int lim = w.lk - k0;
-        if (CAUSAL) lim = min(lim, diag - k0 + 1);
-#pragma unroll
-        for (int c = 0; c < kBlockN; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
-      }
-      float bm = s[0];
-#pragma unroll
-      for (int c = 1; c < kBlockN; ++c) bm = fmaxf(bm, s[c]);
-      float alpha = 1.f;
-      bool rescale = false;
-      if (j == 0) {
-        m = bm;
-      } else {
-        const float m_cur = fmaxf(m, bm);
-        const float diff = (m_cur == -INFINITY) ? 0.f : (m - m_cur) * scale_log2;
-        if (!(diff >= neg_thr)) {
-          alpha = ex2(diff);
-          l *= alpha;
-          m = m_cur;
-          rescale = true;
-        }
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O_t(j-1) must be final before it is rescaled in place
-        if (!warp_wait(o_ready(t), (j - 1) & 1)) { ok = false; break; }
+    for (int i = 0;; ++i) {
+      const int unit = unit_of(i);
+      if (unit >= p.total_units) break;
+      const Work w = decode_work<CAUSAL, VARLEN>(p, unit, lane);
+      if (!w.valid || w.m0[t] >= w.lq) continue;  // no rows of this tile
+      const int m0 = w.m0[t];        // per-tile fields read once per unit
+      const int n_kv = w.n_kv[t];
+      const int lq = w.lq, lk = w.lk;
+      const int qi = m0 + row;       // query row within its sequence
+      const int diag = qi + lk - lq;  // last visible key of this row (causal)
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        if (!warp_wait(s_full(t), s_seen & 1)) { ok = false; break; }
+        ++s_seen;
+        [[maybe_unused]] const bool tr = i == 0 && quarter == 0 && lane == 0 && j < 63;
+        FA_TRACE_AT(tr, (t * 64 + j) * 8);
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t orr[32];
-          tmem_ld32_wait(o_addr + c * 32, orr);
+        uint32_t sr[128];
+        tmem_ld128_wait(s_addr, sr);
+        float *s = reinterpret_cast<float *>(sr);
+        FA_TRACE_AT(tr, (t * 64 + j) * 8 + 1);
+        const int k0 = j * kBlockN;
+        const bool need_mask =
+            (k0 + kBlockN > lk) || (CAUSAL && (k0 + kBlockN - 1 > m0 + lk - lq));
+        if (need_mask) {
+          int lim = lk - k0;  // keys [0, lim) of this tile are visible to the row
+          if (CAUSAL) lim = min(lim, diag - k0 + 1);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-          tmem_st32(o_addr + c * 32, orr);
+          for (int c = 0; c < kBlockN; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
         }
-      }
-      const float ms = (m == -INFINITY) ? 0.f : m * scale_log2;
-      float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = c4 * 32 + 2 * i;
-          float x0, x1;
-          fma_f32x2(x0, x1, s[c], s[c + 1], scale_log2, scale_log2, -ms, -ms);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          ls0 += p0;
-          ls1 += p1;
-          if (BF16) {
-            __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-            pk[i] = *reinterpret_cast<uint32_t *>(&h);
-          } else {
-            __half2 h = __floats2half2_rn(p0, p1);
-            pk[i] = *reinterpret_cast<uint32_t *>(&h);
-          }
+        const float bm = fmax3(fmaxf(max32(s), max32(s + 32)), max32(s + 64), max32(s + 96));
+        float alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m = bm;  // the first tile sets the max, no threshold
+        } else {
+          const float m_cur = fmaxf(m, bm);
+          const float diff = (m_cur == -INFINITY) ? 0.f : (m - m_cur) * scale_log2;
+          if (!(diff >= neg_thr)) {  // rise above the threshold: rescale
+            alpha = ex2(diff);
+            m = m_cur;
+            rescale = true;
+          }                          // else skip and keep the lagged max
         }
-        tmem_st16(s_addr + c4 * 16, pk);  // 32 keys -> 16 packed columns
-      }
-      l += ls0 + ls1;
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(t));
-    }
-    // --------------------------------------------------------------- epilogue
-    const bool row_valid = qi < w.lq && w.m0[t] < w.lq;
-    const int64_t tok = w.o_row0 + qi;
-    if (ok && w.m0[t] < w.lq) {
-      elem_t *o = reinterpret_cast<elem_t *>(p.o) + (tok * p.Hq + w.head[t]) * (int64_t)D;
-      if (n_kv > 0) {
-        if (warp_wait(o_ready(t), (n_kv - 1) & 1)) {
-          tc_fence_after();
-          const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        FA_TRACE_AT(tr, (t * 64 + j) * 8 + 2);
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O_t holds P V up to tile j-1: S_t(j) was committed after that PV,
+          // so it has completed and no MMA writes O_t until this P is ready
+          l *= alpha;
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t orr[32];
             tmem_ld32_wait(o_addr + c * 32, orr);
-            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float a = __uint_as_float(orr[2 * i]) * inv_l;
-              const float b = __uint_as_float(orr[2 * i + 1]) * inv_l;
-              if (BF16) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-                pk[i] = *reinterpret_cast<uint32_t *>(&h);
-              } else {
-                __half2 h = __floats2half2_rn(a, b);
-                pk[i] = *reinterpret_cast<uint32_t *>(&h);
-              }
-            }
-            if (row_valid) {
-              uint4 *dst = reinterpret_cast<uint4 *>(o + c * 32);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            }
+            for (int k = 0; k < 32; ++k)
+              orr[k] = __float_as_uint(__uint_as_float(orr[k]) * alpha);
+            tmem_st32(o_addr + c * 32, orr);
           }
-        } else {
-          ok = false;
         }
-      } else if (row_valid) {
+        const float ms = (m == -INFINITY) ? 0.f : m * scale_log2;
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          softmax_chunk<BF16>(s + 32 * c, scale_log2, ms, acc, s_addr + 16 * c);
+        add_f32x2(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+        add_f32x2(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+        add_f32x2(acc[0].x, acc[0].y, acc[2].x, acc[2].y);
+        l += acc[0].x + acc[0].y;
+        FA_TRACE_AT(tr, (t * 64 + j) * 8 + 3);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(t));
+        FA_TRACE_AT(tr, (t * 64 + j) * 8 + 4);
+      }
+      // ------------------------------------------------------------- epilogue
+      [[maybe_unused]] const bool tr = i == 0 && quarter == 0 && lane == 0;
+      FA_TRACE_AT(tr, (t * 64 + 63) * 8 + 5);
+      // O_t of this unit (zero when no key is visible), read out of tensor
+      // memory and released first so the next unit's O += P V can start
+      uint32_t orr[D];
+#pragma unroll
+      for (int k = 0; k < D; ++k) orr[k] = 0u;
+      if (n_kv > 0 && ok) {
+        ok = warp_wait(o_ready(t), o_seen & 1);
+        ++o_seen;
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c)
+            tmem_ld32(o_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(orr + 32 * c));
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c)
+            tmem_wait_ld32(*reinterpret_cast<uint32_t(*)[32]>(orr + 32 * c));
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_free(t));
+        }
+      }
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const bool row_valid = qi < lq;
+      const int64_t tok = w.o_row0 + qi;
+      auto packed = [&](int k) {  // 16-bit pair of normalised O columns 2k, 2k+1
+        return pack_p<BF16>(__uint_as_float(orr[2 * k]) * inv_l,
+                            __uint_as_float(orr[2 * k + 1]) * inv_l);
+      };
+      // a packed tile cut by its sequence end would spill into the next
+      // sequence through the tensor map, so it is stored row by row instead
+      const bool use_tma = !VARLEN || (m0 + kBlockM <= lq);
+      if (use_tma) {
+#pragma unroll
+        for (int half = 0; half < D / 64; ++half) {
+          named_barrier_sync(1 + t, 128);  // staging buffer free
+          if (ok) {
+            // row `row`, 16-byte chunk c at swizzled position c ^ (row % 8)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int k = half * 32 + 4 * c;
+              st_shared_v4(stage + row * 128 + ((c ^ (row & 7)) << 4), packed(k), packed(k + 1),
+                           packed(k + 2), packed(k + 3));
+            }
+            fence_proxy_async_smem();
+          }
+          named_barrier_sync(1 + t, 128);  // staging buffer full
+          if (elected) {
+            if (ok) {
+              tma_store_4d(&tm_o, stage, half * 64, w.head[t], w.q_row0 + m0, w.map_b);
+              bulk_commit_group();
+            }
+            bulk_wait_group_read0();
+          }
+        }
+      } else if (row_valid && ok) {
+        elem_t *o = reinterpret_cast<elem_t *>(p.o) + (tok * p.Hq + w.head[t]) * (int64_t)D;
         uint4 *dst = reinterpret_cast<uint4 *>(o);
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+        for (int k = 0; k < D / 8; ++k)
+          dst[k] = make_uint4(packed(4 * k), packed(4 * k + 1), packed(4 * k + 2), packed(4 * k + 3));
       }
-      if (ok && row_valid && p.lse != nullptr) {
+      if (row_valid && ok && p.lse != nullptr) {
         const float lse = (l > 0.f) ? (m * scale_log2 + log2f(l)) * 0.69314718055994531f
                                     : -INFINITY;
         const int64_t li = VARLEN ? (int64_t)w.head[t] * p.Sq + tok
                                   : ((int64_t)w.b * p.Hq + w.head[t]) * p.Sq + qi;
         p.lse[li] = lse;
       }
+      FA_TRACE_AT(tr, (t * 64 + 63) * 8 + 6);
     }
+    if (elected) bulk_wait_group0();  // output stores complete before the CTA exits
   }
 
   tc_fence_before();

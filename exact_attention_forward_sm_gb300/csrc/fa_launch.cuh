@@ -8,7 +8,7 @@
 namespace fa {
 
 struct LaunchArgs {
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
   FwdParams p;
   int grid;
   cudaStream_t stream;
@@ -27,7 +27,7 @@ cudaError_t launch_fwd(const LaunchArgs &a) {
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  kern<<<a.grid, kThreads, Smem<D>::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
+  kern<<<a.grid, kThreads, Smem<D>::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
   return cudaGetLastError();
 }
 

@@ -5,6 +5,8 @@
 // Only the PTX instructions themselves are used; no vendor library headers.
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstdint>
 
 namespace fa {
@@ -24,6 +26,13 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 // Make barrier initialisation visible to the async proxy (TMA, tcgen05).
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -51,6 +60,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking probe of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Named barrier `id` (1..15) over `count` threads (whole warps).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
@@ -68,6 +95,30 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, uint
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
       "l"(cache_policy)
       : "memory");
+}
+
+// 4-D tiled bulk tensor store from this CTA's shared memory (bulk group).
+__device__ __forceinline__ void tma_store_4d(const void *tmap, uint32_t src, int c0, int c1,
+                                             int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until every committed bulk store has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until every committed bulk store has completed.
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -138,6 +189,27 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Accumulating forms (enable-input-d fixed to true): no per-MMA predicate setup.
+__device__ __forceinline__ void mma_ss_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.eq.u32 p, 1, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_acc(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.eq.u32 p, 1, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc)
+      : "memory");
+}
+
 // Instruction descriptor for kind::f16 with an fp32 accumulator.
 //   bits 4-5 accumulator format (1 = f32), 7-9 / 10-12 A / B format
 //   (0 = f16, 1 = bf16), 15 / 16 A / B major-ness (0 = K-major, 1 = MN-major),
@@ -182,6 +254,28 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
       : "r"(taddr)
       : "memory");
 }
+
+// Load without waiting; pair with tmem_wait_ld32 on the same registers, which
+// ties them to the wait so no use can be scheduled before the data arrives.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : FA_R8(0), FA_R8(8), FA_R8(16), FA_R8(24)
+      : "r"(taddr)
+      : "memory");
+}
+
+#define FA_RW8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), \
+                  "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : FA_RW8(0), FA_RW8(8), FA_RW8(16), FA_RW8(24)
+               :
+               : "memory");
+}
+#undef FA_RW8
 
 __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, uint32_t (&r)[128]) {
   asm volatile(
@@ -229,21 +323,34 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 // --------------------------------------------------------- softmax arithmetic
 
-// (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1) as one packed fp32 FMA (sm_100+
-// fma.rn.f32x2).  Not volatile: the compiler may schedule it freely.
+// (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1) as one packed fp32 FMA
+// (fma.rn.f32x2, sm_100+), through the compiler's f32x2 builtin so the operand
+// pairs are allocated as register pairs; -DFA_UNFUSE_FMA gives two scalar FMAs
+// (ablation).
 __device__ __forceinline__ void fma_f32x2(float &d0, float &d1, float a0, float a1, float b0,
                                           float b1, float c0, float c1) {
-#ifndef FA_UNFUSE_FMA
-  uint64_t a, b, c, d;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(c) : "f"(c0), "f"(c1));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+#if !defined(FA_UNFUSE_FMA)
+  const float2 d = __ffma2_rn(make_float2(a0, a1), make_float2(b0, b1), make_float2(c0, c1));
+  d0 = d.x;
+  d1 = d.y;
 #else
   d0 = __fmaf_rn(a0, b0, c0);
   d1 = __fmaf_rn(a1, b1, c1);
 #endif
+}
+
+// max(a, b, c) in one instruction (sm_100+ three-input max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (a0 + b0, a1 + b1) as one packed fp32 add (add.rn.f32x2, sm_100+).
+__device__ __forceinline__ void add_f32x2(float &a0, float &a1, float b0, float b1) {
+  const float2 d = __fadd2_rn(make_float2(a0, a1), make_float2(b0, b1));
+  a0 = d.x;
+  a1 = d.y;
 }
 
 // 2^x on the special-function unit (flush-to-zero; 2^-inf = +0).

@@ -112,6 +112,16 @@ int fa_get_device_error(fa_stream_t stream);
  */
 int fa_debug_wait_timeout(long long limit_cycles, fa_stream_t stream);
 
+/*
+ * fa_debug_trace_read — pipeline trace of a trace build (libfa_trace.so, built
+ * with -DFA_TRACE).  The first CTA of every fa_fwd launch records SM clock64
+ * stamps of its warp roles (softmax steps, MMA issue, TMA issue) into a
+ * 2048-entry device buffer; this call synchronizes the device, copies the first
+ * `n` entries (n <= 2048) to the HOST array `host_out` and clears the buffer.
+ * Product builds return FA_ERR_UNSUPPORTED.
+ */
+int fa_debug_trace_read(unsigned long long *host_out, int n);
+
 /* Human-readable name of a status code (static string). */
 const char *fa_status_string(int status);
 
