@@ -17,9 +17,10 @@
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3   softmax + epilogue for tile 0 (thread = query row = TMEM lane)
 //   warps 4-7   softmax + epilogue for tile 1
-//   warp  8     TMEM allocation; lane 0 issues every tcgen05.mma
+//   warp  8     TMEM allocation; lane 0 issues tile 0's tcgen05.mma
 //   warp  9     lane 0 issues every TMA load
-//   warps 10-11 idle
+//   warp  10    lane 0 issues tile 1's tcgen05.mma
+//   warp  11    idle
 // After set-up the third warpgroup gives registers back (setmaxnreg) so the
 // softmax warpgroups can hold a full 128-column score row: 2 x 128 x 192 +
 // 128 x 96 = 61440 <= 384 x 168 registers granted at launch.
@@ -31,6 +32,8 @@
 //
 // Per K/V tile j and query tile t the MMA thread issues, in this order,
 //   O_t += P_t(j-1) V(j-1)   then   S_t = Q_t K(j)^T,
+// with the first half of O += P V (keys 0-63) started as soon as the softmax
+// has stored those P values, while it still computes keys 64-127;
 // alternating tiles, so tile 0's softmax runs while the tensor pipe works on
 // tile 1 and vice versa.  The tensor pipe executes one CTA's MMAs in issue
 // order, so the S_t write of step j happens after the P_t read of step j-1
@@ -64,8 +67,9 @@ namespace fa {
 constexpr int kBlockM = 128;      // query rows per tile
 constexpr int kBlockN = 128;      // keys per K/V tile
 constexpr int kThreads = 384;
-constexpr int kMmaWarp = 8;
+constexpr int kMmaWarp = 8;   // issues tile 0's MMAs (and owns the TMEM allocation)
 constexpr int kTmaWarp = 9;
+constexpr int kMmaWarp2 = 10; // issues tile 1's MMAs
 constexpr int kTmemCols = 512;
 constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 64 elements x 2 bytes
 
@@ -91,10 +95,10 @@ struct FwdParams {
 // Pipeline trace (compiled in with -DFA_TRACE): CTA 0 records SM clock stamps
 // of the K/V steps of its first unit into a 2048-entry buffer.
 //   softmax tile t, step j < 63:  (t * 64 + j) * 8 + e   e: 0 S ready, 1 S in
-//       registers, 2 max / rescale decided, 3 P stores issued, 4 P ready
-//       signalled; (t * 64 + 63) * 8 + 5 / 6: epilogue start / end
-//   MMA thread, tile t, step j:  1024 + j * 8 + 2 t + e   e: 0 P(j-1) ready,
-//       1 O += P(j-1) V(j-1) and S = Q K(j)^T issued
+//       registers, 2 max / rescale decided, 3 P of keys 0-63 signalled, 4 P of
+//       keys 64-127 signalled; (t * 64 + 63) * 8 + 5 / 6: epilogue start / end
+//   MMA issuer of tile t, step j:  1024 + j * 8 + 2 + 2t + e   e: 0 inputs
+//       ready, 1 O_t += P_t(j-1) V(j-1) and S_t = Q_t K(j)^T issued
 //   TMA load idx < 256:           1536 + idx  (issue time)
 //   2047: kernel start
 constexpr int kTraceEntries = 2048;
@@ -121,8 +125,8 @@ struct Smem {
   static constexpr uint32_t kStageOff = kKVOff + kStages * kTileBytes;
   static constexpr uint32_t kBarOff = kStageOff + 2 * kChunkBytes;
   // barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2],
-  //           p_full[2], o_ready[2], o_free[2], drain
-  static constexpr int kNumBars = 4 + 2 * kStages + 9;
+  //           p_half[2][2], o_ready[2], o_free[2], drain
+  static constexpr int kNumBars = 4 + 2 * kStages + 11;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -324,12 +328,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto kv_full = [&](int s) { return bar0 + 8u * (4 + s); };
   auto kv_empty = [&](int s) { return bar0 + 8u * (4 + L::kStages + s); };
   auto s_full = [&](int t) { return bar0 + 8u * (4 + 2 * L::kStages + t); };
-  auto p_full = [&](int t) { return bar0 + 8u * (6 + 2 * L::kStages + t); };
-  auto o_ready = [&](int t) { return bar0 + 8u * (8 + 2 * L::kStages + t); };
-  auto o_free = [&](int t) { return bar0 + 8u * (10 + 2 * L::kStages + t); };
-  const uint32_t drain_bar = bar0 + 8u * (12 + 2 * L::kStages);
+  // P_t of keys [64 h, 64 h + 64) is in tensor memory
+  auto p_half = [&](int t, int h) { return bar0 + 8u * (6 + 2 * L::kStages + 2 * t + h); };
+  auto o_ready = [&](int t) { return bar0 + 8u * (10 + 2 * L::kStages + t); };
+  auto o_free = [&](int t) { return bar0 + 8u * (12 + 2 * L::kStages + t); };
+  const uint32_t drain_bar = bar0 + 8u * (14 + 2 * L::kStages);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+  volatile int *mma_turn = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 8);
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
 
   const int tid = threadIdx.x;
@@ -343,15 +349,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(q_full(t), 1);
       mbar_init(q_empty(t), 1);
       mbar_init(s_full(t), 1);
-      mbar_init(p_full(t), 4);   // one arrival per softmax warp
+      mbar_init(p_half(t, 0), 4);  // one arrival per softmax warp
+      mbar_init(p_half(t, 1), 4);
       mbar_init(o_ready(t), 1);
       mbar_init(o_free(t), 4);
     }
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+      mbar_init(kv_empty(s), 2);  // one release per query tile
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(drain_bar, 2);      // one per MMA issuer
+    *mma_turn = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -433,109 +441,140 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_loads1 > 0)
           wait_bar(q_full(1), (q_loads1 - 1) & 1, abort_flag, limit, p.status, false);
       }
-    } else if (warp == kMmaWarp) {
-      // ------------------------------------------------------------ MMA issuer
+    } else if ((warp == kMmaWarp || warp == kMmaWarp2)) {
+      // ------------------------------------------------ MMA issuers, one per tile
+      // Warp 8 lane 0 issues tile 0's MMAs, warp 10 lane 0 tile 1's.  A turn
+      // flag in shared memory makes them take strict turns, bracket by bracket:
+      //   [S0 = Q0 K(0)^T] [S1 = Q1 K(0)^T] [O0 += P0 V(0), S0 = Q0 K(1)^T]
+      //   [O1 += P1 V(0), S1 = Q1 K(1)^T] ...
+      // so the tensor pipe still alternates tiles (tile 0's softmax runs while
+      // the pipe works on tile 1), while each issuer does its barrier waits and
+      // commits during the other one's bracket: issue blocks on a shallow queue,
+      // and one thread doing both left the pipe idle between brackets.
+      const int T = (warp == kMmaWarp) ? 0 : 1;
       constexpr uint32_t idesc_qk = make_idesc_f16(BF16, kBlockM, kBlockN, false);
       constexpr uint32_t idesc_pv = make_idesc_f16(BF16, kBlockM, D, true);
-      const uint64_t q_desc0 = make_sdesc_sw128(sbase + L::kQOff, 16, 1024);
+      // descriptors built once; each MMA adds a compile-time offset
+      const uint64_t q_desc = make_sdesc_sw128(sbase + L::kQOff + T * L::kTileBytes, 16, 1024);
       const uint64_t kv_desc0 = make_sdesc_sw128(sbase + L::kKVOff, 16, 1024);
       const uint64_t v_desc0 = make_sdesc_sw128(sbase + L::kKVOff, kChunkBytes, 1024);
-      auto issue_qk = [&](int t, int kidx) {
-        const uint64_t qd = q_desc0 + ((t * L::kTileBytes) >> 4);
+      const uint32_t d_s = tmem + T * 128, d_o = tmem + 256 + T * D;
+      auto issue_qk = [&](int kidx) {
         const uint64_t kd = kv_desc0 + (((kidx % L::kStages) * L::kTileBytes) >> 4);
-        const uint32_t d = tmem + t * 128;
-        mma_ss(d, qd, kd, idesc_qk, 0u);
+        mma_ss(d_s, q_desc, kd, idesc_qk, 0u);
 #pragma unroll
         for (int kk = 1; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss_acc(d, qd + off, kd + off, idesc_qk);
+          mma_ss_acc(d_s, q_desc + off, kd + off, idesc_qk);
         }
       };
-      auto issue_pv = [&](int t, int vidx, bool first) {
-        const uint64_t vd = v_desc0 + (((vidx % L::kStages) * L::kTileBytes) >> 4);
-        const uint32_t d = tmem + 256 + t * D;
-        const uint32_t a = tmem + t * 128;
-        mma_ts(d, a, vd, idesc_pv, first ? 0u : 1u);
+      // O_T += P_T V for keys [64 h, 64 h + 64): four K = 16 steps reading
+      // P from TMEM columns [32 h, 32 h + 32) of S_T
+      auto issue_pv_half = [&](int vidx, int h, bool first) {
+        const uint64_t vd = v_desc0 + (((vidx % L::kStages) * L::kTileBytes + h * 4 * 2048) >> 4);
+        const uint32_t a = d_s + h * 32;
+        if (h == 0)
+          mma_ts(d_o, a, vd, idesc_pv, first ? 0u : 1u);
+        else
+          mma_ts_acc(d_o, a, vd, idesc_pv);
 #pragma unroll
-        for (int kk = 1; kk < kBlockN / 16; ++kk)
-          mma_ts_acc(d, a + kk * 8, vd + ((kk * 2048) >> 4), idesc_pv);
+        for (int kk = 1; kk < 4; ++kk)
+          mma_ts_acc(d_o, a + kk * 8, vd + ((kk * 2048) >> 4), idesc_pv);
       };
       auto kv_par = [&](int idx) { return (uint32_t)((idx / L::kStages) & 1); };
-      int used = 0;                 // K/V loads consumed (ring index, across units)
-      // per-tile phase counters kept in scalars (tile index is a compile-time
-      // constant below, so nothing is indexed at run time)
-      int q_used0 = 0, q_used1 = 0;    // Q tiles consumed
-      int p_seen0 = 0, p_seen1 = 0;    // P tiles consumed (p_full phases)
-      int o_done0 = 0, o_done1 = 0;    // finished O accumulations (o_ready / o_free)
+      // bounded spin for this issuer's turn (the other one is issuing)
+      auto take_turn = [&]() {
+        if (*mma_turn == T) return true;
+        const long long t0 = clock64();
+        while (*mma_turn != T) {
+          if (*abort_flag) return false;
+          if (clock64() - t0 > limit) {
+            record_status(p.status, 4);
+            *abort_flag = 1;
+            return false;
+          }
+        }
+        return true;
+      };
+      auto pass_turn = [&]() { *mma_turn = 1 - T; };
+      // every K/V load is released by two arrivals, one per tile; a load the
+      // other tile never reads gets both of them from this issuer
+      auto release = [&](int idx, bool other_reads) {
+        tc_commit(kv_empty(idx % L::kStages));
+        if (!other_reads) mbar_arrive(kv_empty(idx % L::kStages));
+      };
+      int used = 0;    // K/V loads consumed (ring index, across units)
+      int q_used = 0;  // Q tiles consumed
+      int p_seen = 0;  // P tiles consumed (p_half phases)
+      int o_done = 0;  // finished O accumulations (o_ready / o_free phases)
       bool ok = true;
-      // step 0 of tile T: S_T = Q_T K(0)^T
-      auto first_qk = [&](auto tc, int n, int k0idx) {
-        constexpr int T = decltype(tc)::value;
-        int &q_used = T ? q_used1 : q_used0;
-        if (n == 0 || !ok) return;
-        ok = wait(q_full(T), q_used & 1);
-        if (!ok) return;
-        ++q_used;
-        tc_fence_after();
-        issue_qk(T, k0idx);
-        tc_commit(s_full(T));
-        if (n == 1) tc_commit(q_empty(T));  // last S_T of this unit issued
-      };
-      // bracket of tile T at step j: O_T += P_T(j-1) V(j-1), then S_T = Q_T K(j)^T
-      auto bracket = [&](auto tc, int n, int j, int vidx, int kidx, int i) {
-        constexpr int T = decltype(tc)::value;
-        int &p_seen = T ? p_seen1 : p_seen0;
-        int &o_done = T ? o_done1 : o_done0;
-        if (!ok) return;
-        if (j - 1 < n) {
-          ok = wait(p_full(T), p_seen & 1);
-          if (!ok) return;
-          ++p_seen;
-          // the first O += P V of a unit overwrites O_T: the previous unit's
-          // epilogue must have read it out
-          if (j == 1 && o_done > 0) {
-            ok = wait(o_free(T), (o_done - 1) & 1);
-            if (!ok) return;
-          }
-          FA_TRACE_AT(i == 0 && j < 64, 1024 + j * 8 + 2 * T);
-          tc_fence_after();
-          issue_pv(T, vidx, j == 1);
-          if (j == n) {
-            tc_commit(o_ready(T));  // tile T of this unit is complete
-            ++o_done;
-          }
-        }
-        if (j < n) {
-          issue_qk(T, kidx);
-          tc_commit(s_full(T));
-          if (j == n - 1) tc_commit(q_empty(T));
-        }
-        FA_TRACE_AT(i == 0 && j < 64, 1024 + j * 8 + 2 * T + 1);
-      };
-      using T0 = std::integral_constant<int, 0>;
-      using T1 = std::integral_constant<int, 1>;
       for (int i = 0; ok; ++i) {
         const int unit = unit_of(i);
         if (unit >= p.total_units) break;
         const Work w = decode_work<CAUSAL, VARLEN>(p, unit, lane);
         if (!w.valid || w.n_max == 0) continue;
         if (lane == 0) {
-          const int n0 = w.n_kv[0], n1 = w.n_kv[1];
+          const int n = w.n_kv[T], n_other = w.n_kv[1 - T];
+          // step 0: S_T = Q_T K(0)^T
           const int k0idx = used;
-          ok = wait(kv_full(k0idx % L::kStages), kv_par(k0idx));
-          first_qk(T0{}, n0, k0idx);
-          first_qk(T1{}, n1, k0idx);
-          if (ok) tc_commit(kv_empty(k0idx % L::kStages));
+          if (n > 0) {
+            ok = wait(kv_full(k0idx % L::kStages), kv_par(k0idx)) && wait(q_full(T), q_used & 1);
+            ++q_used;
+          }
+          ok = ok && take_turn();
+          if (ok) {
+            if (n > 0) {
+              tc_fence_after();
+              issue_qk(k0idx);
+            }
+            pass_turn();
+            if (n > 0) {
+              tc_commit(s_full(T));
+              if (n == 1) tc_commit(q_empty(T));  // last S_T of this unit issued
+              release(k0idx, n_other > 0);
+            }
+          }
           for (int j = 1; j <= w.n_max && ok; ++j) {
             const int vidx = used + 2 * j - 1, kidx = used + 2 * j;
-            const bool last = j == w.n_max;  // only O += P V remains
-            ok = wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
-                 (last || wait(kv_full(kidx % L::kStages), kv_par(kidx)));
-            bracket(T0{}, n0, j, vidx, kidx, i);
-            bracket(T1{}, n1, j, vidx, kidx, i);
-            if (ok) {
-              tc_commit(kv_empty(vidx % L::kStages));
-              if (!last) tc_commit(kv_empty(kidx % L::kStages));
+            const bool pv = j - 1 < n, qk = j < n;
+            if (pv) {
+              // the first O += P V of a unit overwrites O_T: the previous
+              // unit's epilogue must have read it out
+              ok = wait(p_half(T, 0), p_seen & 1) &&
+                   (j > 1 || o_done == 0 || wait(o_free(T), (o_done - 1) & 1)) &&
+                   wait(kv_full(vidx % L::kStages), kv_par(vidx));
+            }
+            if (ok && qk) ok = wait(kv_full(kidx % L::kStages), kv_par(kidx));
+            FA_TRACE_AT(i == 0 && j < 64, 1024 + j * 8 + 2 + 2 * T);
+            ok = ok && take_turn();
+            if (!ok) break;
+            if (pv) {
+              // keys 0-63 go to the tensor pipe while the softmax still works
+              // on keys 64-127; the turn is held until the bracket is complete
+              tc_fence_after();
+              issue_pv_half(vidx, 0, j == 1);
+              if (!wait(p_half(T, 1), p_seen & 1)) {
+                ok = false;
+                break;
+              }
+              ++p_seen;
+              tc_fence_after();
+              issue_pv_half(vidx, 1, false);
+            }
+            if (qk) issue_qk(kidx);
+            pass_turn();
+            FA_TRACE_AT(i == 0 && j < 64, 1024 + j * 8 + 3 + 2 * T);
+            if (pv) {
+              if (j == n) {
+                tc_commit(o_ready(T));  // tile T of this unit is complete
+                ++o_done;
+              }
+              release(vidx, j - 1 < n_other);
+            }
+            if (qk) {
+              tc_commit(s_full(T));
+              if (j == n - 1) tc_commit(q_empty(T));
+              release(kidx, j < n_other);
             }
           }
           used += 2 * w.n_max;
@@ -590,6 +629,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         [[maybe_unused]] const bool tr = i == 0 && quarter == 0 && lane == 0 && j < 63;
         FA_TRACE_AT(tr, (t * 64 + j) * 8);
         tc_fence_after();
+#ifdef FA_PROBE_NOSOFTMAX
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(p_half(t, 0));
+          mbar_arrive(p_half(t, 1));
+        }
+        continue;
+#endif
         uint32_t sr[128];
         tmem_ld128_wait(s_addr, sr);
         float *s = reinterpret_cast<float *>(sr);
@@ -635,19 +682,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float ms = (m == -INFINITY) ? 0.f : m * scale_log2;
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
+        // P of keys 0-63 is handed over before keys 64-127 are computed, so
+        // O += P V for the first half overlaps the second half's exps
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
           softmax_chunk<BF16>(s + 32 * c, scale_log2, ms, acc, s_addr + 16 * c);
+          if (c & 1) {
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_half(t, c >> 1));
+            FA_TRACE_AT(tr, (t * 64 + j) * 8 + 3 + (c >> 1));
+          }
+        }
         add_f32x2(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
         add_f32x2(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
         add_f32x2(acc[0].x, acc[0].y, acc[2].x, acc[2].y);
         l += acc[0].x + acc[0].y;
-        FA_TRACE_AT(tr, (t * 64 + j) * 8 + 3);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_full(t));
-        FA_TRACE_AT(tr, (t * 64 + j) * 8 + 4);
       }
       // ------------------------------------------------------------- epilogue
       [[maybe_unused]] const bool tr = i == 0 && quarter == 0 && lane == 0;
