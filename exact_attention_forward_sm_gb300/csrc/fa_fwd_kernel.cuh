@@ -629,14 +629,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         [[maybe_unused]] const bool tr = i == 0 && quarter == 0 && lane == 0 && j < 63;
         FA_TRACE_AT(tr, (t * 64 + j) * 8);
         tc_fence_after();
-#ifdef FA_PROBE_NOSOFTMAX
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(p_half(t, 0));
-          mbar_arrive(p_half(t, 1));
-        }
-        continue;
-#endif
         uint32_t sr[128];
         tmem_ld128_wait(s_addr, sr);
         float *s = reinterpret_cast<float *>(sr);
