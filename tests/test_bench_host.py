@@ -1,0 +1,70 @@
+"""Host-side logic of bench.py across ranks, on CPU with gloo (world size 2).
+
+Each rank draws its own problem of the same shape (weak scaling, no collective
+on the data path); the reported time is the maximum over ranks.
+"""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        r, lr, ws = bench.dist_env()
+        times = [3.5, 1.25]
+        mx = bench.max_over_ranks(times[rank], ws)
+        bench.barrier(ws)
+        out[rank] = (r, lr, ws, mx, bench.rank_seed(1001, r))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_max_time_and_distinct_problems():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        procs = [ctx.Process(target=_worker, args=(r, world, port, out)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        res = dict(out)
+    assert [res[r][:3] for r in range(world)] == [(0, 0, 2), (1, 1, 2)]
+    assert res[0][3] == res[1][3] == 3.5          # max over ranks
+    assert res[0][4] != res[1][4]                 # independent problems per rank
+
+
+def test_single_rank_defaults(monkeypatch):
+    for k in ("RANK", "LOCAL_RANK", "WORLD_SIZE"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.dist_env() == (0, 0, 1)
+    assert bench.max_over_ranks(2.5, 1) == 2.5
+
+
+def test_visible_rows_match_flop_count():
+    from exact_attention_forward_sm_gb300 import workloads as wl
+    for case in (wl.make_case(2, 3, 1, 300, 300, 64, "bf16", True, seed=1),
+                 wl.make_case(0, 2, 2, 0, 0, 64, "fp16", True, seed=2,
+                              seqlens_q=[5, 130, 64], seqlens_k=[9, 130, 70]),
+                 wl.make_case(1, 4, 4, 100, 50, 128, "bf16", False, seed=3)):
+        vis = bench._visible_per_row(case)
+        assert vis.shape[0] == case.lse_rows()
+        assert 4 * case.D * int(vis.sum()) == wl.attention_flops(case)
