@@ -537,14 +537,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 1; j <= w.n_max && ok; ++j) {
             const int vidx = used + 2 * j - 1, kidx = used + 2 * j;
             const bool pv = j - 1 < n, qk = j < n;
-            if (pv) {
-              // the first O += P V of a unit overwrites O_T: the previous
-              // unit's epilogue must have read it out
-              ok = wait(p_half(T, 0), p_seen & 1) &&
-                   (j > 1 || o_done == 0 || wait(o_free(T), (o_done - 1) & 1)) &&
-                   wait(kv_full(vidx % L::kStages), kv_par(vidx));
-            }
+            // K/V (and, for a unit's first O += P V, the previous unit's
+            // epilogue having read O_T out) are checked first: these barriers
+            // completed long ago, and each check costs a shared-memory round
+            // trip that now hides behind the wait for this tile's softmax
+            if (pv)
+              ok = wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
+                   (j > 1 || o_done == 0 || wait(o_free(T), (o_done - 1) & 1));
             if (ok && qk) ok = wait(kv_full(kidx % L::kStages), kv_par(kidx));
+            if (ok && pv) ok = wait(p_half(T, 0), p_seen & 1);
             FA_TRACE_AT(i == 0 && j < 64, 1024 + j * 8 + 2 + 2 * T);
             ok = ok && take_turn();
             if (!ok) break;
