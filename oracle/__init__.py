@@ -8,7 +8,8 @@ this package imports nothing from the product.
 The arithmetic lives in ``attention_oracle.c`` (plain C, fp64, OpenMP over
 independent rows); this module only builds it with gcc and marshals arrays.
 
-* :func:`attention` — the plain definition (full score row, softmax, O, LSE).
+* :func:`attention` — the plain definition (full score row, softmax, O, LSE),
+  optionally with a local window, a tanh soft cap and ALiBi slopes.
 * :func:`attention_online` — the streaming restatement with the lazy-rescale
   threshold and max lagging of the fork's v1.7 release notes (section 1.2),
   plus its skip / rescale counters and the largest P.
@@ -61,6 +62,9 @@ def _load():
                   ctypes.c_double, c_int, i32p, i32p, i64p, ctypes.c_int64]
         lib.oracle_attention.argtypes = common + [c_int]
         lib.oracle_attention.restype = c_int
+        lib.oracle_attention_ex.argtypes = (
+            common[:13] + [c_int, c_int, ctypes.c_double, f64p] + common[13:] + [c_int])
+        lib.oracle_attention_ex.restype = c_int
         lib.oracle_attention_online.argtypes = common + [
             c_int, ctypes.c_double, c_int, i64p, i64p, f64p, c_int]
         lib.oracle_attention_online.restype = c_int
@@ -105,8 +109,13 @@ def _prep(q, k, v, B, Hq, Hkv, Sq, Sk, D, cu_seqlens_q, cu_seqlens_k, rows):
 
 
 def attention(q, k, v, B, Hq, Hkv, Sq, Sk, D, scale, causal,
-              cu_seqlens_q=None, cu_seqlens_k=None, rows=None, nthreads=0):
+              cu_seqlens_q=None, cu_seqlens_k=None, rows=None, nthreads=0,
+              window_left=-1, window_right=-1, softcap=0.0, alibi_slopes=None):
     """Plain-definition attention in fp64 for the requested rows.
+
+    Optional variants: a local window (``window_left``, ``window_right``; a
+    negative bound is unbounded), a tanh soft cap (``softcap`` > 0) and ALiBi
+    (``alibi_slopes``: one slope per query head, natural-log units).
 
     Returns ``(o_rows [nrows, D] float64, lse_rows [nrows] float64)``; with
     ``rows=None`` every row, in LSE-index order.
@@ -118,10 +127,19 @@ def attention(q, k, v, B, Hq, Hkv, Sq, Sk, D, scale, causal,
     o = np.zeros((n, D), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
     i32n = ctypes.POINTER(ctypes.c_int32)()
-    rc = lib.oracle_attention(
+    slopes = None
+    if alibi_slopes is not None:
+        a = alibi_slopes.detach().cpu().double().numpy() if hasattr(alibi_slopes, "detach") \
+            else alibi_slopes
+        slopes = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+        if slopes.shape != (Hq,):
+            raise ValueError("alibi_slopes must hold one slope per query head")
+    rc = lib.oracle_attention_ex(
         _ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float), _ptr(v, ctypes.c_float),
         _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
         B, Hq, Hkv, Sq, Sk, D, float(scale), int(bool(causal)),
+        int(window_left), int(window_right), float(softcap),
+        _ptr(slopes, ctypes.c_double) if slopes is not None else ctypes.POINTER(ctypes.c_double)(),
         _ptr(cu_q, ctypes.c_int32) if cu_q is not None else i32n,
         _ptr(cu_k, ctypes.c_int32) if cu_k is not None else i32n,
         _ptr(rows, ctypes.c_int64), n, int(nthreads))

@@ -38,10 +38,27 @@
  * packed rows by h * total_q + t (t = global token index).  Outputs are
  * written per requested row: o_rows[r * D + d], lse_rows[r].
  *
+ *  oracle_attention_ex()      the same definition with the score variants the
+ *                             fork's public API lists next to the plain forward
+ *                             (v1.7 release notes, section 2 "Public APIs":
+ *                             window, ALiBi, softcap; validated in section 4.1
+ *                             tests 5-7 and section 4.6): a local window
+ *                             (left, right), a tanh soft cap and ALiBi slopes.
+ *                             oracle_attention() is this function with every
+ *                             variant switched off.
+ *
  * Readings of points the pages leave open (each is also listed in the design
  * notes): LSE is the natural log over the scaled scores; causal masking with
  * Sq != Sk is aligned bottom-right (key j visible iff j <= i + Lk - Lq); a row
- * with no visible key gets O = 0 and LSE = -inf.
+ * with no visible key gets O = 0 and LSE = -inf.  For the variants, with
+ * diag = i + Lk - Lq the bottom-right aligned diagonal of row i:
+ *   window (left, right): key j visible iff diag - left <= j <= diag + right,
+ *     a negative bound meaning unbounded on that side (so window (0, 0) with
+ *     Sq = Sk leaves only key i and O = V[i], as section 4.6 reports); causal
+ *     additionally requires j <= diag;
+ *   softcap c > 0: s = c * tanh(scale * <q, k> / c);
+ *   ALiBi: s gains -slope[h] * |diag - j| (natural-log units, after the soft
+ *     cap), one slope per query head.
  */
 #include <math.h>
 #include <stdint.h>
@@ -106,6 +123,20 @@ static int64_t visible_keys(const row_ref *r, int causal) {
     return n < 0 ? 0 : n;
 }
 
+/* Visible key range [*lo, *hi] of a row under causal masking and a local
+ * window (negative bound = unbounded); returns the number of visible keys. */
+static int64_t visible_range(const row_ref *r, int causal, int window_left,
+                             int window_right, int64_t *lo, int64_t *hi) {
+    const int64_t diag = r->i + r->lk - r->lq;
+    int64_t a = 0, b = r->lk - 1;
+    if (causal && diag < b) b = diag;
+    if (window_right >= 0 && diag + window_right < b) b = diag + window_right;
+    if (window_left >= 0 && diag - window_left > a) a = diag - window_left;
+    *lo = a;
+    *hi = b;
+    return b >= a ? b - a + 1 : 0;
+}
+
 static int check_args(int B, int Hq, int Hkv, int Sq, int Sk, int D,
                       const int32_t *cu_q, const int32_t *cu_k) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return -1;
@@ -114,13 +145,15 @@ static int check_args(int B, int Hq, int Hkv, int Sq, int Sk, int D,
     return 0;
 }
 
-int oracle_attention(const float *q, const float *k, const float *v,
-                     double *o_rows, double *lse_rows,
-                     int B, int Hq, int Hkv, int Sq, int Sk, int D,
-                     double scale, int causal,
-                     const int32_t *cu_q, const int32_t *cu_k,
-                     const int64_t *rows, int64_t nrows, int nthreads) {
+int oracle_attention_ex(const float *q, const float *k, const float *v,
+                        double *o_rows, double *lse_rows,
+                        int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                        double scale, int causal, int window_left, int window_right,
+                        double softcap, const double *alibi_slopes,
+                        const int32_t *cu_q, const int32_t *cu_k,
+                        const int64_t *rows, int64_t nrows, int nthreads) {
     if (check_args(B, Hq, Hkv, Sq, Sk, D, cu_q, cu_k)) return -1;
+    if (!(softcap >= 0.0)) return -1;
     int bad = 0;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
@@ -136,30 +169,37 @@ int oracle_attention(const float *q, const float *k, const float *v,
             row_ref ref = locate_row(rows[r], B, Hq, Hkv, Sq, Sk, cu_q, cu_k);
             double *out = o_rows + r * D;
             if (!ref.ok) { bad |= 1; continue; }
-            int64_t n = visible_keys(&ref, causal);
+            int64_t j0, j1;
+            int64_t n = visible_range(&ref, causal, window_left, window_right, &j0, &j1);
             if (n > s_cap) {
                 free(s);
                 s = (double *)malloc((size_t)n * sizeof(double));
                 s_cap = n;
             }
             const float *qr = q + (ref.q_tok * Hq + ref.h) * (int64_t)D;
-            /* scores s_j = scale * <q, k_j> over the visible keys */
+            const int64_t diag = ref.i + ref.lk - ref.lq;
+            /* scores over the visible keys j0 .. j1: s = scale * <q, k_j>,
+               then the soft cap, then the ALiBi distance penalty */
             double m = -INFINITY;
-            for (int64_t j = 0; j < n; j++) {
+            for (int64_t c = 0; c < n; c++) {
+                const int64_t j = j0 + c;
                 const float *kr = k + ((ref.k_tok0 + j) * Hkv + ref.hkv) * (int64_t)D;
                 double acc = 0.0;
                 for (int d = 0; d < D; d++) acc += (double)qr[d] * (double)kr[d];
-                s[j] = scale * acc;
-                if (s[j] > m) m = s[j];
+                double sc = scale * acc;
+                if (softcap > 0.0) sc = softcap * tanh(sc / softcap);
+                if (alibi_slopes) sc -= alibi_slopes[ref.h] * (double)llabs(diag - j);
+                s[c] = sc;
+                if (sc > m) m = sc;
             }
             for (int d = 0; d < D; d++) out[d] = 0.0;
             if (n == 0) { lse_rows[r] = -INFINITY; continue; }
             /* softmax weights relative to the row max, then O = P V / l */
             double l = 0.0;
-            for (int64_t j = 0; j < n; j++) {
-                double p = exp(s[j] - m);
+            for (int64_t c = 0; c < n; c++) {
+                double p = exp(s[c] - m);
                 l += p;
-                const float *vr = v + ((ref.k_tok0 + j) * Hkv + ref.hkv) * (int64_t)D;
+                const float *vr = v + ((ref.k_tok0 + j0 + c) * Hkv + ref.hkv) * (int64_t)D;
                 for (int d = 0; d < D; d++) out[d] += p * (double)vr[d];
             }
             for (int d = 0; d < D; d++) out[d] /= l;
@@ -168,6 +208,17 @@ int oracle_attention(const float *q, const float *k, const float *v,
         free(s);
     }
     return bad ? -2 : 0;
+}
+
+int oracle_attention(const float *q, const float *k, const float *v,
+                     double *o_rows, double *lse_rows,
+                     int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                     double scale, int causal,
+                     const int32_t *cu_q, const int32_t *cu_k,
+                     const int64_t *rows, int64_t nrows, int nthreads) {
+    return oracle_attention_ex(q, k, v, o_rows, lse_rows, B, Hq, Hkv, Sq, Sk, D, scale,
+                               causal, -1, -1, 0.0, NULL, cu_q, cu_k, rows, nrows,
+                               nthreads);
 }
 
 int oracle_attention_online(const float *q, const float *k, const float *v,
