@@ -19,7 +19,7 @@ import threading
 __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
     "FA_ERR_BAD_SEQLENS", "FA_DTYPE_FP16", "FA_DTYPE_BF16", "LibraryMissing", "FaError",
-    "library_path", "load_library", "fa_fwd", "fa_get_device_error", "fa_debug_wait_timeout",
+    "library_path", "load_library", "fa_fwd", "fa_fwd_ex", "fa_get_device_error", "fa_debug_wait_timeout",
     "fa_debug_trace_read",
     "fa_status_string", "fa_version", "attention_forward", "EXPORTED_SYMBOLS",
 ]
@@ -33,7 +33,7 @@ FA_ERR_BAD_SEQLENS = 5
 FA_DTYPE_FP16 = 0
 FA_DTYPE_BF16 = 1
 
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_get_device_error", "fa_debug_wait_timeout",
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_ex", "fa_get_device_error", "fa_debug_wait_timeout",
                     "fa_debug_trace_read", "fa_status_string", "fa_version")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +74,8 @@ def load_library():
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
                                vp, vp, vp, i32]
         lib.fa_fwd.restype = i32
+        lib.fa_fwd_ex.argtypes = lib.fa_fwd.argtypes + [i32, i32, f32, vp]
+        lib.fa_fwd_ex.restype = i32
         lib.fa_get_device_error.argtypes = [vp]
         lib.fa_get_device_error.restype = i32
         lib.fa_debug_wait_timeout.argtypes = [ctypes.c_longlong, vp]
@@ -114,6 +116,18 @@ def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal,
                       _addr(cu_seqlens_q), _addr(cu_seqlens_k), _stream(stream), int(dtype))
 
 
+def fa_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal,
+              cu_seqlens_q, cu_seqlens_k, stream, dtype, window_left=-1, window_right=-1,
+              softcap=0.0, alibi_slopes=None) -> int:
+    """Call the C ``fa_fwd_ex`` (local window, soft cap, ALiBi slopes)."""
+    lib = load_library()
+    return lib.fa_fwd_ex(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(Hq),
+                         int(Hkv), int(Sq), int(Sk), int(D), float(scale), int(causal),
+                         _addr(cu_seqlens_q), _addr(cu_seqlens_k), _stream(stream), int(dtype),
+                         int(window_left), int(window_right), float(softcap),
+                         _addr(alibi_slopes))
+
+
 def fa_get_device_error(stream=None) -> int:
     return load_library().fa_get_device_error(_stream(stream))
 
@@ -138,12 +152,16 @@ def fa_version() -> int:
 
 
 def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens_q=None,
-                      cu_seqlens_k=None, out=None, lse=None, stream=None):
+                      cu_seqlens_k=None, out=None, lse=None, stream=None,
+                      window_size=(-1, -1), softcap=0.0, alibi_slopes=None):
     """Exact attention forward on CUDA tensors; returns ``(out, lse)``.
 
     Dense: q [B, Sq, Hq, D], k/v [B, Sk, Hkv, D] -> out like q, lse [B, Hq, Sq].
     Packed: q [total_q, Hq, D], k/v [total_k, Hkv, D] with int32 cu_seqlens of
     B + 1 offsets -> out like q, lse [Hq, total_q].
+    ``window_size`` (left, right; -1 = unbounded), ``softcap`` and
+    ``alibi_slopes`` (fp32 CUDA tensor [Hq]) select the score variants of
+    ``fa_fwd_ex``.
     """
     import torch
 
@@ -170,8 +188,13 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens_q=None,
         lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    st = fa_fwd(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, D, scale, int(bool(causal)),
-                cu_seqlens_q, cu_seqlens_k, stream, dtype)
+    if alibi_slopes is not None and (alibi_slopes.dtype != torch.float32
+                                     or alibi_slopes.shape != (Hq,)
+                                     or not alibi_slopes.is_contiguous()):
+        raise FaError(FA_ERR_INVALID_ARG, "attention_forward (alibi_slopes)")
+    st = fa_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, D, scale, int(bool(causal)),
+                   cu_seqlens_q, cu_seqlens_k, stream, dtype, window_size[0], window_size[1],
+                   softcap, alibi_slopes)
     if st != FA_OK:
         raise FaError(st)
     return out, lse

@@ -116,34 +116,23 @@ bool make_map(CUtensorMap *m, const void *base, bool bf16, int D, int heads, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-extern "C" {
-
-int fa_version(void) { return 100; }  // 0.1.0
-
-const char *fa_status_string(int status) {
-  switch (status) {
-    case FA_OK: return "ok";
-    case FA_ERR_INVALID_ARG: return "invalid argument";
-    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
-    case FA_ERR_CUDA: return "CUDA error";
-    case FA_ERR_TIMEOUT: return "device pipeline wait timed out";
-    case FA_ERR_BAD_SEQLENS: return "cu_seqlens inconsistent with Sq / Sk";
-    default: return "unknown status";
-  }
-}
-
-int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
-           int Hkv, int Sq, int Sk, int D, float scale, int causal,
-           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, fa_stream_t stream,
-           int dtype) {
+// Shared body of fa_fwd and fa_fwd_ex.  Window bounds < 0 are unbounded;
+// softcap 0 and alibi == nullptr switch those variants off.
+int forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+            int Hkv, int Sq, int Sk, int D, float scale, int causal,
+            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, fa_stream_t stream,
+            int dtype, int window_left, int window_right, float softcap,
+            const float *alibi_slopes) {
   // ---------------------------------------------------------- argument checks
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(softcap) || softcap < 0.f) return FA_ERR_INVALID_ARG;
+  const float cap_k = softcap > 0.f ? 2.f * scale * 1.4426950408889634f / softcap : 0.f;
+  if (!std::isfinite(cap_k)) return FA_ERR_INVALID_ARG;
+  if (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)) return FA_ERR_INVALID_ARG;
   const bool varlen = cu_seqlens_q != nullptr;
   if (varlen != (cu_seqlens_k != nullptr)) return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
@@ -155,6 +144,16 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   if (varlen && ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) ||
                  (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u)))
     return FA_ERR_INVALID_ARG;
+
+  // Window bounds: negative = unbounded; a bound beyond Sq + Sk (no row is
+  // that far from a key) is unbounded too.  Causal masking is the right bound
+  // 0 intersected with any right bound >= 0.
+  const int64_t span = (int64_t)Sq + Sk;
+  int win_l = (window_left < 0 || window_left > span) ? -1 : window_left;
+  int win_r = (window_right < 0 || window_right > span) ? -1 : window_right;
+  if (causal) win_r = 0;
+  const bool ext = win_l >= 0 || win_r > 0 || softcap > 0.f || alibi_slopes != nullptr;
+  const bool plain_causal = !ext && win_r == 0;
 
   const int group = Hq / Hkv;
   const bool pair_heads = (group % 2) == 0;
@@ -207,6 +206,12 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   p.total_units = (int)units;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.threshold = FA_RESCALE_THRESHOLD;
+  p.win_l = win_l;
+  p.win_r = win_r;
+  p.reverse_rows = (win_l < 0 && win_r >= 0) ? 1 : 0;
+  p.cap_k = cap_k;
+  p.cap_l2 = softcap * 1.4426950408889634f;
+  p.alibi = alibi_slopes;
   p.wait_limit = kDefaultWaitLimit;
   p.status = status;
   p.trace = nullptr;
@@ -222,11 +227,54 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   a.device = device;
 
   cudaError_t e;
-  if (D == 64)
-    e = bf16 ? fa::launch_d64_bf16(a, causal, varlen) : fa::launch_d64_fp16(a, causal, varlen);
-  else
-    e = bf16 ? fa::launch_d128_bf16(a, causal, varlen) : fa::launch_d128_fp16(a, causal, varlen);
+  if (ext) {
+    if (D == 64)
+      e = bf16 ? fa::launch_ext_d64_bf16(a, varlen) : fa::launch_ext_d64_fp16(a, varlen);
+    else
+      e = bf16 ? fa::launch_ext_d128_bf16(a, varlen) : fa::launch_ext_d128_fp16(a, varlen);
+  } else if (D == 64) {
+    e = bf16 ? fa::launch_d64_bf16(a, plain_causal, varlen)
+             : fa::launch_d64_fp16(a, plain_causal, varlen);
+  } else {
+    e = bf16 ? fa::launch_d128_bf16(a, plain_causal, varlen)
+             : fa::launch_d128_fp16(a, plain_causal, varlen);
+  }
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }  // 0.1.0
+
+const char *fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case FA_ERR_BAD_SEQLENS: return "cu_seqlens inconsistent with Sq / Sk";
+    default: return "unknown status";
+  }
+}
+
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+           int Hkv, int Sq, int Sk, int D, float scale, int causal,
+           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, fa_stream_t stream,
+           int dtype) {
+  return forward(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, cu_seqlens_q,
+                 cu_seqlens_k, stream, dtype, -1, -1, 0.f, nullptr);
+}
+
+int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+              int Hkv, int Sq, int Sk, int D, float scale, int causal,
+              const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, fa_stream_t stream,
+              int dtype, int window_left, int window_right, float softcap,
+              const float *alibi_slopes) {
+  return forward(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, cu_seqlens_q,
+                 cu_seqlens_k, stream, dtype, window_left, window_right, softcap, alibi_slopes);
 }
 
 int fa_get_device_error(fa_stream_t stream) {

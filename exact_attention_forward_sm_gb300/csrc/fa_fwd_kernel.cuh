@@ -87,6 +87,13 @@ struct FwdParams {
   int total_units;          // units to process (packed: an upper bound)
   float scale_log2;         // scale * log2(e)
   float threshold;          // lazy-rescale threshold, log2 units
+  // score variants (kernels instantiated with EXT only)
+  int win_l, win_r;         // local window around the diagonal, -1 = unbounded;
+                            // a causal mask arrives here as win_r = 0
+  int reverse_rows;         // later row blocks see more keys: schedule them first
+  float cap_k;              // soft cap c: 2 * scale * log2(e) / c, 0 = no soft cap
+  float cap_l2;             // soft cap c: c * log2(e)
+  const float *alibi;       // ALiBi slope per query head (natural-log units) or null
   long long wait_limit;     // bounded-wait limit in SM clock cycles
   int *status;              // device status word (first error wins)
   unsigned long long *trace;  // clock64 pipeline trace (trace builds only)
@@ -164,8 +171,10 @@ struct Work {
   int k_row0;        // tensor-map row of key 0 of the sequence
   int map_b;         // tensor-map batch coordinate
   int64_t o_row0;    // global token index of query row 0 of the sequence
-  int n_kv[2];       // K/V tiles each query tile visits
-  int n_max;
+  int n_kv[2];       // K/V tiles each query tile visits ...
+  int kv_begin[2];   // ... starting at this K/V tile of the sequence
+  int kv_ub;         // first K/V tile loaded for the unit (min over its tiles)
+  int n_max;         // K/V tiles loaded for the unit (the union of both ranges)
 };
 
 template <bool CAUSAL>
@@ -179,6 +188,24 @@ __device__ __forceinline__ int tile_kv_count(int m0, int lq, int lk) {
   return min(full, last_key / kBlockN + 1);
 }
 
+// K/V tiles visited by the query tile of rows [m0, m0 + 128) under a local
+// window (kernels with score variants): keys [lo, hi] where lo is the left
+// bound of the first row and hi the right bound of the last row.  Returns the
+// count and sets *begin.  With both bounds >= 0 or unbounded, the ranges of two
+// consecutive row tiles overlap or touch, so their union is contiguous.
+__device__ __forceinline__ int window_kv_range(const FwdParams &p, int m0, int lq, int lk,
+                                               int *begin) {
+  *begin = 0;
+  if (m0 >= lq || lk <= 0) return 0;
+  const int off = lk - lq;
+  const int last_row = min(m0 + kBlockM, lq) - 1;
+  const int lo = p.win_l < 0 ? 0 : max(0, m0 + off - p.win_l);
+  const int hi = p.win_r < 0 ? lk - 1 : min(lk - 1, last_row + off + p.win_r);
+  if (hi < lo) return 0;
+  *begin = lo / kBlockN;
+  return hi / kBlockN - *begin + 1;
+}
+
 // The i-th unit of this CTA (snake over the heavy-first unit order).
 __device__ __forceinline__ int unit_of(int i) {
   const int G = gridDim.x;
@@ -189,7 +216,7 @@ __device__ __forceinline__ int unit_of(int i) {
 // Dense: the row-unit index (heaviest causal rows first) is the slowest-varying
 // part of the unit index.  Packed: units are numbered sequence by sequence
 // (heaviest rows of a sequence first); the warp scans cu_seqlens cooperatively.
-template <bool CAUSAL, bool VARLEN>
+template <bool CAUSAL, bool VARLEN, bool EXT>
 __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
   Work w;
   w.valid = 0;
@@ -251,7 +278,7 @@ __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
     w.map_b = 0;
     w.o_row0 = q0;
   }
-  if (CAUSAL) ru = n_ru - 1 - ru;  // heavier (later) rows first
+  if (CAUSAL || (EXT && p.reverse_rows)) ru = n_ru - 1 - ru;  // heavier (later) rows first
   w.b = b;
   if (p.pair_heads) {
     w.head[0] = 2 * hu;
@@ -263,9 +290,23 @@ __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
     w.m0[1] = ru * 2 * kBlockM + kBlockM;
   }
   w.hkv = w.head[0] / p.group;
-  w.n_kv[0] = tile_kv_count<CAUSAL>(w.m0[0], w.lq, w.lk);
-  w.n_kv[1] = tile_kv_count<CAUSAL>(w.m0[1], w.lq, w.lk);
-  w.n_max = max(w.n_kv[0], w.n_kv[1]);
+  if (EXT) {
+    w.n_kv[0] = window_kv_range(p, w.m0[0], w.lq, w.lk, &w.kv_begin[0]);
+    w.n_kv[1] = window_kv_range(p, w.m0[1], w.lq, w.lk, &w.kv_begin[1]);
+  } else {
+    w.n_kv[0] = tile_kv_count<CAUSAL>(w.m0[0], w.lq, w.lk);
+    w.n_kv[1] = tile_kv_count<CAUSAL>(w.m0[1], w.lq, w.lk);
+    w.kv_begin[0] = w.kv_begin[1] = 0;
+  }
+  if (w.n_kv[0] == 0 && w.n_kv[1] == 0) {
+    w.kv_ub = 0;
+    w.n_max = 0;
+  } else {
+    const int b0 = w.n_kv[0] ? w.kv_begin[0] : w.kv_begin[1];
+    const int b1 = w.n_kv[1] ? w.kv_begin[1] : w.kv_begin[0];
+    w.kv_ub = min(b0, b1);
+    w.n_max = max(w.kv_begin[0] + w.n_kv[0], w.kv_begin[1] + w.n_kv[1]) - w.kv_ub;
+  }
   w.valid = 1;
   return w;
 }
@@ -311,7 +352,7 @@ __device__ __forceinline__ void softmax_chunk(const float *x, float scale_log2, 
   tmem_st16(p_addr, pk);
 }
 
-template <int D, bool BF16, bool CAUSAL, bool VARLEN>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -393,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; ok; ++i) {
         const int unit = unit_of(i);
         if (unit >= p.total_units) break;
-        const Work w = decode_work<CAUSAL, VARLEN>(p, unit, lane);
+        const Work w = decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane);
         if (!w.valid) continue;
         if (lane == 0) {
 #pragma unroll
@@ -424,7 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(kv_full(s), L::kTileBytes);
               for (int c = 0; c < L::kChunks; ++c)
                 tma_load_4d(sbase + L::kKVOff + s * L::kTileBytes + c * kChunkBytes, tm,
-                            kv_full(s), c * 64, w.hkv, w.k_row0 + j * kBlockN, w.map_b, pol_kv);
+                            kv_full(s), c * 64, w.hkv, w.k_row0 + (w.kv_ub + j) * kBlockN,
+                            w.map_b, pol_kv);
               issued = idx + 1;
             }
           }
@@ -511,49 +553,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; ok; ++i) {
         const int unit = unit_of(i);
         if (unit >= p.total_units) break;
-        const Work w = decode_work<CAUSAL, VARLEN>(p, unit, lane);
+        const Work w = decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane);
         if (!w.valid || w.n_max == 0) continue;
         if (lane == 0) {
           const int n = w.n_kv[T], n_other = w.n_kv[1 - T];
-          // step 0: S_T = Q_T K(0)^T
-          const int k0idx = used;
-          if (n > 0) {
-            ok = wait(kv_full(k0idx % L::kStages), kv_par(k0idx)) && wait(q_full(T), q_used & 1);
-            ++q_used;
-          }
-          ok = ok && take_turn();
-          if (ok) {
-            if (n > 0) {
-              tc_fence_after();
-              issue_qk(k0idx);
+          // bracket u = 0 .. n_max of the unit: O_T += P_T V(u-1) if this
+          // tile read load u-1, then S_T = Q_T K(u)^T if it reads load u.
+          // Both issuers walk every bracket, so the turns stay paired even
+          // when the tiles' K/V ranges differ (local windows).
+          const int off = w.kv_begin[T] - w.kv_ub;
+          const int off_other = w.kv_begin[1 - T] - w.kv_ub;
+          auto other_reads = [&](int u) { return u >= off_other && u < off_other + n_other; };
+          for (int u = 0; u <= w.n_max && ok; ++u) {
+            const int jq = u - off;  // this tile's step: S_T = Q_T K(jq)^T
+            const bool qk = jq >= 0 && jq < n, pv = jq >= 1 && jq <= n;
+            const int kidx = used + 2 * u, vidx = used + 2 * u - 1;
+            if (qk && jq == 0) {  // first S_T of the unit: Q_T must have landed
+              ok = wait(q_full(T), q_used & 1);
+              ++q_used;
             }
-            pass_turn();
-            if (n > 0) {
-              tc_commit(s_full(T));
-              if (n == 1) tc_commit(q_empty(T));  // last S_T of this unit issued
-              release(k0idx, n_other > 0);
-            }
-          }
-          for (int j = 1; j <= w.n_max && ok; ++j) {
-            const int vidx = used + 2 * j - 1, kidx = used + 2 * j;
-            const bool pv = j - 1 < n, qk = j < n;
             // K/V (and, for a unit's first O += P V, the previous unit's
             // epilogue having read O_T out) are checked first: these barriers
             // completed long ago, and each check costs a shared-memory round
             // trip that now hides behind the wait for this tile's softmax
-            if (pv)
+            if (ok && pv)
               ok = wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
-                   (j > 1 || o_done == 0 || wait(o_free(T), (o_done - 1) & 1));
+                   (jq > 1 || o_done == 0 || wait(o_free(T), (o_done - 1) & 1));
             if (ok && qk) ok = wait(kv_full(kidx % L::kStages), kv_par(kidx));
             if (ok && pv) ok = wait(p_half(T, 0), p_seen & 1);
-            FA_TRACE_AT(i == 0 && j < 64, 1024 + j * 8 + 2 + 2 * T);
+            FA_TRACE_AT(i == 0 && u < 64, 1024 + u * 8 + 2 + 2 * T);
             ok = ok && take_turn();
             if (!ok) break;
+            tc_fence_after();
             if (pv) {
               // keys 0-63 go to the tensor pipe while the softmax still works
               // on keys 64-127; the turn is held until the bracket is complete
-              tc_fence_after();
-              issue_pv_half(vidx, 0, j == 1);
+              issue_pv_half(vidx, 0, jq == 1);
               if (!wait(p_half(T, 1), p_seen & 1)) {
                 ok = false;
                 break;
@@ -564,18 +599,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (qk) issue_qk(kidx);
             pass_turn();
-            FA_TRACE_AT(i == 0 && j < 64, 1024 + j * 8 + 3 + 2 * T);
+            FA_TRACE_AT(i == 0 && u < 64, 1024 + u * 8 + 3 + 2 * T);
             if (pv) {
-              if (j == n) {
+              if (jq == n) {
                 tc_commit(o_ready(T));  // tile T of this unit is complete
                 ++o_done;
               }
-              release(vidx, j - 1 < n_other);
+              release(vidx, other_reads(u - 1));
             }
             if (qk) {
               tc_commit(s_full(T));
-              if (j == n - 1) tc_commit(q_empty(T));
-              release(kidx, j < n_other);
+              if (jq == n - 1) tc_commit(q_empty(T));  // last S_T of this unit issued
+              release(kidx, other_reads(u));
             }
           }
           used += 2 * w.n_max;
@@ -597,7 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t s_addr = lane_base + t * 128;
     const uint32_t o_addr = lane_base + 256 + t * D;
-    const float scale_log2 = p.scale_log2;
+    // plain kernels keep raw scores and fold scale * log2(e) into the exps;
+    // kernels with score variants turn every score into log2 units first
+    const float scale_log2 = EXT ? 1.f : p.scale_log2;
     const float neg_thr = -p.threshold;
     // every lane of a warp must agree before the warp-wide tcgen05.ld / st
     auto warp_wait = [&](uint32_t bar, uint32_t parity) {
@@ -616,13 +653,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0;; ++i) {
       const int unit = unit_of(i);
       if (unit >= p.total_units) break;
-      const Work w = decode_work<CAUSAL, VARLEN>(p, unit, lane);
+      const Work w = decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane);
       if (!w.valid || w.m0[t] >= w.lq) continue;  // no rows of this tile
       const int m0 = w.m0[t];        // per-tile fields read once per unit
       const int n_kv = w.n_kv[t];
       const int lq = w.lq, lk = w.lk;
       const int qi = m0 + row;       // query row within its sequence
       const int diag = qi + lk - lq;  // last visible key of this row (causal)
+      [[maybe_unused]] const int kv_begin = w.kv_begin[t];
+      [[maybe_unused]] const float slope_l2 =
+          (EXT && p.alibi) ? p.alibi[w.head[t]] * 1.4426950408889634f : 0.f;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n_kv && ok; ++j) {
         if (!warp_wait(s_full(t), s_seen & 1)) { ok = false; break; }
@@ -634,10 +674,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld128_wait(s_addr, sr);
         float *s = reinterpret_cast<float *>(sr);
         FA_TRACE_AT(tr, (t * 64 + j) * 8 + 1);
-        const int k0 = j * kBlockN;
-        const bool need_mask =
-            (k0 + kBlockN > lk) || (CAUSAL && (k0 + kBlockN - 1 > m0 + lk - lq));
-        if (need_mask) {
+        const int k0 = (EXT ? kv_begin + j : j) * kBlockN;
+        if constexpr (EXT) {
+          // scores in log2 units: soft cap c tanh(scale s / c), written as
+          // c (1 - 2 / (1 + e^(2 scale s / c))) with the hardware exp2 and
+          // reciprocal, then the ALiBi penalty -slope |diag - key|
+          if (p.cap_k != 0.f) {
+            const float ck = p.cap_k, cl = p.cap_l2;
+#pragma unroll
+            for (int c = 0; c < kBlockN; ++c)
+              s[c] = fmaf(rcp_approx(1.f + ex2(s[c] * ck)), -2.f * cl, cl);
+          } else {
+            const float sl2 = p.scale_log2;
+#pragma unroll
+            for (int c = 0; c < kBlockN; ++c) s[c] *= sl2;
+          }
+          if (p.alibi) {
+            const float d0 = (float)(diag - k0);
+#pragma unroll
+            for (int c = 0; c < kBlockN; ++c) s[c] = fmaf(-slope_l2, fabsf(d0 - (float)c), s[c]);
+          }
+          const int last_row = min(m0 + kBlockM, lq) - 1;
+          const bool need_mask = (k0 + kBlockN > lk) ||
+                                 (p.win_r >= 0 && k0 + kBlockN - 1 > m0 + lk - lq + p.win_r) ||
+                                 (p.win_l >= 0 && k0 < last_row + lk - lq - p.win_l);
+          if (need_mask) {
+            // keys [lo, hi) of this tile are visible to the row
+            const int lo = p.win_l < 0 ? 0 : diag - p.win_l - k0;
+            const int hi = min(lk, p.win_r < 0 ? lk : diag + p.win_r + 1) - k0;
+#pragma unroll
+            for (int c = 0; c < kBlockN; ++c) s[c] = (c >= lo && c < hi) ? s[c] : -INFINITY;
+          }
+        } else if ((k0 + kBlockN > lk) || (CAUSAL && (k0 + kBlockN - 1 > m0 + lk - lq))) {
           int lim = lk - k0;  // keys [0, lim) of this tile are visible to the row
           if (CAUSAL) lim = min(lim, diag - k0 + 1);
 #pragma unroll

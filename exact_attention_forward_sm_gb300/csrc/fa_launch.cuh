@@ -15,9 +15,9 @@ struct LaunchArgs {
   int device;
 };
 
-template <int D, bool BF16, bool CAUSAL, bool VARLEN>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT = false>
 cudaError_t launch_fwd(const LaunchArgs &a) {
-  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN>;
+  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN, EXT>;
   // opt in to the large dynamic shared memory once per device
   static std::atomic<unsigned long long> configured{0};
   const unsigned long long bit = 1ull << (a.device & 63);
@@ -43,9 +43,21 @@ cudaError_t launch_fwd(const LaunchArgs &a) {
                   : launch_fwd<D, BF16, false, false>(a);                       \
   }
 
+// Kernels with score variants (local window, soft cap, ALiBi): causal masking
+// is folded into the window, so only the packed flag selects the instance.
+#define FA_DEFINE_EXT_LAUNCHER(NAME, D, BF16)                                   \
+  cudaError_t NAME(const LaunchArgs &a, bool varlen) {                         \
+    return varlen ? launch_fwd<D, BF16, false, true, true>(a)                   \
+                  : launch_fwd<D, BF16, false, false, true>(a);                 \
+  }
+
 cudaError_t launch_d64_fp16(const LaunchArgs &a, bool causal, bool varlen);
 cudaError_t launch_d64_bf16(const LaunchArgs &a, bool causal, bool varlen);
 cudaError_t launch_d128_fp16(const LaunchArgs &a, bool causal, bool varlen);
 cudaError_t launch_d128_bf16(const LaunchArgs &a, bool causal, bool varlen);
+cudaError_t launch_ext_d64_fp16(const LaunchArgs &a, bool varlen);
+cudaError_t launch_ext_d64_bf16(const LaunchArgs &a, bool varlen);
+cudaError_t launch_ext_d128_fp16(const LaunchArgs &a, bool varlen);
+cudaError_t launch_ext_d128_bf16(const LaunchArgs &a, bool varlen);
 
 }  // namespace fa

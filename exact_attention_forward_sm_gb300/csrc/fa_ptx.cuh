@@ -360,4 +360,11 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 1 / x on the special-function unit (rcp.approx.ftz.f32; 1 / inf = +0).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 }  // namespace fa

@@ -17,6 +17,10 @@ Recipe (all draws on the CPU, ``torch.Generator().manual_seed(seed)``):
   by 0.5 * (blk mod 25) log2 units at block blk >= 1, so successive block maxima
   rise by 0 .. 12 log2 units and both skipped and performed lazy rescales occur
   when the keys are walked in ascending order.
+
+Score variants (local window, soft cap, ALiBi) are carried on the case as plain
+parameters; ALiBi slopes follow the geometric sequence 2^(-8 (h + 1) / H) of
+the ALiBi paper (for H a power of two), one per query head.
 """
 from __future__ import annotations
 
@@ -84,6 +88,15 @@ class Case:
     cu_seqlens_q: Optional[torch.Tensor] = None   # int32 [B + 1] (CPU)
     cu_seqlens_k: Optional[torch.Tensor] = None
     meta: dict = field(default_factory=dict)
+    window_left: int = -1                         # -1: unbounded
+    window_right: int = -1
+    softcap: float = 0.0                          # 0: off
+    alibi_slopes: Optional[torch.Tensor] = None   # fp32 [Hq] (CPU) or None
+
+    @property
+    def has_variants(self) -> bool:
+        return (self.window_left >= 0 or self.window_right >= 0 or self.softcap > 0
+                or self.alibi_slopes is not None)
 
     @property
     def varlen(self) -> bool:
@@ -112,6 +125,11 @@ def rising_bias_log2(n_keys: int, block: int = 128, period: int = 25,
     return per_block.repeat_interleave(block)[:n_keys]
 
 
+def alibi_slopes_geometric(H: int) -> torch.Tensor:
+    """ALiBi slopes 2^(-8 (h + 1) / H), h = 0 .. H-1 (fp32)."""
+    return torch.tensor([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], dtype=torch.float32)
+
+
 def _draw(shape, sigma, dtype, g):
     x = torch.randn(shape, generator=g, dtype=torch.float32)
     if sigma != 1.0:
@@ -121,7 +139,8 @@ def _draw(shape, sigma, dtype, g):
 
 def make_case(B, Hq, Hkv, Sq, Sk, D, dtype="bf16", causal=False, seed=0,
               sigma=1.0, rising_bias=False, seqlens_q=None, seqlens_k=None,
-              scale=None, zero_q=False) -> Case:
+              scale=None, zero_q=False, window=(-1, -1), softcap=0.0,
+              alibi_slopes=None) -> Case:
     """Draw one problem.
 
     Dense when ``seqlens_q`` is None (q [B, Sq, Hq, D], k/v [B, Sk, Hkv, D]);
@@ -158,7 +177,11 @@ def make_case(B, Hq, Hkv, Sq, Sk, D, dtype="bf16", causal=False, seed=0,
                 s0, s1 = int(cu_k[b]), int(cu_k[b + 1])
                 bias = rising_bias_log2(s1 - s0) * math.log(2.0) / scale
                 k[s0:s1, :, D - 1] = bias.view(-1, 1).to(k.dtype)
-    return Case(q, k, v, B, Hq, Hkv, Sq, Sk, D, scale, bool(causal), dtype, cu_q, cu_k)
+    if alibi_slopes is not None:
+        alibi_slopes = torch.as_tensor(alibi_slopes, dtype=torch.float32).reshape(Hq)
+    return Case(q, k, v, B, Hq, Hkv, Sq, Sk, D, scale, bool(causal), dtype, cu_q, cu_k,
+                window_left=int(window[0]), window_right=int(window[1]),
+                softcap=float(softcap), alibi_slopes=alibi_slopes)
 
 
 def make_workload(w: Workload) -> Case:
@@ -179,16 +202,22 @@ def make_workload(w: Workload) -> Case:
 
 def visible_pairs(case: Case) -> int:
     """Number of (query, key) pairs the mask leaves visible, summed over the
-    sequences of one head (bottom-right aligned causal mask)."""
+    sequences of one head (bottom-right aligned causal mask and local window)."""
     total = 0
     for lq, lk in case.seq_lengths():
-        if not case.causal:
+        if not case.causal and case.window_left < 0 and case.window_right < 0:
             total += lq * lk
             continue
-        off = lk - lq
-        # row i sees min(lk, max(0, i + off + 1)) keys
-        for_rows = torch.arange(lq, dtype=torch.int64) + off + 1
-        total += int(for_rows.clamp(min=0, max=lk).sum())
+        diag = torch.arange(lq, dtype=torch.int64) + (lk - lq)
+        hi = torch.full_like(diag, lk - 1)
+        if case.causal:
+            hi = torch.minimum(hi, diag)
+        if case.window_right >= 0:
+            hi = torch.minimum(hi, diag + case.window_right)
+        lo = torch.zeros_like(diag)
+        if case.window_left >= 0:
+            lo = torch.maximum(lo, diag - case.window_left)
+        total += int((hi - lo + 1).clamp(min=0).sum())
     return total
 
 

@@ -97,6 +97,41 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            fa_stream_t stream, int dtype);
 
 /*
+ * fa_fwd_ex — fa_fwd with the score variants that the upstream forward API
+ * offers next to plain causal masking (the fork's v1.7 release notes, section
+ * 2 "Public APIs": local window, ALiBi, softcap; validated by tests 5-7 of
+ * section 4.1 and the extra checks of section 4.6).  With window_left =
+ * window_right = -1, softcap = 0 and alibi_slopes = NULL it is fa_fwd.
+ *
+ * All arguments of fa_fwd keep their meaning, layout and ownership.  Let
+ * diag = i + (Lk - Lq) be the bottom-right aligned diagonal of query row i.
+ *   window_left, window_right   local window: key j is visible to row i iff
+ *               diag - window_left <= j <= diag + window_right; a negative
+ *               bound is unbounded on that side.  causal = 1 additionally
+ *               requires j <= diag.  Window (0, 0) with Lq == Lk leaves only
+ *               key i, so O = V (section 4.6).
+ *   softcap     0 (off) or a finite c > 0: each score becomes
+ *               c * tanh(scale * <q_i, k_j> / c) before the softmax.
+ *   alibi_slopes  NULL (off) or a DEVICE array of Hq fp32 slopes (4-byte
+ *               aligned, read-only, finite): row i of query head h adds
+ *               -alibi_slopes[h] * |diag - j| to each score (after the soft
+ *               cap), natural-log units.
+ * Every score is then combined in the same online softmax as fa_fwd (lazy
+ * rescale, threshold 8 log2 units, max lagging); LSE is ln sum_j exp(score).
+ * A row with no visible key gets O = 0 and LSE = -inf.
+ *
+ * Returns as fa_fwd; FA_ERR_INVALID_ARG also for a negative or non-finite
+ * softcap (or one so small that scale / softcap overflows) and a misaligned
+ * alibi_slopes.
+ */
+int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+              int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
+              const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+              fa_stream_t stream, int dtype,
+              int window_left, int window_right, float softcap,
+              const float *alibi_slopes);
+
+/*
  * fa_get_device_error — synchronize `stream`, then return and clear the status
  * word that kernels on the current device set on a device-side error
  * (FA_OK if none).  Returns FA_ERR_CUDA if the synchronization itself fails.

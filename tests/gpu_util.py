@@ -28,9 +28,14 @@ def run_gpu(case, dev="cuda:0", with_lse=True, stream=None):
     o = torch.full_like(q, float("nan"))
     shape = (case.Hq, case.Sq) if case.varlen else (case.B, case.Hq, case.Sq)
     lse = torch.full(shape, float("nan"), dtype=torch.float32, device=dev) if with_lse else None
-    st = fa.fa_fwd(q, k, v, o, lse, case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D,
-                   case.scale, int(case.causal), cu_q, cu_k,
-                   stream or torch.cuda.current_stream(), wl.DTYPE_CODE[case.dtype])
+    args = (q, k, v, o, lse, case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D, case.scale,
+            int(case.causal), cu_q, cu_k, stream or torch.cuda.current_stream(),
+            wl.DTYPE_CODE[case.dtype])
+    if case.has_variants:
+        slopes = case.alibi_slopes.to(dev) if case.alibi_slopes is not None else None
+        st = fa.fa_fwd_ex(*args, case.window_left, case.window_right, case.softcap, slopes)
+    else:
+        st = fa.fa_fwd(*args)
     assert st == fa.FA_OK, fa.fa_status_string(st)
     dst = fa.fa_get_device_error(stream or torch.cuda.current_stream())
     assert dst == fa.FA_OK, fa.fa_status_string(dst)
@@ -50,7 +55,9 @@ def rows_in_oracle_order(case, o, lse):
 def oracle_rows(case, rows=None):
     return oracle.attention(case.q, case.k, case.v, case.B, case.Hq, case.Hkv, case.Sq,
                             case.Sk, case.D, case.scale, case.causal, case.cu_seqlens_q,
-                            case.cu_seqlens_k, rows=rows)
+                            case.cu_seqlens_k, rows=rows, window_left=case.window_left,
+                            window_right=case.window_right, softcap=case.softcap,
+                            alibi_slopes=case.alibi_slopes)
 
 
 def check(case, o, lse, rows=None, tag=""):

@@ -61,6 +61,28 @@ def test_invalid_arguments_rejected_without_launch(lib, bad):
     assert _call(**bad) == fa.FA_ERR_INVALID_ARG
 
 
+def _call_ex(window_left=-1, window_right=-1, softcap=0.0, alibi_slopes=None, **kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=None, B=1, Hq=2, Hkv=2, Sq=8, Sk=8, D=64,
+                scale=0.125, causal=0, cu_seqlens_q=None, cu_seqlens_k=None, stream=None,
+                dtype=fa.FA_DTYPE_BF16)
+    args.update(kw)
+    return fa.fa_fwd_ex(**args, window_left=window_left, window_right=window_right,
+                        softcap=softcap, alibi_slopes=alibi_slopes)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(softcap=-1.0), dict(softcap=float("nan")), dict(softcap=float("inf")),
+    dict(softcap=1e-40), dict(alibi_slopes=18), dict(B=-1), dict(causal=3),
+])
+def test_variant_arguments_rejected_without_launch(lib, bad):
+    assert _call_ex(**bad) == fa.FA_ERR_INVALID_ARG
+
+
+def test_variant_empty_problems_are_noops(lib):
+    assert _call_ex(B=0, window_left=3, softcap=30.0) == fa.FA_OK
+    assert _call_ex(Sq=0, alibi_slopes=16) == fa.FA_OK
+
+
 @pytest.mark.parametrize("D", [32, 96, 256])
 def test_unbuilt_head_dims_unsupported(lib, D):
     assert _call(D=D) == fa.FA_ERR_UNSUPPORTED

@@ -7,6 +7,7 @@ against the oracle.  Gates: O rel_Linf <= 2e-2 (fp16) / 1e-2 (bf16), cosine
 >= 0.9995, LSE max abs error <= 1e-3.
 """
 import math
+import zlib
 
 import numpy as np
 import pytest
@@ -52,7 +53,7 @@ SMALL = [
     *s[:6], "causal" if s[6] else "full"))
 def test_small_shapes_all_rows(shape):
     B, Hq, Hkv, S, D, dtype, causal = shape
-    case = wl.make_case(B, Hq, Hkv, S, S, D, dtype, causal, seed=hash(shape) % 1000)
+    case = wl.make_case(B, Hq, Hkv, S, S, D, dtype, causal, seed=zlib.crc32(repr(shape).encode()) % 1000)
     o, lse = run_gpu(case)
     check(case, o, lse, tag=str(shape))
 

@@ -1,0 +1,130 @@
+"""GPU parity of the score variants (local window, tanh soft cap, ALiBi)
+through ``fa_fwd_ex`` against the fp64 oracle.
+
+The fork's v1.7 release notes list these variants in the public API (section
+2) and validate them with window_size=(32, 32), alibi_slopes and softcap=30.0
+(section 4.1, tests 5-7); section 4.6 adds window (0, 0) == V exactly and
+softcap with causal masking staying finite.  Gates as for the plain path:
+O rel_Linf <= 2e-2 (fp16) / 1e-2 (bf16), cosine >= 0.9995, LSE abs <= 1e-3.
+"""
+import json
+import os
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines too
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import exact_attention_forward_sm_gb300 as fa  # noqa: E402
+from exact_attention_forward_sm_gb300 import workloads as wl  # noqa: E402
+from tests.gpu_util import check, run_gpu, sample_rows, to_device  # noqa: E402
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from exact_attention_forward_sm_gb300 import _build
+    _build.build()
+    fa.load_library()
+
+
+def _seed(*key):
+    return zlib.crc32(repr(key).encode()) % 100000
+
+
+@pytest.mark.parametrize("D,dtype", [(64, "fp16"), (128, "bf16"), (128, "fp16")])
+@pytest.mark.parametrize("softcap", [0.0, 30.0])
+def test_window_00_output_equals_v_exactly(D, dtype, softcap):
+    gold = json.load(open(os.path.join(GOLDEN, "window_00_output_equals_v.json")))
+    case = wl.make_case(2, 4, 2, 300, 300, D, dtype, False, seed=_seed(D, dtype, softcap),
+                        window=tuple(gold["window"]), softcap=softcap)
+    o, lse = run_gpu(case)
+    v = case.v.to(o.device)                                  # [B, S, Hkv, D]
+    want = v.repeat_interleave(2, dim=2)                     # query head h reads h // 2
+    diff = (o.float() - want.float()).abs().max().item()
+    assert diff == gold["expected_max_abs_diff"]
+    check(case, o, lse, tag=f"window00 D{D} {dtype} cap{softcap}")
+
+
+WINDOWS = [(32, 32), (128, 0), (0, 127), (200, 50), (-1, 300), (513, -1), (5, 0), (1000, 1000)]
+
+
+@pytest.mark.parametrize("win", WINDOWS, ids=lambda w: f"w{w[0]}_{w[1]}")
+@pytest.mark.parametrize("causal", [False, True])
+def test_windows_all_rows(win, causal):
+    case = wl.make_case(1, 4, 2, 700, 700, 128, "bf16", causal, seed=_seed(win, causal),
+                        window=win)
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag=f"window {win} causal={causal}")
+
+
+@pytest.mark.parametrize("sq,sk", [(100, 600), (600, 100), (257, 513)])
+@pytest.mark.parametrize("win", [(64, 64), (300, 0), (0, 0)])
+def test_windows_unequal_lengths(sq, sk, win):
+    case = wl.make_case(2, 3, 3, sq, sk, 64, "fp16", False, seed=_seed(sq, sk, win),
+                        window=win)
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag=f"window {win} sq{sq} sk{sk}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("cap,sigma", [(30.0, 3.0), (5.0, 2.0), (50.0, 1.0)])
+def test_softcap_all_rows(causal, cap, sigma):
+    case = wl.make_case(2, 4, 4, 400, 400, 128, "bf16", causal, seed=_seed(cap, causal),
+                        sigma=sigma, softcap=cap)
+    o, lse = run_gpu(case)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    check(case, o, lse, tag=f"softcap {cap} sigma {sigma} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("sq,sk,D,dtype", [(512, 512, 128, "bf16"), (300, 700, 64, "fp16"),
+                                           (700, 300, 128, "fp16")])
+def test_alibi_all_rows(causal, sq, sk, D, dtype):
+    Hq = 8
+    case = wl.make_case(1, Hq, 2, sq, sk, D, dtype, causal, seed=_seed(sq, sk, causal),
+                        alibi_slopes=wl.alibi_slopes_geometric(Hq))
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag=f"alibi sq{sq} sk{sk} causal={causal}")
+
+
+@pytest.mark.parametrize("D,dtype", [(64, "fp16"), (128, "bf16")])
+def test_all_variants_packed_gqa(D, dtype):
+    Hq = 8
+    case = wl.make_case(0, Hq, 4, 0, 0, D, dtype, True, seed=_seed(D, dtype), sigma=2.0,
+                        seqlens_q=[1, 130, 640, 77, 0, 300], seqlens_k=[5, 130, 700, 300, 9, 300],
+                        window=(150, 20), softcap=20.0,
+                        alibi_slopes=wl.alibi_slopes_geometric(Hq))
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag=f"all variants packed D{D}")
+
+
+def test_variants_off_match_plain_bitwise():
+    case = wl.make_case(2, 4, 2, 333, 333, 128, "bf16", True, seed=7)
+    o0, l0 = run_gpu(case)
+    q, k, v, _, _ = to_device(case)
+    o1 = torch.empty_like(q)
+    l1 = torch.empty_like(l0)
+    st = fa.fa_fwd_ex(q, k, v, o1, l1, case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D,
+                      case.scale, 1, None, None, torch.cuda.current_stream(),
+                      fa.FA_DTYPE_BF16, -1, -1, 0.0, None)
+    assert st == fa.FA_OK
+    torch.cuda.synchronize()
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+
+
+def test_window_full_size_sampled_rows():
+    """A sliding-window causal problem at the size of the causal benchmark
+    (b4 h16 s2048 d128 bf16) with ALiBi, in the benchmark's launch
+    configuration; sampled rows against the oracle."""
+    case = wl.make_case(4, 16, 16, 2048, 2048, 128, "bf16", True, seed=1101,
+                        window=(256, 0), alibi_slopes=wl.alibi_slopes_geometric(16))
+    o, lse = run_gpu(case)
+    rows = sample_rows(case, per_head=96, seed=3)
+    check(case, o, lse, rows=rows, tag="window256 alibi b4h16s2048")
