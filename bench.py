@@ -180,7 +180,9 @@ def oracle_sample(case, seconds, seed=0):
         t0 = time.perf_counter()
         oracle.attention(q, k, v, case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D,
                          case.scale, case.causal, case.cu_seqlens_q, case.cu_seqlens_k,
-                         rows=rows, nthreads=threads)
+                         rows=rows, nthreads=threads, window_left=case.window_left,
+                         window_right=case.window_right, softcap=case.softcap,
+                         alibi_slopes=case.alibi_slopes)
         return time.perf_counter() - t0, 4.0 * case.D * float(vis[rows].sum())
 
     calib = np.sort(rng.choice(n_rows, size=min(n_rows, 256), replace=False))
@@ -197,22 +199,30 @@ def _visible_per_row(case):
     """Visible keys of every row in LSE-index order."""
     out = []
     lens = case.seq_lengths()
+    win = (case.window_left, case.window_right)
     if case.varlen:
         for _h in range(case.Hq):
             for lq, lk in lens:
-                out.append(_vis_rows(lq, lk, case.causal))
+                out.append(_vis_rows(lq, lk, case.causal, win))
     else:
         for lq, lk in lens:
             for _h in range(case.Hq):
-                out.append(_vis_rows(lq, lk, case.causal))
+                out.append(_vis_rows(lq, lk, case.causal, win))
     return np.concatenate(out) if out else np.zeros(0)
 
 
-def _vis_rows(lq, lk, causal):
-    i = np.arange(lq, dtype=np.int64)
-    if not causal:
-        return np.full(lq, lk, dtype=np.int64)
-    return np.clip(i + lk - lq + 1, 0, lk)
+def _vis_rows(lq, lk, causal, window=(-1, -1)):
+    """Visible keys per row (bottom-right aligned causal mask, local window)."""
+    diag = np.arange(lq, dtype=np.int64) + lk - lq
+    hi = np.full(lq, lk - 1, dtype=np.int64)
+    if causal:
+        hi = np.minimum(hi, diag)
+    if window[1] >= 0:
+        hi = np.minimum(hi, diag + window[1])
+    lo = np.zeros(lq, dtype=np.int64)
+    if window[0] >= 0:
+        lo = np.maximum(lo, diag - window[0])
+    return np.clip(hi - lo + 1, 0, None)
 
 
 # --------------------------------------------------------------- GPU benchmark
@@ -240,10 +250,17 @@ def run_gpu_arm(args, rank, local_rank, world):
     lse_shape = (case.Hq, case.Sq) if case.varlen else (case.B, case.Hq, case.Sq)
     lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    slopes = case.alibi_slopes.to(dev) if case.alibi_slopes is not None else None
 
     def launch(qq, kk, vv, oo, ll):
-        st = fa.fa_fwd(qq, kk, vv, oo, ll, case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D,
-                       case.scale, int(case.causal), cu_q, cu_k, stream, dtype_code)
+        if case.has_variants:
+            st = fa.fa_fwd_ex(qq, kk, vv, oo, ll, case.B, case.Hq, case.Hkv, case.Sq, case.Sk,
+                              case.D, case.scale, int(case.causal), cu_q, cu_k, stream,
+                              dtype_code, case.window_left, case.window_right, case.softcap,
+                              slopes)
+        else:
+            st = fa.fa_fwd(qq, kk, vv, oo, ll, case.B, case.Hq, case.Hkv, case.Sq, case.Sk,
+                           case.D, case.scale, int(case.causal), cu_q, cu_k, stream, dtype_code)
         if st != fa.FA_OK:
             raise RuntimeError(f"fa_fwd: {fa.fa_status_string(st)}")
 
@@ -305,7 +322,22 @@ def run_gpu_arm(args, rank, local_rank, world):
     peaks, peak_src = load_peaks()
     dense_key = "bf16_tflops"
     peak = float(peaks.get(dense_key, PEAK_FALLBACK[dense_key]))
+    hbm_peak = float(peaks.get("hbm_gbs", PEAK_FALLBACK["hbm_gbs"]))
+    alg_bytes = wl.algorithmic_bytes(case)
+    # below the ridge point (peak FLOP/s / peak bytes/s) the launch is bound by
+    # HBM: report algorithmic bytes / time against the measured copy bandwidth
+    hbm_bound = flops / alg_bytes < peak * 1e12 / (hbm_peak * 1e9)
     achieved = flops / (kernel_ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": UNIT,
+            "frac": round(achieved / peak, 4)}
+    if hbm_bound:
+        gbs = alg_bytes / (kernel_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(gbs, 2), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(gbs / hbm_peak, 4)}
+    variants = {}
+    if case.has_variants:
+        variants = {"window": [case.window_left, case.window_right], "softcap": case.softcap,
+                    "alibi": "geometric slopes" if case.alibi_slopes is not None else None}
     line = {
         "metric": METRIC,
         "value": round(world * flops / (kernel_ms_max * 1e-3) / 1e12, 3),
@@ -322,20 +354,18 @@ def run_gpu_arm(args, rank, local_rank, world):
         "config": {
             "workload": w.name, "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv,
             "Sq": case.Sq, "Sk": case.Sk, "D": case.D, "causal": case.causal,
-            "varlen": case.varlen, "flops_per_step_per_gpu": flops,
+            "varlen": case.varlen, **variants, "flops_per_step_per_gpu": flops,
+            "algorithmic_bytes_per_step_per_gpu": alg_bytes,
             "l2": "flushed before every step (256 MiB write, outside the kernel events)",
             "parallelism": f"replicas x{world} (independent problems, no collective)",
             "wall_ms_per_step_incl_flush": round(wall * 1e3 / args.steps, 4),
             **({"ablation_variant": args.variant} if args.variant else {}),
         },
         "roofline": {
-            "bound": "tensor",
-            "achieved": round(achieved, 3),
-            "peak": peak,
-            "unit": UNIT,
-            "frac": round(achieved / peak, 4),
+            **roof,
             "traffic": profiled_traffic(w.name),
-            "peak_source": f"{peak_src} {dense_key} (burst, cuBLAS bf16)",
+            "peak_source": (f"{peak_src} hbm_gbs (copy bandwidth)" if hbm_bound
+                            else f"{peak_src} {dense_key} (burst, cuBLAS bf16)"),
             "kernel": "fa_fwd_kernel",
             "kernel_ms_mean": round(kernel_ms, 5),
             "kernel_ms_min": round(min(times_ms), 5),
@@ -350,7 +380,7 @@ def run_gpu_arm(args, rank, local_rank, world):
         "gpu_launches": args.steps,
         "clocks": clock,
     }
-    if "bf16_tflops_sustained" in peaks:
+    if "bf16_tflops_sustained" in peaks and not hbm_bound:
         line["roofline"]["frac_of_sustained"] = round(
             achieved / float(peaks["bf16_tflops_sustained"]), 4)
     return line, case

@@ -51,6 +51,9 @@ class Workload:
     varlen_min: int = 0
     varlen_max: int = 0
     seed: int = 0
+    window: tuple = (-1, -1)   # local window (left, right), -1 = unbounded
+    softcap: float = 0.0
+    alibi: bool = False        # geometric ALiBi slopes, one per query head
 
 
 # The five workloads the method is validated and measured on.  Seeds are
@@ -67,7 +70,20 @@ WORKLOADS = [
     Workload("b1_h8_s32768_d128_bf16_noncausal_sigma2", 1, 8, 8, 32768, 128, "bf16",
              False, sigma=math.sqrt(2.0), seed=1004),
 ]
-BY_NAME = {w.name: w for w in WORKLOADS}
+# Score-variant workloads (local window, soft cap, ALiBi): the shapes of the
+# causal benchmark problem and a long sliding-window problem.  They are not
+# part of the five validation workloads; seeds are 1100 + index.
+VARIANT_WORKLOADS = [
+    Workload("b4_h16_s2048_d128_bf16_causal_softcap30", 4, 16, 16, 2048, 128, "bf16", True,
+             seed=1100, softcap=30.0),
+    Workload("b4_h16_s2048_d128_bf16_causal_alibi", 4, 16, 16, 2048, 128, "bf16", True,
+             seed=1101, alibi=True),
+    Workload("b2_h16_s16384_d128_bf16_causal_window1024", 2, 16, 16, 16384, 128, "bf16",
+             True, seed=1102, window=(1024, 0)),
+    Workload("b4_h16_s2048_d128_bf16_window32_32", 4, 16, 16, 2048, 128, "bf16", False,
+             seed=1103, window=(32, 32)),
+]
+BY_NAME = {w.name: w for w in WORKLOADS + VARIANT_WORKLOADS}
 
 
 @dataclass
@@ -184,6 +200,11 @@ def make_case(B, Hq, Hkv, Sq, Sk, D, dtype="bf16", causal=False, seed=0,
                 softcap=float(softcap), alibi_slopes=alibi_slopes)
 
 
+def _variants(w: Workload) -> dict:
+    return {"window": tuple(w.window), "softcap": w.softcap,
+            "alibi_slopes": alibi_slopes_geometric(w.Hq) if w.alibi else None}
+
+
 def make_workload(w: Workload) -> Case:
     """Draw the inputs of one named workload."""
     if w.varlen_count:
@@ -192,10 +213,11 @@ def make_workload(w: Workload) -> Case:
                              generator=g).tolist()
         case = make_case(w.varlen_count, w.Hq, w.Hkv, 0, 0, w.D, w.dtype, w.causal,
                          seed=w.seed + 7919, sigma=w.sigma,
-                         rising_bias=w.rising_bias, seqlens_q=lens)
+                         rising_bias=w.rising_bias, seqlens_q=lens, **_variants(w))
     else:
         case = make_case(w.B, w.Hq, w.Hkv, w.S, w.S, w.D, w.dtype, w.causal,
-                         seed=w.seed, sigma=w.sigma, rising_bias=w.rising_bias)
+                         seed=w.seed, sigma=w.sigma, rising_bias=w.rising_bias,
+                         **_variants(w))
     case.meta["workload"] = w.name
     return case
 

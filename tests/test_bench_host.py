@@ -64,7 +64,10 @@ def test_visible_rows_match_flop_count():
     for case in (wl.make_case(2, 3, 1, 300, 300, 64, "bf16", True, seed=1),
                  wl.make_case(0, 2, 2, 0, 0, 64, "fp16", True, seed=2,
                               seqlens_q=[5, 130, 64], seqlens_k=[9, 130, 70]),
-                 wl.make_case(1, 4, 4, 100, 50, 128, "bf16", False, seed=3)):
+                 wl.make_case(1, 4, 4, 100, 50, 128, "bf16", False, seed=3),
+                 wl.make_case(2, 2, 2, 90, 300, 64, "bf16", False, seed=4, window=(17, 5)),
+                 wl.make_case(0, 2, 1, 0, 0, 64, "fp16", True, seed=5, window=(40, -1),
+                              seqlens_q=[70, 1, 200], seqlens_k=[30, 9, 260])):
         vis = bench._visible_per_row(case)
         assert vis.shape[0] == case.lse_rows()
         assert 4 * case.D * int(vis.sum()) == wl.attention_flops(case)
