@@ -252,8 +252,22 @@ def run_gpu_arm(args, rank, local_rank, world):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     slopes = case.alibi_slopes.to(dev) if case.alibi_slopes is not None else None
 
+    splits = w.splits if args.splits is None else args.splits
+    launches_per_step = 1
+    if splits >= 0:
+        used, _ = fa.fa_split_plan(case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D,
+                                   case.varlen, splits)
+        if used < 1:
+            raise RuntimeError(f"fa_split_plan: status {-used}")
+        launches_per_step = 2 if used > 1 else 1   # partial pass + combine
+
     def launch(qq, kk, vv, oo, ll):
-        if case.has_variants:
+        if splits >= 0:
+            st = fa.fa_fwd_split(qq, kk, vv, oo, ll, case.B, case.Hq, case.Hkv, case.Sq,
+                                 case.Sk, case.D, case.scale, int(case.causal), cu_q, cu_k,
+                                 stream, dtype_code, case.window_left, case.window_right,
+                                 case.softcap, slopes, splits)
+        elif case.has_variants:
             st = fa.fa_fwd_ex(qq, kk, vv, oo, ll, case.B, case.Hq, case.Hkv, case.Sq, case.Sk,
                               case.D, case.scale, int(case.causal), cu_q, cu_k, stream,
                               dtype_code, case.window_left, case.window_right, case.softcap,
@@ -360,6 +374,7 @@ def run_gpu_arm(args, rank, local_rank, world):
             "parallelism": f"replicas x{world} (independent problems, no collective)",
             "wall_ms_per_step_incl_flush": round(wall * 1e3 / args.steps, 4),
             **({"ablation_variant": args.variant} if args.variant else {}),
+            **({"num_splits": splits, "num_splits_used": used} if splits >= 0 else {}),
         },
         "roofline": {
             **roof,
@@ -377,7 +392,7 @@ def run_gpu_arm(args, rank, local_rank, world):
             "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms, 4),
         },
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clock,
     }
     if "bf16_tflops_sustained" in peaks and not hbm_bound:
@@ -433,6 +448,9 @@ def main():
     ap.add_argument("--reference-budget-s", type=float, default=90.0,
                     help="total oracle seconds for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="split-KV chunks through fa_fwd_split (0 = library's choice); "
+                         "default: the workload's own setting")
     ap.add_argument("--variant", choices=["unfused", "threshold0"], default=None,
                     help="time an ablation build instead of the product library")
     args = ap.parse_args()

@@ -19,7 +19,8 @@ import threading
 __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
     "FA_ERR_BAD_SEQLENS", "FA_DTYPE_FP16", "FA_DTYPE_BF16", "LibraryMissing", "FaError",
-    "library_path", "load_library", "fa_fwd", "fa_fwd_ex", "fa_get_device_error", "fa_debug_wait_timeout",
+    "library_path", "load_library", "fa_fwd", "fa_fwd_ex", "fa_fwd_split", "fa_split_plan",
+    "fa_get_device_error", "fa_debug_wait_timeout",
     "fa_debug_trace_read",
     "fa_status_string", "fa_version", "attention_forward", "EXPORTED_SYMBOLS",
 ]
@@ -33,7 +34,8 @@ FA_ERR_BAD_SEQLENS = 5
 FA_DTYPE_FP16 = 0
 FA_DTYPE_BF16 = 1
 
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_ex", "fa_get_device_error", "fa_debug_wait_timeout",
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_split", "fa_split_plan",
+                    "fa_get_device_error", "fa_debug_wait_timeout",
                     "fa_debug_trace_read", "fa_status_string", "fa_version")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -76,6 +78,10 @@ def load_library():
         lib.fa_fwd.restype = i32
         lib.fa_fwd_ex.argtypes = lib.fa_fwd.argtypes + [i32, i32, f32, vp]
         lib.fa_fwd_ex.restype = i32
+        lib.fa_fwd_split.argtypes = lib.fa_fwd_ex.argtypes + [i32]
+        lib.fa_fwd_split.restype = i32
+        lib.fa_split_plan.argtypes = [i32] * 8 + [ctypes.POINTER(ctypes.c_longlong)]
+        lib.fa_split_plan.restype = i32
         lib.fa_get_device_error.argtypes = [vp]
         lib.fa_get_device_error.restype = i32
         lib.fa_debug_wait_timeout.argtypes = [ctypes.c_longlong, vp]
@@ -128,6 +134,26 @@ def fa_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal,
                          _addr(alibi_slopes))
 
 
+def fa_fwd_split(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal,
+                 cu_seqlens_q, cu_seqlens_k, stream, dtype, window_left=-1, window_right=-1,
+                 softcap=0.0, alibi_slopes=None, num_splits=0) -> int:
+    """Call the C ``fa_fwd_split`` (split-KV forward + LSE merge)."""
+    lib = load_library()
+    return lib.fa_fwd_split(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B),
+                            int(Hq), int(Hkv), int(Sq), int(Sk), int(D), float(scale),
+                            int(causal), _addr(cu_seqlens_q), _addr(cu_seqlens_k),
+                            _stream(stream), int(dtype), int(window_left), int(window_right),
+                            float(softcap), _addr(alibi_slopes), int(num_splits))
+
+
+def fa_split_plan(B, Hq, Hkv, Sq, Sk, D, varlen, num_splits=0):
+    """(split count or minus a status code, scratch bytes) of ``fa_fwd_split``."""
+    nbytes = ctypes.c_longlong(0)
+    n = load_library().fa_split_plan(int(B), int(Hq), int(Hkv), int(Sq), int(Sk), int(D),
+                                     int(bool(varlen)), int(num_splits), ctypes.byref(nbytes))
+    return n, nbytes.value
+
+
 def fa_get_device_error(stream=None) -> int:
     return load_library().fa_get_device_error(_stream(stream))
 
@@ -153,7 +179,7 @@ def fa_version() -> int:
 
 def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens_q=None,
                       cu_seqlens_k=None, out=None, lse=None, stream=None,
-                      window_size=(-1, -1), softcap=0.0, alibi_slopes=None):
+                      window_size=(-1, -1), softcap=0.0, alibi_slopes=None, num_splits=1):
     """Exact attention forward on CUDA tensors; returns ``(out, lse)``.
 
     Dense: q [B, Sq, Hq, D], k/v [B, Sk, Hkv, D] -> out like q, lse [B, Hq, Sq].
@@ -161,7 +187,8 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens_q=None,
     B + 1 offsets -> out like q, lse [Hq, total_q].
     ``window_size`` (left, right; -1 = unbounded), ``softcap`` and
     ``alibi_slopes`` (fp32 CUDA tensor [Hq]) select the score variants of
-    ``fa_fwd_ex``.
+    ``fa_fwd_ex``; ``num_splits`` != 1 runs the split-KV path of
+    ``fa_fwd_split`` (0 = chosen by the library).
     """
     import torch
 
@@ -192,9 +219,9 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens_q=None,
                                      or alibi_slopes.shape != (Hq,)
                                      or not alibi_slopes.is_contiguous()):
         raise FaError(FA_ERR_INVALID_ARG, "attention_forward (alibi_slopes)")
-    st = fa_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, D, scale, int(bool(causal)),
-                   cu_seqlens_q, cu_seqlens_k, stream, dtype, window_size[0], window_size[1],
-                   softcap, alibi_slopes)
+    st = fa_fwd_split(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, D, scale, int(bool(causal)),
+                      cu_seqlens_q, cu_seqlens_k, stream, dtype, window_size[0],
+                      window_size[1], softcap, alibi_slopes, num_splits)
     if st != FA_OK:
         raise FaError(st)
     return out, lse

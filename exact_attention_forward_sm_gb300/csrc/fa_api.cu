@@ -3,11 +3,13 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
 
 #include "fa.h"
+#include "fa_combine.cuh"
 #include "fa_launch.cuh"
 
 // Status word written by kernels on a device-side error (first error wins).
@@ -116,13 +118,49 @@ bool make_map(CUtensorMap *m, const void *base, bool bf16, int D, int heads, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Shared body of fa_fwd and fa_fwd_ex.  Window bounds < 0 are unbounded;
-// softcap 0 and alibi == nullptr switch those variants off.
+constexpr int kMaxSplits = 128;
+
+// Split count for num_splits = 0: the smallest split count whose wave
+// efficiency (units * s over whole waves of SMs) is within 85% of the best
+// one, with at least one K/V tile per split.  Problems that already fill the
+// GPU are not split.
+int choose_splits(int64_t units, int64_t kv_tiles, int sms) {
+  if (units <= 0 || sms <= 0 || units * 5 >= (int64_t)sms * 4) return 1;
+  const int64_t max_s = std::min<int64_t>({(int64_t)kMaxSplits, kv_tiles, (int64_t)sms});
+  if (max_s <= 1) return 1;
+  auto eff = [&](int64_t s) {
+    const int64_t work = units * s;
+    const int64_t waves = (work + sms - 1) / sms;
+    return (double)work / (double)(waves * sms);
+  };
+  double best = 0.0;
+  for (int64_t s = 1; s <= max_s; ++s) best = std::max(best, eff(s));
+  for (int64_t s = 1; s <= max_s; ++s)
+    if (eff(s) >= 0.85 * best) return (int)s;
+  return 1;
+}
+
+// Split count chosen for num_splits = 0 (sizes already validated).
+int auto_splits(int B, int Hq, int Hkv, int Sq, int Sk, bool varlen, int sms) {
+  const bool pair_heads = ((Hq / Hkv) % 2) == 0;
+  const int head_units = pair_heads ? Hq / 2 : Hq;
+  const int rows_per_unit = pair_heads ? fa::kBlockM : 2 * fa::kBlockM;
+  const int64_t row_units = (Sq + rows_per_unit - 1) / rows_per_unit;
+  // K/V tiles of a sequence: dense Sk, packed the mean length
+  const int64_t per_seq = varlen ? (Sk + B - 1) / B : Sk;
+  return choose_splits(row_units * head_units * (varlen ? 1 : B),
+                       (per_seq + fa::kBlockN - 1) / fa::kBlockN, sms);
+}
+
+// Shared body of fa_fwd, fa_fwd_ex and fa_fwd_split.  Window bounds < 0 are
+// unbounded; softcap 0 and alibi == nullptr switch those variants off;
+// num_splits 1 = no split, 0 = choose.
 int forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
             int Hkv, int Sq, int Sk, int D, float scale, int causal,
             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, fa_stream_t stream,
             int dtype, int window_left, int window_right, float softcap,
-            const float *alibi_slopes) {
+            const float *alibi_slopes, int num_splits) {
+  if (num_splits < 0 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
   // ---------------------------------------------------------- argument checks
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
@@ -152,8 +190,6 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   int win_l = (window_left < 0 || window_left > span) ? -1 : window_left;
   int win_r = (window_right < 0 || window_right > span) ? -1 : window_right;
   if (causal) win_r = 0;
-  const bool ext = win_l >= 0 || win_r > 0 || softcap > 0.f || alibi_slopes != nullptr;
-  const bool plain_causal = !ext && win_r == 0;
 
   const int group = Hq / Hkv;
   const bool pair_heads = (group % 2) == 0;
@@ -162,14 +198,24 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   const int64_t row_units = (Sq + rows_per_unit - 1) / rows_per_unit;
   // packed problems: each sequence rounds its row count up once, so this
   // bounds the number of units; the kernel skips the ones past the last
-  const int64_t units = varlen ? (row_units + B) * head_units : row_units * B * head_units;
-  if (units <= 0 || units > 0x7fffffffll) return FA_ERR_UNSUPPORTED;
+  const int64_t base_units =
+      varlen ? (row_units + B) * head_units : row_units * B * head_units;
+  if (base_units <= 0 || base_units > 0x7fffffffll) return FA_ERR_UNSUPPORTED;
 
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
   int *status = status_ptr(device);
   const int sms = sm_count(device);
   if (!status || sms <= 0) return FA_ERR_CUDA;
+
+  const int splits = num_splits ? num_splits : auto_splits(B, Hq, Hkv, Sq, Sk, varlen, sms);
+  // the instances with score variants also carry the split-KV path
+  const bool ext =
+      win_l >= 0 || win_r > 0 || softcap > 0.f || alibi_slopes != nullptr || splits > 1;
+  const bool plain_causal = !ext && win_r == 0;
+  const int64_t units = base_units * splits;
+  if (units > 0x7fffffffll) return FA_ERR_UNSUPPORTED;
+  const int64_t lse_rows = (int64_t)Hq * Sq * (varlen ? 1 : B);
   // dense: persistent, one CTA per SM walking a snake over the heavy-first
   // unit order; packed: unit costs follow the sequence lengths, so one CTA per
   // unit and the hardware's in-order CTA dispatch balances them
@@ -212,6 +258,10 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   p.cap_k = cap_k;
   p.cap_l2 = softcap * 1.4426950408889634f;
   p.alibi = alibi_slopes;
+  p.num_splits = splits;
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
+  p.part_rows = lse_rows;
   p.wait_limit = kDefaultWaitLimit;
   p.status = status;
   p.trace = nullptr;
@@ -226,6 +276,19 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.device = device;
 
+  // split-KV scratch: stream-ordered allocation, freed after the combine
+  void *scratch = nullptr;
+  if (splits > 1) {
+    const size_t o_bytes = (size_t)splits * (size_t)lse_rows * (size_t)D * sizeof(float);
+    const size_t l_bytes = (size_t)splits * (size_t)lse_rows * sizeof(float);
+    if (cudaMallocAsync(&scratch, o_bytes + l_bytes, a.stream) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_CUDA;
+    }
+    p.o_part = static_cast<float *>(scratch);
+    p.lse_part = reinterpret_cast<float *>(static_cast<char *>(scratch) + o_bytes);
+  }
+
   cudaError_t e;
   if (ext) {
     if (D == 64)
@@ -239,6 +302,22 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
     e = bf16 ? fa::launch_d128_bf16(a, plain_causal, varlen)
              : fa::launch_d128_fp16(a, plain_causal, varlen);
   }
+  if (e == cudaSuccess && splits > 1) {
+    fa::CombineParams c;
+    c.o_part = p.o_part;
+    c.lse_part = p.lse_part;
+    c.o = o;
+    c.lse = lse;
+    c.rows = lse_rows;
+    c.num_splits = splits;
+    c.B = B;
+    c.Hq = Hq;
+    c.Sq = Sq;
+    c.cu_q = cu_seqlens_q;
+    e = fa::launch_combine(c, D, bf16, sms, a.stream);
+  }
+  if (scratch && cudaFreeAsync(scratch, a.stream) != cudaSuccess && e == cudaSuccess)
+    e = cudaErrorUnknown;
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -265,7 +344,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, fa_stream_t stream,
            int dtype) {
   return forward(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, cu_seqlens_q,
-                 cu_seqlens_k, stream, dtype, -1, -1, 0.f, nullptr);
+                 cu_seqlens_k, stream, dtype, -1, -1, 0.f, nullptr, 1);
 }
 
 int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
@@ -274,7 +353,41 @@ int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, 
               int dtype, int window_left, int window_right, float softcap,
               const float *alibi_slopes) {
   return forward(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, cu_seqlens_q,
-                 cu_seqlens_k, stream, dtype, window_left, window_right, softcap, alibi_slopes);
+                 cu_seqlens_k, stream, dtype, window_left, window_right, softcap, alibi_slopes,
+                 1);
+}
+
+int fa_fwd_split(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                 int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
+                 const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, fa_stream_t stream,
+                 int dtype, int window_left, int window_right, float softcap,
+                 const float *alibi_slopes, int num_splits) {
+  return forward(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, cu_seqlens_q,
+                 cu_seqlens_k, stream, dtype, window_left, window_right, softcap, alibi_slopes,
+                 num_splits);
+}
+
+int fa_split_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int varlen, int num_splits,
+                  long long *scratch_bytes) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || Hq % Hkv != 0) return -FA_ERR_INVALID_ARG;
+  if (varlen != 0 && varlen != 1) return -FA_ERR_INVALID_ARG;
+  if (num_splits < 0 || num_splits > kMaxSplits) return -FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return -FA_ERR_UNSUPPORTED;
+  int splits = num_splits;
+  if (B == 0 || Sq == 0) {
+    splits = 1;
+  } else if (splits == 0) {
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return -FA_ERR_CUDA;
+    const int sms = sm_count(device);
+    if (sms <= 0) return -FA_ERR_CUDA;
+    splits = auto_splits(B, Hq, Hkv, Sq, Sk, varlen != 0, sms);
+  }
+  if (scratch_bytes) {
+    const long long rows = (long long)Hq * Sq * (varlen ? 1 : B);
+    *scratch_bytes = splits > 1 ? (long long)splits * rows * (D + 1) * 4 : 0;
+  }
+  return splits;
 }
 
 int fa_get_device_error(fa_stream_t stream) {

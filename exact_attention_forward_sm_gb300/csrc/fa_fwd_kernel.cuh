@@ -94,6 +94,14 @@ struct FwdParams {
   float cap_k;              // soft cap c: 2 * scale * log2(e) / c, 0 = no soft cap
   float cap_l2;             // soft cap c: c * log2(e)
   const float *alibi;       // ALiBi slope per query head (natural-log units) or null
+  // split-KV (instances with score variants only): each unit of the problem
+  // becomes num_splits units, split s taking the s-th of num_splits equal
+  // chunks of its sequence's K/V tiles and writing a partial result instead
+  // of O / LSE
+  int num_splits;           // 1: no split (o_part / lse_part unused)
+  float *o_part;            // [num_splits][part_rows][D] fp32, O_s / l_s
+  float *lse_part;          // [num_splits][part_rows] fp32, LSE_s (-inf: no visible key)
+  int64_t part_rows;        // rows per split slab: one per LSE entry
   long long wait_limit;     // bounded-wait limit in SM clock cycles
   int *status;              // device status word (first error wins)
   unsigned long long *trace;  // clock64 pipeline trace (trace builds only)
@@ -164,6 +172,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 struct Work {
   int valid;
+  int split;         // K/V split of the unit (0 without split-KV)
   int b, head[2], hkv;
   int m0[2];         // first query row of each tile within its sequence
   int lq, lk;        // sequence lengths
@@ -220,6 +229,11 @@ template <bool CAUSAL, bool VARLEN, bool EXT>
 __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
   Work w;
   w.valid = 0;
+  w.split = 0;
+  if (EXT && p.num_splits > 1) {  // splits of one unit are adjacent: heavy units stay first
+    w.split = unit % p.num_splits;
+    unit /= p.num_splits;
+  }
   const int hu = unit % p.head_units;
   int b = 0, ru = 0, n_ru = 0;
   if (!VARLEN) {
@@ -297,6 +311,20 @@ __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
     w.n_kv[0] = tile_kv_count<CAUSAL>(w.m0[0], w.lq, w.lk);
     w.n_kv[1] = tile_kv_count<CAUSAL>(w.m0[1], w.lq, w.lk);
     w.kv_begin[0] = w.kv_begin[1] = 0;
+  }
+  if (EXT && p.num_splits > 1) {
+    // split s keeps K/V tiles [s c, s c + c) of the sequence, c = ceil(tiles / splits);
+    // cutting two overlapping or touching ranges at the same bounds keeps
+    // their union contiguous
+    const int nt = (w.lk + kBlockN - 1) / kBlockN;
+    const int chunk = (nt + p.num_splits - 1) / p.num_splits;
+    const int lo = w.split * chunk, hi = min(nt, lo + chunk);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int b = max(w.kv_begin[t], lo), e = min(w.kv_begin[t] + w.n_kv[t], hi);
+      w.n_kv[t] = max(0, e - b);
+      w.kv_begin[t] = b;
+    }
   }
   if (w.n_kv[0] == 0 && w.n_kv[1] == 0) {
     w.kv_ub = 0;
@@ -792,10 +820,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         return pack_p<BF16>(__uint_as_float(orr[2 * k]) * inv_l,
                             __uint_as_float(orr[2 * k + 1]) * inv_l);
       };
+      const int64_t li = VARLEN ? (int64_t)w.head[t] * p.Sq + tok
+                                : ((int64_t)w.b * p.Hq + w.head[t]) * p.Sq + qi;
+      const float lse = (l > 0.f) ? (m * scale_log2 + log2f(l)) * 0.69314718055994531f
+                                  : -INFINITY;
       // a packed tile cut by its sequence end would spill into the next
       // sequence through the tensor map, so it is stored row by row instead
       const bool use_tma = !VARLEN || (m0 + kBlockM <= lq);
-      if (use_tma) {
+      if (EXT && p.num_splits > 1) {
+        // split-KV partial: normalised fp32 O_s and LSE_s of this split
+        if (row_valid && ok) {
+          const int64_t slot = (int64_t)w.split * p.part_rows + li;
+          float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * D);
+#pragma unroll
+          for (int k = 0; k < D / 4; ++k)
+            dst[k] = make_float4(__uint_as_float(orr[4 * k]) * inv_l,
+                                 __uint_as_float(orr[4 * k + 1]) * inv_l,
+                                 __uint_as_float(orr[4 * k + 2]) * inv_l,
+                                 __uint_as_float(orr[4 * k + 3]) * inv_l);
+          p.lse_part[slot] = lse;
+        }
+      } else if (use_tma) {
 #pragma unroll
         for (int half = 0; half < D / 64; ++half) {
           named_barrier_sync(1 + t, 128);  // staging buffer free
@@ -825,13 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < D / 8; ++k)
           dst[k] = make_uint4(packed(4 * k), packed(4 * k + 1), packed(4 * k + 2), packed(4 * k + 3));
       }
-      if (row_valid && ok && p.lse != nullptr) {
-        const float lse = (l > 0.f) ? (m * scale_log2 + log2f(l)) * 0.69314718055994531f
-                                    : -INFINITY;
-        const int64_t li = VARLEN ? (int64_t)w.head[t] * p.Sq + tok
-                                  : ((int64_t)w.b * p.Hq + w.head[t]) * p.Sq + qi;
-        p.lse[li] = lse;
-      }
+      if (row_valid && ok && p.lse != nullptr && !(EXT && p.num_splits > 1)) p.lse[li] = lse;
       FA_TRACE_AT(tr, (t * 64 + 63) * 8 + 6);
     }
     if (elected) bulk_wait_group0();  // output stores complete before the CTA exits

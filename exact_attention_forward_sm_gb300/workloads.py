@@ -54,6 +54,8 @@ class Workload:
     window: tuple = (-1, -1)   # local window (left, right), -1 = unbounded
     softcap: float = 0.0
     alibi: bool = False        # geometric ALiBi slopes, one per query head
+    Sk: int = 0                # dense keys per sequence when != S (0: Sk = S)
+    splits: int = -1           # split-KV chunks: -1 unsplit path, 0 chosen, >= 1 forced
 
 
 # The five workloads the method is validated and measured on.  Seeds are
@@ -83,7 +85,17 @@ VARIANT_WORKLOADS = [
     Workload("b4_h16_s2048_d128_bf16_window32_32", 4, 16, 16, 2048, 128, "bf16", False,
              seed=1103, window=(32, 32)),
 ]
-BY_NAME = {w.name: w for w in WORKLOADS + VARIANT_WORKLOADS}
+# Split-KV workloads: too few query tiles to fill the GPU, many K/V tiles each
+# (a prefill chunk at the end of a long context; one query row per sequence and
+# head, as in decoding).  Seeds 1200 + index; the split count is chosen by the
+# library.
+SPLIT_WORKLOADS = [
+    Workload("b1_h32_sq512_sk16384_d128_bf16_causal_chunk", 1, 32, 32, 512, 128, "bf16",
+             True, seed=1200, Sk=16384, splits=0),
+    Workload("b8_h8_sq1_sk8192_d128_bf16_decode", 8, 8, 8, 1, 128, "bf16", True,
+             seed=1201, Sk=8192, splits=0),
+]
+BY_NAME = {w.name: w for w in WORKLOADS + VARIANT_WORKLOADS + SPLIT_WORKLOADS}
 
 
 @dataclass
@@ -215,7 +227,7 @@ def make_workload(w: Workload) -> Case:
                          seed=w.seed + 7919, sigma=w.sigma,
                          rising_bias=w.rising_bias, seqlens_q=lens, **_variants(w))
     else:
-        case = make_case(w.B, w.Hq, w.Hkv, w.S, w.S, w.D, w.dtype, w.causal,
+        case = make_case(w.B, w.Hq, w.Hkv, w.S, w.Sk or w.S, w.D, w.dtype, w.causal,
                          seed=w.seed, sigma=w.sigma, rising_bias=w.rising_bias,
                          **_variants(w))
     case.meta["workload"] = w.name

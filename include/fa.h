@@ -132,6 +132,50 @@ int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
               const float *alibi_slopes);
 
 /*
+ * fa_fwd_split — fa_fwd_ex with the keys of every query tile split into
+ * `num_splits` chunks processed by separate work units, each writing a
+ * partial result (normalised O and LSE of its chunk), followed by an
+ * LSE-weighted merge: M = max_s LSE_s, O = sum_s e^(LSE_s - M) O_s /
+ * sum_s e^(LSE_s - M), LSE = M + ln sum_s e^(LSE_s - M).  This is the
+ * split-KV forward of upstream FA2 (compute_attn_1rowblock_splitkv, one of
+ * the dispatch sites in the fork's v1.2 notes, section 3); it fills the GPU
+ * when a problem has fewer query tiles than streaming multiprocessors.  The
+ * online softmax inside each chunk is the same as fa_fwd's (lazy rescale,
+ * threshold 8 log2 units, max lagging; the chunk's first K/V tile sets its
+ * max).  Each sequence's K/V tiles are cut into num_splits chunks of equal
+ * tile count; a chunk a query row sees no key of contributes nothing.
+ *
+ * Arguments are those of fa_fwd_ex, plus:
+ *   num_splits  1 = no split (same result as fa_fwd_ex); 2 .. 128 = that many
+ *               chunks; 0 = chosen from the problem size and the number of
+ *               multiprocessors (1 when the problem already fills the GPU).
+ *
+ * Scratch: with more than one split the call allocates
+ * num_splits * rows * (D + 1) * 4 bytes of device memory (rows = number of
+ * LSE entries) with cudaMallocAsync on `stream` and frees it with
+ * cudaFreeAsync after the merge, both stream-ordered; the merge is a second
+ * kernel on the same stream.  Returns as fa_fwd_ex; FA_ERR_INVALID_ARG also
+ * for num_splits outside 0 .. 128, FA_ERR_CUDA if the scratch cannot be
+ * allocated.
+ */
+int fa_fwd_split(const void *q, const void *k, const void *v, void *o, float *lse,
+                 int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
+                 const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                 fa_stream_t stream, int dtype,
+                 int window_left, int window_right, float softcap,
+                 const float *alibi_slopes, int num_splits);
+
+/*
+ * fa_split_plan — the split count fa_fwd_split would use for these sizes
+ * (varlen: 1 for packed problems, where Sq / Sk are the packed totals) and
+ * the device scratch it would allocate (bytes, written to *scratch_bytes if
+ * non-NULL).  num_splits = 0 asks for the library's choice on the current
+ * device.  Returns the split count (>= 1), or minus a status code.
+ */
+int fa_split_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int varlen,
+                  int num_splits, long long *scratch_bytes);
+
+/*
  * fa_get_device_error — synchronize `stream`, then return and clear the status
  * word that kernels on the current device set on a device-side error
  * (FA_OK if none).  Returns FA_ERR_CUDA if the synchronization itself fails.

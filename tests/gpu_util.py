@@ -22,8 +22,9 @@ def to_device(case, dev="cuda:0"):
     return q, k, v, cu_q, cu_k
 
 
-def run_gpu(case, dev="cuda:0", with_lse=True, stream=None):
-    """Run fa_fwd on the case; returns (o, lse) device tensors (library layout)."""
+def run_gpu(case, dev="cuda:0", with_lse=True, stream=None, num_splits=None):
+    """Run fa_fwd on the case (fa_fwd_ex with score variants, fa_fwd_split when
+    ``num_splits`` is given); returns (o, lse) device tensors (library layout)."""
     q, k, v, cu_q, cu_k = to_device(case, dev)
     o = torch.full_like(q, float("nan"))
     shape = (case.Hq, case.Sq) if case.varlen else (case.B, case.Hq, case.Sq)
@@ -31,8 +32,11 @@ def run_gpu(case, dev="cuda:0", with_lse=True, stream=None):
     args = (q, k, v, o, lse, case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D, case.scale,
             int(case.causal), cu_q, cu_k, stream or torch.cuda.current_stream(),
             wl.DTYPE_CODE[case.dtype])
-    if case.has_variants:
-        slopes = case.alibi_slopes.to(dev) if case.alibi_slopes is not None else None
+    slopes = case.alibi_slopes.to(dev) if case.alibi_slopes is not None else None
+    if num_splits is not None:
+        st = fa.fa_fwd_split(*args, case.window_left, case.window_right, case.softcap, slopes,
+                             num_splits)
+    elif case.has_variants:
         st = fa.fa_fwd_ex(*args, case.window_left, case.window_right, case.softcap, slopes)
     else:
         st = fa.fa_fwd(*args)

@@ -78,6 +78,23 @@ def test_variant_arguments_rejected_without_launch(lib, bad):
     assert _call_ex(**bad) == fa.FA_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("splits", [-1, 129, 1 << 20])
+def test_split_count_out_of_range_rejected(lib, splits):
+    args = dict(q=16, k=16, v=16, o=16, lse=None, B=1, Hq=2, Hkv=2, Sq=8, Sk=8, D=64,
+                scale=0.125, causal=0, cu_seqlens_q=None, cu_seqlens_k=None, stream=None,
+                dtype=fa.FA_DTYPE_BF16)
+    assert fa.fa_fwd_split(**args, num_splits=splits) == fa.FA_ERR_INVALID_ARG
+
+
+def test_split_plan_forced_counts_and_scratch(lib):
+    assert fa.fa_split_plan(2, 8, 2, 100, 5000, 128, 0, 4) == (4, 4 * 2 * 8 * 100 * 129 * 4)
+    assert fa.fa_split_plan(3, 4, 4, 70, 90, 64, 1, 1) == (1, 0)
+    assert fa.fa_split_plan(0, 4, 4, 70, 90, 64, 0, 0) == (1, 0)   # no rows: nothing to split
+    assert fa.fa_split_plan(1, 3, 2, 8, 8, 64, 0, 2)[0] == -fa.FA_ERR_INVALID_ARG
+    assert fa.fa_split_plan(1, 2, 2, 8, 8, 96, 0, 2)[0] == -fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_split_plan(1, 2, 2, 8, 8, 64, 0, 200)[0] == -fa.FA_ERR_INVALID_ARG
+
+
 def test_variant_empty_problems_are_noops(lib):
     assert _call_ex(B=0, window_left=3, softcap=30.0) == fa.FA_OK
     assert _call_ex(Sq=0, alibi_slopes=16) == fa.FA_OK
