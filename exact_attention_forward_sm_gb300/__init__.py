@@ -18,8 +18,9 @@ import threading
 
 __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
-    "FA_ERR_BAD_SEQLENS", "FA_DTYPE_FP16", "FA_DTYPE_BF16", "LibraryMissing", "FaError",
+    "FA_ERR_BAD_SEQLENS", "FA_ERR_SCRATCH_LIMIT", "FA_DTYPE_FP16", "FA_DTYPE_BF16", "LibraryMissing", "FaError",
     "library_path", "load_library", "fa_fwd", "fa_fwd_ex", "fa_fwd_split", "fa_split_plan",
+    "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes",
     "fa_get_device_error", "fa_debug_wait_timeout",
     "fa_debug_trace_read",
     "fa_status_string", "fa_version", "attention_forward", "EXPORTED_SYMBOLS",
@@ -31,10 +32,12 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_BAD_SEQLENS = 5
+FA_ERR_SCRATCH_LIMIT = 6
 FA_DTYPE_FP16 = 0
 FA_DTYPE_BF16 = 1
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_split", "fa_split_plan",
+                    "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes",
                     "fa_get_device_error", "fa_debug_wait_timeout",
                     "fa_debug_trace_read", "fa_status_string", "fa_version")
 
@@ -82,6 +85,10 @@ def load_library():
         lib.fa_fwd_split.restype = i32
         lib.fa_split_plan.argtypes = [i32] * 8 + [ctypes.POINTER(ctypes.c_longlong)]
         lib.fa_split_plan.restype = i32
+        lib.fa_fwd_split_noalloc.argtypes = lib.fa_fwd_split.argtypes
+        lib.fa_fwd_split_noalloc.restype = i32
+        lib.fa_noalloc_scratch_bytes.argtypes = []
+        lib.fa_noalloc_scratch_bytes.restype = ctypes.c_longlong
         lib.fa_get_device_error.argtypes = [vp]
         lib.fa_get_device_error.restype = i32
         lib.fa_debug_wait_timeout.argtypes = [ctypes.c_longlong, vp]
@@ -144,6 +151,23 @@ def fa_fwd_split(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal,
                             int(causal), _addr(cu_seqlens_q), _addr(cu_seqlens_k),
                             _stream(stream), int(dtype), int(window_left), int(window_right),
                             float(softcap), _addr(alibi_slopes), int(num_splits))
+
+
+def fa_fwd_split_noalloc(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal,
+                         cu_seqlens_q, cu_seqlens_k, stream, dtype, window_left=-1,
+                         window_right=-1, softcap=0.0, alibi_slopes=None, num_splits=0) -> int:
+    """Call the C ``fa_fwd_split_noalloc`` (split scratch in a fixed device array)."""
+    lib = load_library()
+    return lib.fa_fwd_split_noalloc(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse),
+                                    int(B), int(Hq), int(Hkv), int(Sq), int(Sk), int(D),
+                                    float(scale), int(causal), _addr(cu_seqlens_q),
+                                    _addr(cu_seqlens_k), _stream(stream), int(dtype),
+                                    int(window_left), int(window_right), float(softcap),
+                                    _addr(alibi_slopes), int(num_splits))
+
+
+def fa_noalloc_scratch_bytes() -> int:
+    return int(load_library().fa_noalloc_scratch_bytes())
 
 
 def fa_split_plan(B, Hq, Hkv, Sq, Sk, D, varlen, num_splits=0):

@@ -16,6 +16,11 @@
 // Host code only ever uses its device address, fetched per device below.
 __device__ int g_fa_status;
 
+// Fixed split-KV scratch of fa_fwd_split_noalloc (that call allocates nothing;
+// concurrent calls on one device share this array).
+constexpr size_t kFixedScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_fa_fixed_scratch[kFixedScratchBytes];
+
 #ifdef FA_TRACE
 // Pipeline trace buffer of trace builds (see FA_TRACE_AT in the kernel).
 __device__ unsigned long long g_fa_trace[fa::kTraceEntries];
@@ -97,6 +102,23 @@ int *status_ptr(int device) {
   return g_status_ptr[device];
 }
 
+void *g_fixed_scratch[kMaxDevices] = {};
+
+// Device address of g_fa_fixed_scratch on `device` (looked up once per device).
+void *fixed_scratch_ptr(int device) {
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_fixed_scratch[device]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fa_fixed_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_fixed_scratch[device] = ptr;
+  }
+  return g_fixed_scratch[device];
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Tensor map over a [batch, rows, heads, D] (or packed [rows, heads, D]) buffer,
@@ -152,14 +174,22 @@ int auto_splits(int B, int Hq, int Hkv, int Sq, int Sk, bool varlen, int sms) {
                        (per_seq + fa::kBlockN - 1) / fa::kBlockN, sms);
 }
 
-// Shared body of fa_fwd, fa_fwd_ex and fa_fwd_split.  Window bounds < 0 are
-// unbounded; softcap 0 and alibi == nullptr switch those variants off;
-// num_splits 1 = no split, 0 = choose.
+// Caller-chosen split-KV scratch (fa_fwd_split_noalloc): used instead of a
+// stream-ordered allocation.
+struct FixedScratch {
+  void *ptr;
+  size_t bytes;
+};
+
+// Shared body of fa_fwd, fa_fwd_ex, fa_fwd_split and fa_fwd_split_noalloc.
+// Window bounds < 0 are unbounded; softcap 0 and alibi == nullptr switch those
+// variants off; num_splits 1 = no split, 0 = choose; fixed != nullptr takes
+// the split scratch from that buffer instead of allocating it.
 int forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
             int Hkv, int Sq, int Sk, int D, float scale, int causal,
             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, fa_stream_t stream,
             int dtype, int window_left, int window_right, float softcap,
-            const float *alibi_slopes, int num_splits) {
+            const float *alibi_slopes, int num_splits, const FixedScratch *fixed = nullptr) {
   if (num_splits < 0 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
   // ---------------------------------------------------------- argument checks
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
@@ -276,17 +306,25 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.device = device;
 
-  // split-KV scratch: stream-ordered allocation, freed after the combine
+  // split-KV scratch: the caller's fixed buffer, else a stream-ordered
+  // allocation freed after the combine
   void *scratch = nullptr;
   if (splits > 1) {
     const size_t o_bytes = (size_t)splits * (size_t)lse_rows * (size_t)D * sizeof(float);
     const size_t l_bytes = (size_t)splits * (size_t)lse_rows * sizeof(float);
-    if (cudaMallocAsync(&scratch, o_bytes + l_bytes, a.stream) != cudaSuccess) {
-      cudaGetLastError();
-      return FA_ERR_CUDA;
+    char *base = nullptr;
+    if (fixed) {
+      if (o_bytes + l_bytes > fixed->bytes) return FA_ERR_SCRATCH_LIMIT;
+      base = static_cast<char *>(fixed->ptr);
+    } else {
+      if (cudaMallocAsync(&scratch, o_bytes + l_bytes, a.stream) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+      }
+      base = static_cast<char *>(scratch);
     }
-    p.o_part = static_cast<float *>(scratch);
-    p.lse_part = reinterpret_cast<float *>(static_cast<char *>(scratch) + o_bytes);
+    p.o_part = reinterpret_cast<float *>(base);
+    p.lse_part = reinterpret_cast<float *>(base + o_bytes);
   }
 
   cudaError_t e;
@@ -335,6 +373,7 @@ const char *fa_status_string(int status) {
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_TIMEOUT: return "device pipeline wait timed out";
     case FA_ERR_BAD_SEQLENS: return "cu_seqlens inconsistent with Sq / Sk";
+    case FA_ERR_SCRATCH_LIMIT: return "split scratch larger than the fixed buffer";
     default: return "unknown status";
   }
 }
@@ -366,6 +405,24 @@ int fa_fwd_split(const void *q, const void *k, const void *v, void *o, float *ls
                  cu_seqlens_k, stream, dtype, window_left, window_right, softcap, alibi_slopes,
                  num_splits);
 }
+
+int fa_fwd_split_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
+                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                         fa_stream_t stream, int dtype, int window_left, int window_right,
+                         float softcap, const float *alibi_slopes, int num_splits) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
+  FixedScratch fixed;
+  fixed.ptr = fixed_scratch_ptr(device);
+  fixed.bytes = kFixedScratchBytes;
+  if (!fixed.ptr) return FA_ERR_CUDA;
+  return forward(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, cu_seqlens_q,
+                 cu_seqlens_k, stream, dtype, window_left, window_right, softcap, alibi_slopes,
+                 num_splits, &fixed);
+}
+
+long long fa_noalloc_scratch_bytes(void) { return (long long)kFixedScratchBytes; }
 
 int fa_split_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int varlen, int num_splits,
                   long long *scratch_bytes) {

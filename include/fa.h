@@ -44,7 +44,9 @@ enum {
   FA_ERR_UNSUPPORTED = 2,  /* valid but not built (e.g. head dim other than 64 / 128)      */
   FA_ERR_CUDA = 3,         /* a CUDA runtime / driver call failed (no device, launch error) */
   FA_ERR_TIMEOUT = 4,      /* device: a pipeline wait exceeded its limit; outputs invalid    */
-  FA_ERR_BAD_SEQLENS = 5   /* device: cu_seqlens not monotone or beyond Sq / Sk; rows skipped */
+  FA_ERR_BAD_SEQLENS = 5,  /* device: cu_seqlens not monotone or beyond Sq / Sk; rows skipped */
+  FA_ERR_SCRATCH_LIMIT = 6 /* fa_fwd_split_noalloc: the split scratch would exceed its fixed
+                              buffer; nothing launched */
 };
 
 /* Element type of q, k, v and o. */
@@ -164,6 +166,38 @@ int fa_fwd_split(const void *q, const void *k, const void *v, void *o, float *ls
                  fa_stream_t stream, int dtype,
                  int window_left, int window_right, float softcap,
                  const float *alibi_slopes, int num_splits);
+
+/*
+ * fa_fwd_split_noalloc — fa_fwd_split that allocates nothing.  It has no
+ * counterpart in the pages: it exists for callers that must not allocate
+ * device memory per call.  Arguments, results and status codes are those of
+ * fa_fwd_split, computed by the same kernels.
+ *
+ * Scratch: instead of allocating, the split partials (num_splits * rows *
+ * (D + 1) * 4 bytes, see fa_split_plan) live in one fixed device array of
+ * fa_noalloc_scratch_bytes() bytes (32 MiB) inside the library, one per
+ * device.  A call whose partials would not fit returns FA_ERR_SCRATCH_LIMIT
+ * with nothing launched (pass a smaller num_splits, or use fa_fwd_split).
+ * A call that needs no split (num_splits resolving to 1) does not touch the
+ * array.  Nothing in the array has to start at zero: every partial slot the
+ * merge reads is written by the same call first.
+ *
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress (and fails with FA_ERR_CUDA if that lookup fails);
+ * make that first call before any stream capture.  Calls that may overlap in
+ * time on one device (different streams, or different host threads) share
+ * the array and race: their outputs are then undefined.  Serialise them on
+ * one stream, or use fa_fwd_split.
+ */
+int fa_fwd_split_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
+                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                         fa_stream_t stream, int dtype,
+                         int window_left, int window_right, float softcap,
+                         const float *alibi_slopes, int num_splits);
+
+/* Size in bytes of the fixed scratch array of fa_fwd_split_noalloc. */
+long long fa_noalloc_scratch_bytes(void);
 
 /*
  * fa_split_plan — the split count fa_fwd_split would use for these sizes

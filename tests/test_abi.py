@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     assert fa.fa_version() >= 100
-    for code in range(6):
+    for code in range(7):
         assert fa.fa_status_string(code) not in ("", "unknown status")
     assert fa.fa_status_string(99) == "unknown status"
 
