@@ -10,6 +10,8 @@ independent rows); this module only builds it with gcc and marshals arrays.
 
 * :func:`attention` — the plain definition (full score row, softmax, O, LSE),
   optionally with a local window, a tanh soft cap and ALiBi slopes.
+* :func:`attention_kvcache` — the same definition over a contiguous or paged
+  KV cache (keys addressed through the block table, :func:`gather_kv_cache`).
 * :func:`attention_online` — the streaming restatement with the lazy-rescale
   threshold and max lagging of the fork's v1.7 release notes (section 1.2),
   plus its skip / rescale counters and the largest P.
@@ -189,3 +191,58 @@ def row_index_dense(b, h, i, Hq, Sq):
 def row_index_packed(h, t, total_q):
     """LSE index of packed row (h, global token t)."""
     return np.asarray(h, dtype=np.int64) * total_q + t
+
+
+def gather_kv_cache(cache, cache_seqlens, block_table=None):
+    """Keys (or values) of each sequence read out of a KV cache, packed.
+
+    Contiguous cache [B, capacity, Hkv, D]: sequence b's key j is cache[b, j].
+    Paged cache [num_pages, page_rows, Hkv, D] with block_table [B, max_blocks]:
+    key j of sequence b is row j % page_rows of page block_table[b, j // page_rows].
+    Returns (packed [sum_b lk_b, Hkv, D] float32, cu_seqlens [B + 1] int32).
+    """
+    c = _as_f32(cache)
+    lens = np.asarray(cache_seqlens.cpu() if hasattr(cache_seqlens, "cpu") else cache_seqlens,
+                      dtype=np.int64)
+    parts = []
+    for b, lk in enumerate(lens):
+        j = np.arange(int(lk))
+        if block_table is None:
+            parts.append(c[b, j])
+        else:
+            bt = np.asarray(block_table.cpu() if hasattr(block_table, "cpu") else block_table)
+            page_rows = c.shape[1]
+            parts.append(c[bt[b, j // page_rows], j % page_rows])
+    packed = np.concatenate(parts, axis=0) if parts else np.zeros((0,) + c.shape[2:], np.float32)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    return np.ascontiguousarray(packed), cu
+
+
+def attention_kvcache(q, k_cache, v_cache, cache_seqlens, scale, causal, block_table=None,
+                      rows=None, nthreads=0, window_left=-1, window_right=-1, softcap=0.0,
+                      alibi_slopes=None):
+    """Attention of q [B, Sq, Hq, D] over a KV cache (fp64, plain definition).
+
+    Query token i of sequence b sits at position i + lk_b - Sq of its sequence
+    (the bottom-right alignment of the plain path).  The cache is read by
+    :func:`gather_kv_cache`; the attention itself is :func:`attention` on the
+    resulting packed problem.  ``rows`` and the results use the LSE index of
+    the [B, Hq, Sq] layout: (b * Hq + h) * Sq + i.
+    """
+    qf = _as_f32(q)
+    B, Sq, Hq, D = qf.shape
+    k, cu_k = gather_kv_cache(k_cache, cache_seqlens, block_table)
+    v, _ = gather_kv_cache(v_cache, cache_seqlens, block_table)
+    Hkv = k.shape[1] if k.ndim == 3 else _as_f32(k_cache).shape[2]
+    cu_q = (np.arange(B + 1) * Sq).astype(np.int32)
+    total_q = B * Sq
+    if rows is None:
+        rows = np.arange(B * Hq * Sq, dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    b, rem = rows // (Hq * Sq), rows % (Hq * Sq)
+    h, i = rem // Sq, rem % Sq
+    packed_rows = h * total_q + b * Sq + i
+    return attention(qf.reshape(total_q, Hq, D), k, v, B, Hq, Hkv, total_q, int(cu_k[-1]), D,
+                     scale, causal, cu_q, cu_k, rows=packed_rows, nthreads=nthreads,
+                     window_left=window_left, window_right=window_right, softcap=softcap,
+                     alibi_slopes=alibi_slopes)
