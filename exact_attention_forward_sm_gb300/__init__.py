@@ -18,9 +18,10 @@ import threading
 
 __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
-    "FA_ERR_BAD_SEQLENS", "FA_ERR_SCRATCH_LIMIT", "FA_DTYPE_FP16", "FA_DTYPE_BF16", "LibraryMissing", "FaError",
+    "FA_ERR_BAD_SEQLENS", "FA_ERR_SCRATCH_LIMIT", "FA_DTYPE_FP16", "FA_DTYPE_BF16",
+    "LibraryMissing", "FaError",
     "library_path", "load_library", "fa_fwd", "fa_fwd_ex", "fa_fwd_split", "fa_split_plan",
-    "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes",
+    "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes", "fa_fwd_kvcache", "attention_kvcache",
     "fa_get_device_error", "fa_debug_wait_timeout",
     "fa_debug_trace_read",
     "fa_status_string", "fa_version", "attention_forward", "EXPORTED_SYMBOLS",
@@ -37,7 +38,7 @@ FA_DTYPE_FP16 = 0
 FA_DTYPE_BF16 = 1
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_split", "fa_split_plan",
-                    "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes",
+                    "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes", "fa_fwd_kvcache",
                     "fa_get_device_error", "fa_debug_wait_timeout",
                     "fa_debug_trace_read", "fa_status_string", "fa_version")
 
@@ -87,6 +88,9 @@ def load_library():
         lib.fa_split_plan.restype = i32
         lib.fa_fwd_split_noalloc.argtypes = lib.fa_fwd_split.argtypes
         lib.fa_fwd_split_noalloc.restype = i32
+        lib.fa_fwd_kvcache.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
+                                       vp, vp, i32, i32, i32, vp, i32, i32, i32, f32, vp, i32]
+        lib.fa_fwd_kvcache.restype = i32
         lib.fa_noalloc_scratch_bytes.argtypes = []
         lib.fa_noalloc_scratch_bytes.restype = ctypes.c_longlong
         lib.fa_get_device_error.argtypes = [vp]
@@ -164,6 +168,20 @@ def fa_fwd_split_noalloc(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal,
                                     _addr(cu_seqlens_k), _stream(stream), int(dtype),
                                     int(window_left), int(window_right), float(softcap),
                                     _addr(alibi_slopes), int(num_splits))
+
+
+def fa_fwd_kvcache(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Sq, D, scale, causal,
+                   cache_seqlens, block_table, max_blocks, page_rows, num_pages, stream, dtype,
+                   window_left=-1, window_right=-1, softcap=0.0, alibi_slopes=None,
+                   num_splits=0) -> int:
+    """Call the C ``fa_fwd_kvcache`` (attention over a contiguous or paged KV cache)."""
+    lib = load_library()
+    return lib.fa_fwd_kvcache(_addr(q), _addr(k_cache), _addr(v_cache), _addr(o), _addr(lse),
+                              int(B), int(Hq), int(Hkv), int(Sq), int(D), float(scale),
+                              int(causal), _addr(cache_seqlens), _addr(block_table),
+                              int(max_blocks), int(page_rows), int(num_pages), _stream(stream),
+                              int(dtype), int(window_left), int(window_right), float(softcap),
+                              _addr(alibi_slopes), int(num_splits))
 
 
 def fa_noalloc_scratch_bytes() -> int:
@@ -248,4 +266,39 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens_q=None,
                       window_size[1], softcap, alibi_slopes, num_splits)
     if st != FA_OK:
         raise FaError(st)
+    return out, lse
+
+
+def attention_kvcache(q, k_cache, v_cache, cache_seqlens, block_table=None, causal=False,
+                      scale=None, out=None, lse=None, stream=None, window_size=(-1, -1),
+                      softcap=0.0, alibi_slopes=None, num_splits=0):
+    """Attention of q [B, Sq, Hq, D] over a KV cache; returns ``(out, lse)``.
+
+    Contiguous cache: k_cache / v_cache [B, capacity, Hkv, D].  Paged cache:
+    k_cache / v_cache [num_pages, page_rows, Hkv, D] with an int32
+    ``block_table`` [B, max_blocks].  ``cache_seqlens``: int32 [B] keys per
+    sequence.  All tensors on the same CUDA device.
+    """
+    import torch
+
+    dtype = {torch.float16: FA_DTYPE_FP16, torch.bfloat16: FA_DTYPE_BF16}.get(q.dtype)
+    if dtype is None:
+        raise FaError(FA_ERR_UNSUPPORTED, "attention_kvcache (dtype)")
+    B, Sq, Hq, D = q.shape
+    pages, page_rows, Hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    max_blocks = block_table.shape[1] if block_table is not None else 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = fa_fwd_kvcache(q, k_cache, v_cache, out, lse, B, Hq, Hkv, Sq, D, scale,
+                        int(bool(causal)), cache_seqlens, block_table, max_blocks, page_rows,
+                        pages, stream, dtype, window_size[0], window_size[1], softcap,
+                        alibi_slopes, num_splits)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_kvcache")
     return out, lse

@@ -125,14 +125,14 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // box = 128 rows x 64 elements of one head, 128-byte swizzle.  Out-of-range
 // rows read as zero.
 bool make_map(CUtensorMap *m, const void *base, bool bf16, int D, int heads, int64_t rows,
-              int64_t batch) {
+              int64_t batch, int box_heads = 1, int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows,
                               (cuuint64_t)batch};
   const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2,
                                  (cuuint64_t)rows * heads * D * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t box[4] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -180,6 +180,51 @@ struct FixedScratch {
   void *ptr;
   size_t bytes;
 };
+
+// Launch the attention kernel (`launch`) and, with more than one split, the
+// combine that merges its partials; the split scratch is the caller's fixed
+// buffer or a stream-ordered allocation freed after the combine.
+template <class LaunchFn>
+int run_split(fa::LaunchArgs &a, int splits, int64_t lse_rows, int D, bool bf16, void *o,
+              float *lse, int B, int Hq, int Sq, const int32_t *cu_q, int sms,
+              const FixedScratch *fixed, LaunchFn launch) {
+  void *scratch = nullptr;
+  if (splits > 1) {
+    const size_t o_bytes = (size_t)splits * (size_t)lse_rows * (size_t)D * sizeof(float);
+    const size_t l_bytes = (size_t)splits * (size_t)lse_rows * sizeof(float);
+    char *base = nullptr;
+    if (fixed) {
+      if (o_bytes + l_bytes > fixed->bytes) return FA_ERR_SCRATCH_LIMIT;
+      base = static_cast<char *>(fixed->ptr);
+    } else {
+      if (cudaMallocAsync(&scratch, o_bytes + l_bytes, a.stream) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+      }
+      base = static_cast<char *>(scratch);
+    }
+    a.p.o_part = reinterpret_cast<float *>(base);
+    a.p.lse_part = reinterpret_cast<float *>(base + o_bytes);
+  }
+  cudaError_t e = launch(a);
+  if (e == cudaSuccess && splits > 1) {
+    fa::CombineParams c;
+    c.o_part = a.p.o_part;
+    c.lse_part = a.p.lse_part;
+    c.o = o;
+    c.lse = lse;
+    c.rows = lse_rows;
+    c.num_splits = splits;
+    c.B = B;
+    c.Hq = Hq;
+    c.Sq = Sq;
+    c.cu_q = cu_q;
+    e = fa::launch_combine(c, D, bf16, sms, a.stream);
+  }
+  if (scratch && cudaFreeAsync(scratch, a.stream) != cudaSuccess && e == cudaSuccess)
+    e = cudaErrorUnknown;
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 // Shared body of fa_fwd, fa_fwd_ex, fa_fwd_split and fa_fwd_split_noalloc.
 // Window bounds < 0 are unbounded; softcap 0 and alibi == nullptr switch those
@@ -292,6 +337,11 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   p.o_part = nullptr;
   p.lse_part = nullptr;
   p.part_rows = lse_rows;
+  p.cache_seqlens = nullptr;
+  p.block_table = nullptr;
+  p.max_blocks = p.page_rows = p.num_pages = 0;
+  p.tok_per_tile = fa::kBlockM;
+  p.tok_blocks = 0;
   p.wait_limit = kDefaultWaitLimit;
   p.status = status;
   p.trace = nullptr;
@@ -306,57 +356,133 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.device = device;
 
-  // split-KV scratch: the caller's fixed buffer, else a stream-ordered
-  // allocation freed after the combine
-  void *scratch = nullptr;
-  if (splits > 1) {
-    const size_t o_bytes = (size_t)splits * (size_t)lse_rows * (size_t)D * sizeof(float);
-    const size_t l_bytes = (size_t)splits * (size_t)lse_rows * sizeof(float);
-    char *base = nullptr;
-    if (fixed) {
-      if (o_bytes + l_bytes > fixed->bytes) return FA_ERR_SCRATCH_LIMIT;
-      base = static_cast<char *>(fixed->ptr);
-    } else {
-      if (cudaMallocAsync(&scratch, o_bytes + l_bytes, a.stream) != cudaSuccess) {
-        cudaGetLastError();
-        return FA_ERR_CUDA;
-      }
-      base = static_cast<char *>(scratch);
+  auto launch = [&](const fa::LaunchArgs &la) {
+    if (ext) {
+      if (D == 64)
+        return bf16 ? fa::launch_ext_d64_bf16(la, varlen) : fa::launch_ext_d64_fp16(la, varlen);
+      return bf16 ? fa::launch_ext_d128_bf16(la, varlen) : fa::launch_ext_d128_fp16(la, varlen);
     }
-    p.o_part = reinterpret_cast<float *>(base);
-    p.lse_part = reinterpret_cast<float *>(base + o_bytes);
-  }
-
-  cudaError_t e;
-  if (ext) {
     if (D == 64)
-      e = bf16 ? fa::launch_ext_d64_bf16(a, varlen) : fa::launch_ext_d64_fp16(a, varlen);
-    else
-      e = bf16 ? fa::launch_ext_d128_bf16(a, varlen) : fa::launch_ext_d128_fp16(a, varlen);
-  } else if (D == 64) {
-    e = bf16 ? fa::launch_d64_bf16(a, plain_causal, varlen)
-             : fa::launch_d64_fp16(a, plain_causal, varlen);
-  } else {
-    e = bf16 ? fa::launch_d128_bf16(a, plain_causal, varlen)
-             : fa::launch_d128_fp16(a, plain_causal, varlen);
-  }
-  if (e == cudaSuccess && splits > 1) {
-    fa::CombineParams c;
-    c.o_part = p.o_part;
-    c.lse_part = p.lse_part;
-    c.o = o;
-    c.lse = lse;
-    c.rows = lse_rows;
-    c.num_splits = splits;
-    c.B = B;
-    c.Hq = Hq;
-    c.Sq = Sq;
-    c.cu_q = cu_seqlens_q;
-    e = fa::launch_combine(c, D, bf16, sms, a.stream);
-  }
-  if (scratch && cudaFreeAsync(scratch, a.stream) != cudaSuccess && e == cudaSuccess)
-    e = cudaErrorUnknown;
-  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+      return bf16 ? fa::launch_d64_bf16(la, plain_causal, varlen)
+                  : fa::launch_d64_fp16(la, plain_causal, varlen);
+    return bf16 ? fa::launch_d128_bf16(la, plain_causal, varlen)
+                : fa::launch_d128_fp16(la, plain_causal, varlen);
+  };
+  return run_split(a, splits, lse_rows, D, bf16, o, lse, B, Hq, Sq, cu_seqlens_q, sms, fixed,
+                   launch);
+}
+
+// Body of fa_fwd_kvcache (see include/fa.h).
+int forward_kvcache(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                    int B, int Hq, int Hkv, int Sq, int D, float scale, int causal,
+                    const int32_t *cache_seqlens, const int32_t *block_table, int max_blocks,
+                    int page_rows, int num_pages, fa_stream_t stream, int dtype,
+                    int window_left, int window_right, float softcap,
+                    const float *alibi_slopes, int num_splits) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || D <= 0) return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(softcap) || softcap < 0.f) return FA_ERR_INVALID_ARG;
+  const float cap_k = softcap > 0.f ? 2.f * scale * 1.4426950408889634f / softcap : 0.f;
+  if (!std::isfinite(cap_k)) return FA_ERR_INVALID_ARG;
+  if (num_splits < 0 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+  if (page_rows <= 0) return FA_ERR_INVALID_ARG;
+  const bool paged = block_table != nullptr;
+  if (paged && (max_blocks <= 0 || num_pages <= 0 || page_rows % fa::kBlockN != 0))
+    return FA_ERR_INVALID_ARG;
+  if (paged && (reinterpret_cast<uintptr_t>(block_table) & 3u)) return FA_ERR_INVALID_ARG;
+  if (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  const int group = Hq / Hkv;
+  if (group > fa::kBlockM || (fa::kBlockM % group) != 0) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || Sq == 0) return FA_OK;
+  if (!q || !o || !k_cache || !v_cache || !cache_seqlens) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+    return FA_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(cache_seqlens) & 3u) return FA_ERR_INVALID_ARG;
+
+  const int64_t capacity = paged ? (int64_t)max_blocks * page_rows : page_rows;
+  const int64_t span = (int64_t)Sq + capacity;
+  int win_l = (window_left < 0 || window_left > span) ? -1 : window_left;
+  int win_r = (window_right < 0 || window_right > span) ? -1 : window_right;
+  if (causal) win_r = 0;
+
+  const int tok_per_tile = fa::kBlockM / group;
+  const int64_t tok_blocks = (Sq + tok_per_tile - 1) / tok_per_tile;
+  const int64_t base_units = (int64_t)B * Hkv * tok_blocks;
+  if (base_units > 0x7fffffffll) return FA_ERR_UNSUPPORTED;
+
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
+  int *status = status_ptr(device);
+  const int sms = sm_count(device);
+  if (!status || sms <= 0) return FA_ERR_CUDA;
+  const int splits = num_splits ? num_splits
+                                : choose_splits(base_units, (capacity + fa::kBlockN - 1) /
+                                                                fa::kBlockN, sms);
+  const int64_t units = base_units * splits;
+  if (units > 0x7fffffffll) return FA_ERR_UNSUPPORTED;
+  const int64_t lse_rows = (int64_t)B * Hq * Sq;
+
+  fa::LaunchArgs a;
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  // q / o: tiles of (tok_per_tile tokens) x (group heads) starting at head hkv * group
+  if (!make_map(&a.tm_q, q, bf16, D, Hq, Sq, B, group, tok_per_tile)) return FA_ERR_CUDA;
+  if (!make_map(&a.tm_o, o, bf16, D, Hq, Sq, B, group, tok_per_tile)) return FA_ERR_CUDA;
+  // cache: [pages, page_rows, Hkv, D] (contiguous cache: one page per sequence)
+  const int64_t pages = paged ? num_pages : B;
+  if (!make_map(&a.tm_k, k_cache, bf16, D, Hkv, page_rows, pages)) return FA_ERR_CUDA;
+  if (!make_map(&a.tm_v, v_cache, bf16, D, Hkv, page_rows, pages)) return FA_ERR_CUDA;
+  fa::FwdParams &p = a.p;
+  p.o = o;
+  p.lse = lse;
+  p.cu_q = nullptr;
+  p.cu_k = nullptr;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = (int)std::min<int64_t>(capacity, 0x7fffffff);
+  p.group = group;
+  p.pair_heads = 0;
+  p.head_units = Hkv;
+  p.rows_per_unit = tok_per_tile;
+  p.dense_row_units = (int)tok_blocks;
+  p.total_units = (int)units;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.threshold = FA_RESCALE_THRESHOLD;
+  p.win_l = win_l;
+  p.win_r = win_r;
+  p.reverse_rows = 0;
+  p.cap_k = cap_k;
+  p.cap_l2 = softcap * 1.4426950408889634f;
+  p.alibi = alibi_slopes;
+  p.num_splits = splits;
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
+  p.part_rows = lse_rows;
+  p.cache_seqlens = cache_seqlens;
+  p.block_table = block_table;
+  p.max_blocks = paged ? max_blocks : 1;
+  p.page_rows = page_rows;
+  p.num_pages = (int)pages;
+  p.tok_per_tile = tok_per_tile;
+  p.tok_blocks = (int)tok_blocks;
+  p.wait_limit = kDefaultWaitLimit;
+  p.status = status;
+  p.trace = nullptr;
+  a.grid = (int)(units < sms ? units : sms);
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  a.device = device;
+  auto launch = [&](const fa::LaunchArgs &la) {
+    if (D == 64) return bf16 ? fa::launch_kvc_d64_bf16(la) : fa::launch_kvc_d64_fp16(la);
+    return bf16 ? fa::launch_kvc_d128_bf16(la) : fa::launch_kvc_d128_fp16(la);
+  };
+  return run_split(a, splits, lse_rows, D, bf16, o, lse, B, Hq, Sq, nullptr, sms, nullptr,
+                   launch);
 }
 
 }  // namespace
@@ -420,6 +546,17 @@ int fa_fwd_split_noalloc(const void *q, const void *k, const void *v, void *o, f
   return forward(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, cu_seqlens_q,
                  cu_seqlens_k, stream, dtype, window_left, window_right, softcap, alibi_slopes,
                  num_splits, &fixed);
+}
+
+int fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                   int B, int Hq, int Hkv, int Sq, int D, float scale, int causal,
+                   const int32_t *cache_seqlens, const int32_t *block_table, int max_blocks,
+                   int page_rows, int num_pages, fa_stream_t stream, int dtype,
+                   int window_left, int window_right, float softcap,
+                   const float *alibi_slopes, int num_splits) {
+  return forward_kvcache(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Sq, D, scale, causal,
+                         cache_seqlens, block_table, max_blocks, page_rows, num_pages, stream,
+                         dtype, window_left, window_right, softcap, alibi_slopes, num_splits);
 }
 
 long long fa_noalloc_scratch_bytes(void) { return (long long)kFixedScratchBytes; }

@@ -102,6 +102,21 @@ struct FwdParams {
   float *o_part;            // [num_splits][part_rows][D] fp32, O_s / l_s
   float *lse_part;          // [num_splits][part_rows] fp32, LSE_s (-inf: no visible key)
   int64_t part_rows;        // rows per split slab: one per LSE entry
+  // KV-cache decoding (instances with KVC): q / o dense [B, Sq, Hq, D]; the
+  // keys of sequence b are its first cache_seqlens[b] cache rows, key j being
+  // row j % page_rows of page block_table[b * max_blocks + j / page_rows]
+  // (page b when there is no table).  A tile packs the `group` query heads of
+  // one K/V head for tok_per_tile = 128 / group consecutive tokens (row r:
+  // token r / group, head r % group), and both tiles of a unit hold the same
+  // rows and split its K/V tiles between them (even / odd); their partial
+  // results are merged in the epilogue.
+  const int32_t *cache_seqlens;
+  const int32_t *block_table;
+  int max_blocks;           // block_table row length
+  int page_rows;            // cache rows per page
+  int num_pages;            // pages in the cache
+  int tok_per_tile;         // 128 / group
+  int tok_blocks;           // ceil(Sq / tok_per_tile)
   long long wait_limit;     // bounded-wait limit in SM clock cycles
   int *status;              // device status word (first error wins)
   unsigned long long *trace;  // clock64 pipeline trace (trace builds only)
@@ -183,6 +198,7 @@ struct Work {
   int n_kv[2];       // K/V tiles each query tile visits ...
   int kv_begin[2];   // ... starting at this K/V tile of the sequence
   int kv_ub;         // first K/V tile loaded for the unit (min over its tiles)
+  int kv_stride;     // a tile reads every kv_stride-th loaded K/V tile (1, or 2 in KV-cache units)
   int n_max;         // K/V tiles loaded for the unit (the union of both ranges)
 };
 
@@ -203,11 +219,11 @@ __device__ __forceinline__ int tile_kv_count(int m0, int lq, int lk) {
 // count and sets *begin.  With both bounds >= 0 or unbounded, the ranges of two
 // consecutive row tiles overlap or touch, so their union is contiguous.
 __device__ __forceinline__ int window_kv_range(const FwdParams &p, int m0, int lq, int lk,
-                                               int *begin) {
+                                               int *begin, int rows = kBlockM) {
   *begin = 0;
   if (m0 >= lq || lk <= 0) return 0;
   const int off = lk - lq;
-  const int last_row = min(m0 + kBlockM, lq) - 1;
+  const int last_row = min(m0 + rows, lq) - 1;
   const int lo = p.win_l < 0 ? 0 : max(0, m0 + off - p.win_l);
   const int hi = p.win_r < 0 ? lk - 1 : min(lk - 1, last_row + off + p.win_r);
   if (hi < lo) return 0;
@@ -225,11 +241,69 @@ __device__ __forceinline__ int unit_of(int i) {
 // Dense: the row-unit index (heaviest causal rows first) is the slowest-varying
 // part of the unit index.  Packed: units are numbered sequence by sequence
 // (heaviest rows of a sequence first); the warp scans cu_seqlens cooperatively.
+// Cut a unit's K/V tile range [*b, *b + *n) to split `split` of its sequence's
+// nt tiles (chunks of ceil(nt / num_splits) tiles).
+__device__ __forceinline__ void split_range(const FwdParams &p, int split, int lk, int *b,
+                                            int *n) {
+  const int nt = (lk + kBlockN - 1) / kBlockN;
+  const int chunk = (nt + p.num_splits - 1) / p.num_splits;
+  const int lo = split * chunk, hi = min(nt, lo + chunk);
+  const int bb = max(*b, lo), e = min(*b + *n, hi);
+  *n = max(0, e - bb);
+  *b = bb;
+}
+
+// KV-cache unit: (split, K/V head, token block, sequence), split fastest.
+__device__ inline Work decode_work_kvc(const FwdParams &p, int unit, int lane) {
+  Work w;
+  w.valid = 0;
+  w.split = 0;
+  if (p.num_splits > 1) {
+    w.split = unit % p.num_splits;
+    unit /= p.num_splits;
+  }
+  const int hkv = unit % p.Hkv;
+  unit /= p.Hkv;
+  const int tb = unit % p.tok_blocks;
+  const int b = unit / p.tok_blocks;
+  if (b >= p.B) return w;
+  const int lk = p.cache_seqlens[b];
+  const int64_t cap = p.block_table ? (int64_t)p.max_blocks * p.page_rows : p.page_rows;
+  if (lk < 0 || lk > cap) {
+    if (lane == 0) record_status(p.status, 5);
+    return w;
+  }
+  w.b = b;
+  w.hkv = hkv;
+  w.head[0] = w.head[1] = hkv * p.group;
+  w.lq = p.Sq;
+  w.lk = lk;
+  w.m0[0] = w.m0[1] = tb * p.tok_per_tile;
+  w.q_row0 = 0;
+  w.k_row0 = 0;
+  w.map_b = b;
+  w.o_row0 = (int64_t)b * p.Sq;
+  int lo = 0;
+  int n = window_kv_range(p, w.m0[0], w.lq, w.lk, &lo, p.tok_per_tile);
+  if (p.num_splits > 1) split_range(p, w.split, lk, &lo, &n);
+  // tile 0 reads K/V tiles lo, lo + 2, ...; tile 1 reads lo + 1, lo + 3, ...
+  w.kv_stride = 2;
+  w.kv_ub = lo;
+  w.n_max = n;
+  w.kv_begin[0] = lo;
+  w.kv_begin[1] = lo + 1;
+  w.n_kv[0] = (n + 1) / 2;
+  w.n_kv[1] = n / 2;
+  w.valid = 1;
+  return w;
+}
+
 template <bool CAUSAL, bool VARLEN, bool EXT>
 __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
   Work w;
   w.valid = 0;
   w.split = 0;
+  w.kv_stride = 1;
   if (EXT && p.num_splits > 1) {  // splits of one unit are adjacent: heavy units stay first
     w.split = unit % p.num_splits;
     unit /= p.num_splits;
@@ -316,15 +390,8 @@ __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
     // split s keeps K/V tiles [s c, s c + c) of the sequence, c = ceil(tiles / splits);
     // cutting two overlapping or touching ranges at the same bounds keeps
     // their union contiguous
-    const int nt = (w.lk + kBlockN - 1) / kBlockN;
-    const int chunk = (nt + p.num_splits - 1) / p.num_splits;
-    const int lo = w.split * chunk, hi = min(nt, lo + chunk);
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const int b = max(w.kv_begin[t], lo), e = min(w.kv_begin[t] + w.n_kv[t], hi);
-      w.n_kv[t] = max(0, e - b);
-      w.kv_begin[t] = b;
-    }
+    split_range(p, w.split, w.lk, &w.kv_begin[0], &w.n_kv[0]);
+    split_range(p, w.split, w.lk, &w.kv_begin[1], &w.n_kv[1]);
   }
   if (w.n_kv[0] == 0 && w.n_kv[1] == 0) {
     w.kv_ub = 0;
@@ -380,7 +447,7 @@ __device__ __forceinline__ void softmax_chunk(const float *x, float scale_log2, 
   tmem_st16(p_addr, pk);
 }
 
-template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT, bool KVC = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -462,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; ok; ++i) {
         const int unit = unit_of(i);
         if (unit >= p.total_units) break;
-        const Work w = decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane);
+        const Work w = (KVC ? decode_work_kvc(p, unit, lane) : decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane));
         if (!w.valid) continue;
         if (lane == 0) {
 #pragma unroll
@@ -480,7 +547,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                           q_full(t), c * 64, w.head[t], w.q_row0 + w.m0[t], w.map_b, pol_q);
             ++q_loads;
           }
+          // KV cache: the page of the next K/V tile is read one tile ahead
+          int next_page = 0;
+          auto page_of = [&](int kt) {
+            int pg = w.map_b;
+            if (p.block_table) {
+              pg = __ldg(p.block_table + (int64_t)w.b * p.max_blocks + (kt * kBlockN) / p.page_rows);
+              if (pg < 0 || pg >= p.num_pages) {
+                record_status(p.status, 5);
+                pg = 0;
+              }
+            }
+            return pg;
+          };
+          if (KVC && w.n_max > 0) next_page = page_of(w.kv_ub);
           for (int j = 0; j < w.n_max && ok; ++j) {
+            int k_row = w.k_row0 + (w.kv_ub + j) * kBlockN, k_b = w.map_b;
+            if (KVC) {
+              k_b = next_page;
+              k_row = ((w.kv_ub + j) * kBlockN) % p.page_rows;
+              if (j + 1 < w.n_max) next_page = page_of(w.kv_ub + j + 1);
+            }
             for (int which = 0; which < 2; ++which) {
               const int idx = issued;
               const int s = idx % L::kStages;
@@ -493,8 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(kv_full(s), L::kTileBytes);
               for (int c = 0; c < L::kChunks; ++c)
                 tma_load_4d(sbase + L::kKVOff + s * L::kTileBytes + c * kChunkBytes, tm,
-                            kv_full(s), c * 64, w.hkv, w.k_row0 + (w.kv_ub + j) * kBlockN,
-                            w.map_b, pol_kv);
+                            kv_full(s), c * 64, w.hkv, k_row, k_b, pol_kv);
               issued = idx + 1;
             }
           }
@@ -581,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; ok; ++i) {
         const int unit = unit_of(i);
         if (unit >= p.total_units) break;
-        const Work w = decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane);
+        const Work w = (KVC ? decode_work_kvc(p, unit, lane) : decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane));
         if (!w.valid || w.n_max == 0) continue;
         if (lane == 0) {
           const int n = w.n_kv[T], n_other = w.n_kv[1 - T];
@@ -589,13 +675,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           // tile read load u-1, then S_T = Q_T K(u)^T if it reads load u.
           // Both issuers walk every bracket, so the turns stay paired even
           // when the tiles' K/V ranges differ (local windows).
+          // (KV-cache units: the tiles take every other load, so a bracket
+          // holds work for one of them and the brackets run to n_max + 1)
+          const int st = KVC ? w.kv_stride : 1;
           const int off = w.kv_begin[T] - w.kv_ub;
           const int off_other = w.kv_begin[1 - T] - w.kv_ub;
-          auto other_reads = [&](int u) { return u >= off_other && u < off_other + n_other; };
-          for (int u = 0; u <= w.n_max && ok; ++u) {
-            const int jq = u - off;  // this tile's step: S_T = Q_T K(jq)^T
-            const bool qk = jq >= 0 && jq < n, pv = jq >= 1 && jq <= n;
-            const int kidx = used + 2 * u, vidx = used + 2 * u - 1;
+          auto reads = [&](int u, int o, int cnt) {
+            const int d = u - o;
+            return d >= 0 && (st == 1 || (d & 1) == 0) && d / st < cnt;
+          };
+          auto other_reads = [&](int u) { return reads(u, off_other, n_other); };
+          for (int u = 0; u <= w.n_max + st - 1 && ok; ++u) {
+            const int d = u - off;
+            const bool mine = d >= 0 && (st == 1 || (d & 1) == 0);
+            const int jq = d / st;  // this tile's step: S_T = Q_T K(jq)^T
+            const bool qk = mine && jq < n, pv = mine && jq >= 1 && jq <= n;
+            const int kidx = used + 2 * u, vidx = used + 2 * (u - st) + 1;
             if (qk && jq == 0) {  // first S_T of the unit: Q_T must have landed
               ok = wait(q_full(T), q_used & 1);
               ++q_used;
@@ -633,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit(o_ready(T));  // tile T of this unit is complete
                 ++o_done;
               }
-              release(vidx, other_reads(u - 1));
+              release(vidx, other_reads(u - st));
             }
             if (qk) {
               tc_commit(s_full(T));
@@ -671,6 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int s_seen = 0;   // S tiles consumed (s_full phases, across units)
     int o_seen = 0;   // finished units of this tile (o_ready phases)
+    [[maybe_unused]] int x_units = 0;  // KV-cache units merged (exchange buffer parity)
     const bool elected = quarter == 0 && lane == 0;  // issues this tile's TMA stores
     const uint32_t stage = sbase + L::kStageOff + t * kChunkBytes;
     // The warpgroup meets at named barrier 1 + t in the epilogue.  To keep every
@@ -681,16 +777,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0;; ++i) {
       const int unit = unit_of(i);
       if (unit >= p.total_units) break;
-      const Work w = decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane);
+      const Work w = (KVC ? decode_work_kvc(p, unit, lane) : decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane));
       if (!w.valid || w.m0[t] >= w.lq) continue;  // no rows of this tile
       const int m0 = w.m0[t];        // per-tile fields read once per unit
       const int n_kv = w.n_kv[t];
       const int lq = w.lq, lk = w.lk;
-      const int qi = m0 + row;       // query row within its sequence
+      // query row within its sequence and its head (KV-cache tiles pack
+      // (token, head) pairs: row r is token m0 + r / group, head r % group)
+      const int qi = KVC ? m0 + row / p.group : m0 + row;
+      const int head = KVC ? w.head[t] + row % p.group : w.head[t];
       const int diag = qi + lk - lq;  // last visible key of this row (causal)
       [[maybe_unused]] const int kv_begin = w.kv_begin[t];
       [[maybe_unused]] const float slope_l2 =
-          (EXT && p.alibi) ? p.alibi[w.head[t]] * 1.4426950408889634f : 0.f;
+          (EXT && p.alibi) ? p.alibi[head] * 1.4426950408889634f : 0.f;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n_kv && ok; ++j) {
         if (!warp_wait(s_full(t), s_seen & 1)) { ok = false; break; }
@@ -702,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld128_wait(s_addr, sr);
         float *s = reinterpret_cast<float *>(sr);
         FA_TRACE_AT(tr, (t * 64 + j) * 8 + 1);
-        const int k0 = (EXT ? kv_begin + j : j) * kBlockN;
+        const int k0 = (EXT ? kv_begin + (KVC ? 2 * j : j) : j) * kBlockN;
         if constexpr (EXT) {
           // scores in log2 units: soft cap c tanh(scale s / c), written as
           // c (1 - 2 / (1 + e^(2 scale s / c))) with the hardware exp2 and
@@ -722,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < kBlockN; ++c) s[c] = fmaf(-slope_l2, fabsf(d0 - (float)c), s[c]);
           }
-          const int last_row = min(m0 + kBlockM, lq) - 1;
+          const int last_row = min(m0 + (KVC ? p.tok_per_tile : kBlockM), lq) - 1;
           const bool need_mask = (k0 + kBlockN > lk) ||
                                  (p.win_r >= 0 && k0 + kBlockN - 1 > m0 + lk - lq + p.win_r) ||
                                  (p.win_l >= 0 && k0 < last_row + lk - lq - p.win_l);
@@ -797,7 +896,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t orr[D];
 #pragma unroll
       for (int k = 0; k < D; ++k) orr[k] = 0u;
-      if (n_kv > 0 && ok) {
+      if constexpr (KVC) {
+        // both tiles hold the same rows over even / odd K/V tiles: tile 1
+        // hands its row max and sum to tile 0 through shared memory (tile 1's
+        // unused output staging buffer, double-buffered by unit), tile 0 reads
+        // both accumulators out of tensor memory and merges them:
+        //   M = max(m0, m1), O = O0 2^(m0 - M) + O1 2^(m1 - M), l likewise
+        float *xm = reinterpret_cast<float *>(smem + L::kStageOff + kChunkBytes) +
+                    (x_units & 1) * 256;
+        float *xl = xm + 128;
+        ++x_units;
+        if (n_kv > 0 && ok) {
+          ok = warp_wait(o_ready(t), o_seen & 1);
+          ++o_seen;
+        }
+        if (t == 1) {
+          xm[row] = (l > 0.f && ok) ? m : -INFINITY;
+          xl[row] = ok ? l : 0.f;
+          tc_fence_before();
+          named_barrier_sync(3, 256);
+          continue;  // tile 0 stores the merged rows
+        }
+        named_barrier_sync(3, 256);
+        tc_fence_after();
+        const int n1 = w.n_kv[1];
+        const float m1 = xm[row], l1 = xl[row];
+        const float mine = l > 0.f ? m : -INFINITY;
+        const float mx = fmaxf(mine, m1);
+        const float a0 = mine == -INFINITY ? 0.f : ex2(mine - mx);
+        const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - mx);
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o1[32];
+            if (n_kv > 0) tmem_ld32_wait(o_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(orr + 32 * c));
+            if (n1 > 0) {
+              tmem_ld32_wait(o_addr + D + c * 32, o1);
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                orr[32 * c + k] = __float_as_uint(__uint_as_float(orr[32 * c + k]) * a0 +
+                                                  __uint_as_float(o1[k]) * a1);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                orr[32 * c + k] = __float_as_uint(__uint_as_float(orr[32 * c + k]) * a0);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (n_kv > 0) mbar_arrive(o_free(0));
+            if (n1 > 0) mbar_arrive(o_free(1));
+          }
+        }
+        l = l * a0 + l1 * a1;
+        m = mx;
+      } else if (n_kv > 0 && ok) {
         ok = warp_wait(o_ready(t), o_seen & 1);
         ++o_seen;
         if (ok) {
@@ -820,8 +974,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         return pack_p<BF16>(__uint_as_float(orr[2 * k]) * inv_l,
                             __uint_as_float(orr[2 * k + 1]) * inv_l);
       };
-      const int64_t li = VARLEN ? (int64_t)w.head[t] * p.Sq + tok
-                                : ((int64_t)w.b * p.Hq + w.head[t]) * p.Sq + qi;
+      const int64_t li = VARLEN ? (int64_t)head * p.Sq + tok
+                                : ((int64_t)w.b * p.Hq + head) * p.Sq + qi;
       const float lse = (l > 0.f) ? (m * scale_log2 + log2f(l)) * 0.69314718055994531f
                                   : -INFINITY;
       // a packed tile cut by its sequence end would spill into the next
@@ -864,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (row_valid && ok) {
-        elem_t *o = reinterpret_cast<elem_t *>(p.o) + (tok * p.Hq + w.head[t]) * (int64_t)D;
+        elem_t *o = reinterpret_cast<elem_t *>(p.o) + (tok * p.Hq + head) * (int64_t)D;
         uint4 *dst = reinterpret_cast<uint4 *>(o);
 #pragma unroll
         for (int k = 0; k < D / 8; ++k)

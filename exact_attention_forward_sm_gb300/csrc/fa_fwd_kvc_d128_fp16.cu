@@ -1,0 +1,7 @@
+// Instantiations of the attention kernel for KV-cache decoding (paged or
+// contiguous cache, packed GQA heads) for head dim 128, fp16.
+#include "fa_launch.cuh"
+
+namespace fa {
+FA_DEFINE_KVC_LAUNCHER(launch_kvc_d128_fp16, 128, false)
+}  // namespace fa

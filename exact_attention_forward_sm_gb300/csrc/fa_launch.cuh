@@ -15,9 +15,9 @@ struct LaunchArgs {
   int device;
 };
 
-template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT = false>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT = false, bool KVC = false>
 cudaError_t launch_fwd(const LaunchArgs &a) {
-  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN, EXT>;
+  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN, EXT, KVC>;
   // opt in to the large dynamic shared memory once per device
   static std::atomic<unsigned long long> configured{0};
   const unsigned long long bit = 1ull << (a.device & 63);
@@ -51,6 +51,10 @@ cudaError_t launch_fwd(const LaunchArgs &a) {
                   : launch_fwd<D, BF16, false, false, true>(a);                 \
   }
 
+// KV-cache decoding instances (score variants included).
+#define FA_DEFINE_KVC_LAUNCHER(NAME, D, BF16)                                   \
+  cudaError_t NAME(const LaunchArgs &a) { return launch_fwd<D, BF16, false, false, true, true>(a); }
+
 cudaError_t launch_d64_fp16(const LaunchArgs &a, bool causal, bool varlen);
 cudaError_t launch_d64_bf16(const LaunchArgs &a, bool causal, bool varlen);
 cudaError_t launch_d128_fp16(const LaunchArgs &a, bool causal, bool varlen);
@@ -59,5 +63,9 @@ cudaError_t launch_ext_d64_fp16(const LaunchArgs &a, bool varlen);
 cudaError_t launch_ext_d64_bf16(const LaunchArgs &a, bool varlen);
 cudaError_t launch_ext_d128_fp16(const LaunchArgs &a, bool varlen);
 cudaError_t launch_ext_d128_bf16(const LaunchArgs &a, bool varlen);
+cudaError_t launch_kvc_d64_fp16(const LaunchArgs &a);
+cudaError_t launch_kvc_d64_bf16(const LaunchArgs &a);
+cudaError_t launch_kvc_d128_fp16(const LaunchArgs &a);
+cudaError_t launch_kvc_d128_bf16(const LaunchArgs &a);
 
 }  // namespace fa

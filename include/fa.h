@@ -168,6 +168,48 @@ int fa_fwd_split(const void *q, const void *k, const void *v, void *o, float *ls
                  const float *alibi_slopes, int num_splits);
 
 /*
+ * fa_fwd_kvcache — attention of new query tokens over a KV cache, the
+ * decoding path of the upstream API (flash_attn_with_kvcache, run as test 4
+ * of the fork's v1.7 notes, section 4.1; paged KV caches per the upstream
+ * survey and the FA4 changelog).  The cache is read as it is; this call does
+ * not append to it.
+ *
+ * Layouts (element type `dtype`, row-major, contiguous):
+ *   q, o      [B, Sq, Hq, D]   the Sq newest tokens of each sequence
+ *   lse       [B, Hq, Sq] fp32 (natural log), or NULL
+ *   contiguous cache (block_table == NULL):
+ *     k_cache, v_cache  [B, page_rows, Hkv, D]: sequence b's keys are rows
+ *     0 .. cache_seqlens[b]-1 of k_cache[b] (page_rows = cache capacity)
+ *   paged cache (block_table != NULL):
+ *     k_cache, v_cache  [num_pages, page_rows, Hkv, D]; block_table int32
+ *     [B, max_blocks]: key j of sequence b is row j % page_rows of page
+ *     block_table[b * max_blocks + j / page_rows]; page_rows must be a
+ *     multiple of 128.
+ *   cache_seqlens  int32 [B] (device): keys of each sequence, 0 ..
+ *     capacity (page_rows without a table, max_blocks * page_rows with one).
+ * Query token i of sequence b sits at position i + (cache_seqlens[b] - Sq)
+ * of its sequence: causal = 1 makes key j visible iff j <= i +
+ * cache_seqlens[b] - Sq (the bottom-right diagonal of fa_fwd).  window_left,
+ * window_right, softcap and alibi_slopes are those of fa_fwd_ex; num_splits
+ * those of fa_fwd_split (0 = chosen; scratch as documented there).
+ *
+ * Hq / Hkv must divide 128: the Hq / Hkv query heads of a K/V head are
+ * processed together, so each K/V tile is read once for all of them.
+ * Returns as fa_fwd; FA_ERR_INVALID_ARG also for page_rows <= 0, a paged
+ * cache with max_blocks <= 0, num_pages <= 0 or page_rows not a multiple of
+ * 128, or a NULL cache_seqlens; FA_ERR_UNSUPPORTED for Hq / Hkv not dividing
+ * 128.  A cache_seqlens entry beyond the capacity, or a block_table entry
+ * outside [0, num_pages), is reported as FA_ERR_BAD_SEQLENS by
+ * fa_get_device_error (the affected outputs are not valid).
+ */
+int fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache, void *o,
+                   float *lse, int B, int Hq, int Hkv, int Sq, int D, float scale,
+                   int causal, const int32_t *cache_seqlens, const int32_t *block_table,
+                   int max_blocks, int page_rows, int num_pages, fa_stream_t stream,
+                   int dtype, int window_left, int window_right, float softcap,
+                   const float *alibi_slopes, int num_splits);
+
+/*
  * fa_fwd_split_noalloc — fa_fwd_split that allocates nothing.  It has no
  * counterpart in the pages: it exists for callers that must not allocate
  * device memory per call.  Arguments, results and status codes are those of

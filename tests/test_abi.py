@@ -95,6 +95,29 @@ def test_split_plan_forced_counts_and_scratch(lib):
     assert fa.fa_split_plan(1, 2, 2, 8, 8, 64, 0, 200)[0] == -fa.FA_ERR_INVALID_ARG
 
 
+def _kvc(**kw):
+    args = dict(q=16, k_cache=16, v_cache=16, o=16, lse=None, B=1, Hq=4, Hkv=2, Sq=1, D=64,
+                scale=0.125, causal=0, cache_seqlens=16, block_table=None, max_blocks=1,
+                page_rows=256, num_pages=1, stream=None, dtype=fa.FA_DTYPE_BF16)
+    args.update(kw)
+    return fa.fa_fwd_kvcache(**args)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(page_rows=0), dict(block_table=16, page_rows=100), dict(block_table=16, max_blocks=0),
+    dict(block_table=16, num_pages=0), dict(block_table=18), dict(cache_seqlens=0),
+    dict(cache_seqlens=18), dict(num_splits=-1), dict(softcap=-2.0), dict(Hq=3),
+    dict(q=8), dict(k_cache=0),
+])
+def test_kvcache_arguments_rejected_without_launch(lib, bad):
+    assert _kvc(**bad) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(6, 2, 64), (4, 2, 96), (256, 1, 64)])
+def test_kvcache_unsupported(lib, Hq, Hkv, D):
+    assert _kvc(Hq=Hq, Hkv=Hkv, D=D) == fa.FA_ERR_UNSUPPORTED
+
+
 def test_variant_empty_problems_are_noops(lib):
     assert _call_ex(B=0, window_left=3, softcap=30.0) == fa.FA_OK
     assert _call_ex(Sq=0, alibi_slopes=16) == fa.FA_OK
