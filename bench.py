@@ -195,6 +195,31 @@ def oracle_sample(case, seconds, seed=0):
             "rows_total": int(n_rows), "flops": fl, "threads": threads}
 
 
+def oracle_sample_kvcache(case, seconds, seed=0):
+    """oracle_sample for a KV-cache workload (rows in [B, Hq, Sq] order)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    n_rows = case.lse_rows()
+    vis = wl.kv_visible_per_row(case).numpy()
+    threads = len(os.sched_getaffinity(0))
+
+    def run(rows):
+        t0 = time.perf_counter()
+        oracle.attention_kvcache(case.q, case.k_cache, case.v_cache, case.cache_seqlens,
+                                 case.scale, case.causal, block_table=case.block_table,
+                                 rows=rows, nthreads=threads)
+        return time.perf_counter() - t0, 4.0 * case.D * float(vis[rows].sum())
+
+    calib = np.sort(rng.choice(n_rows, size=min(n_rows, 64), replace=False))
+    dt, fl = run(calib)
+    rate = fl / max(dt, 1e-6)
+    want = int(min(n_rows, max(64, seconds * rate / max(fl / len(calib), 1.0))))
+    rows = np.sort(rng.choice(n_rows, size=want, replace=False))
+    dt, fl = run(rows)
+    return {"tflops": fl / dt / 1e12, "seconds": dt, "rows": int(len(rows)),
+            "rows_total": int(n_rows), "flops": fl, "threads": threads}
+
+
 def _visible_per_row(case):
     """Visible keys of every row in LSE-index order."""
     out = []
@@ -227,6 +252,110 @@ def _vis_rows(lq, lk, causal, window=(-1, -1)):
 
 # --------------------------------------------------------------- GPU benchmark
 
+class Problem:
+    """One timed workload: device inputs (copied from pinned host memory in the
+    e2e leg), outputs, a launch closure and the work it does per step."""
+
+    def __init__(self, name, dtype, flops, alg_bytes, host_inputs, dev_inputs, outputs, launch,
+                 launches_per_step, config, oracle_sample):
+        self.name, self.dtype = name, dtype
+        self.flops, self.alg_bytes = flops, alg_bytes
+        self.host_inputs, self.dev_inputs, self.outputs = host_inputs, dev_inputs, outputs
+        self.launch, self.launches_per_step = launch, launches_per_step
+        self.config, self.oracle_sample = config, oracle_sample
+
+
+def attention_problem(args, fa, rank, dev, stream):
+    """fa_fwd / fa_fwd_ex / fa_fwd_split over one of the attention workloads."""
+    w = wl.BY_NAME[args.workload]
+    w_rank = wl.Workload(**{**w.__dict__, "seed": rank_seed(w.seed, rank)})
+    case = wl.make_workload(w_rank)
+    dtype_code = wl.DTYPE_CODE[case.dtype]
+    q, k, v = (t.to(dev) for t in (case.q, case.k, case.v))
+    cu_q = case.cu_seqlens_q.to(dev) if case.varlen else None
+    cu_k = case.cu_seqlens_k.to(dev) if case.varlen else None
+    o = torch.empty_like(q)
+    lse_shape = (case.Hq, case.Sq) if case.varlen else (case.B, case.Hq, case.Sq)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    slopes = case.alibi_slopes.to(dev) if case.alibi_slopes is not None else None
+
+    splits = w.splits if args.splits is None else args.splits
+    launches_per_step, used = 1, None
+    if splits >= 0:
+        used, _ = fa.fa_split_plan(case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D,
+                                   case.varlen, splits)
+        if used < 1:
+            raise RuntimeError(f"fa_split_plan: status {-used}")
+        launches_per_step = 2 if used > 1 else 1   # partial pass + combine
+
+    def launch():
+        if splits >= 0:
+            st = fa.fa_fwd_split(q, k, v, o, lse, case.B, case.Hq, case.Hkv, case.Sq,
+                                 case.Sk, case.D, case.scale, int(case.causal), cu_q, cu_k,
+                                 stream, dtype_code, case.window_left, case.window_right,
+                                 case.softcap, slopes, splits)
+        elif case.has_variants:
+            st = fa.fa_fwd_ex(q, k, v, o, lse, case.B, case.Hq, case.Hkv, case.Sq, case.Sk,
+                              case.D, case.scale, int(case.causal), cu_q, cu_k, stream,
+                              dtype_code, case.window_left, case.window_right, case.softcap,
+                              slopes)
+        else:
+            st = fa.fa_fwd(q, k, v, o, lse, case.B, case.Hq, case.Hkv, case.Sq, case.Sk,
+                           case.D, case.scale, int(case.causal), cu_q, cu_k, stream, dtype_code)
+        if st != fa.FA_OK:
+            raise RuntimeError(f"fa_fwd: {fa.fa_status_string(st)}")
+
+    variants = {}
+    if case.has_variants:
+        variants = {"window": [case.window_left, case.window_right], "softcap": case.softcap,
+                    "alibi": "geometric slopes" if case.alibi_slopes is not None else None}
+    config = {"workload": w.name, "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv,
+              "Sq": case.Sq, "Sk": case.Sk, "D": case.D, "causal": case.causal,
+              "varlen": case.varlen, **variants,
+              **({"num_splits": splits, "num_splits_used": used} if splits >= 0 else {})}
+    return Problem(w.name, case.dtype, wl.attention_flops(case), wl.algorithmic_bytes(case),
+                   [case.q, case.k, case.v], [q, k, v], [o, lse], launch, launches_per_step,
+                   config, lambda secs: oracle_sample(case, secs, seed=12345))
+
+
+def kvcache_problem(args, fa, rank, dev, stream):
+    """fa_fwd_kvcache over one of the KV-cache (decoding) workloads."""
+    w = wl.CACHE_BY_NAME[args.workload]
+    case = wl.make_cache_workload(w, seed=rank_seed(w.seed, rank))
+    dtype_code = wl.DTYPE_CODE[case.dtype]
+    q, kc, vc, lens = (t.to(dev) for t in (case.q, case.k_cache, case.v_cache,
+                                           case.cache_seqlens))
+    table = case.block_table.to(dev) if case.block_table is not None else None
+    o = torch.empty_like(q)
+    lse = torch.empty((case.B, case.Hq, case.Sq), dtype=torch.float32, device=dev)
+    splits = w.splits if args.splits is None else args.splits
+    n_pages = case.num_pages
+
+    def launch():
+        st = fa.fa_fwd_kvcache(q, kc, vc, o, lse, case.B, case.Hq, case.Hkv, case.Sq, case.D,
+                               case.scale, int(case.causal), lens, table, case.max_blocks,
+                               case.page_rows, n_pages, stream, dtype_code, -1, -1, 0.0, None,
+                               splits)
+        if st != fa.FA_OK:
+            raise RuntimeError(f"fa_fwd_kvcache: {fa.fa_status_string(st)}")
+
+    cap = case.page_rows * case.max_blocks
+    used, _ = fa.fa_kvcache_plan(case.B, case.Hq, case.Hkv, case.Sq, case.D, cap, splits)
+    if used < 1:
+        raise RuntimeError(f"fa_kvcache_plan: status {-used}")
+    config = {"workload": w.name, "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "Sq": case.Sq,
+              "D": case.D, "causal": case.causal, "cache": "paged" if table is not None
+              else "contiguous", "page_rows": case.page_rows, "capacity": cap,
+              "cache_seqlens_mean": float(case.cache_seqlens.float().mean()),
+              "num_splits": splits, "num_splits_used": used}
+    inputs_h = [case.q, case.k_cache, case.v_cache, case.cache_seqlens] + (
+        [case.block_table] if table is not None else [])
+    inputs_d = [q, kc, vc, lens] + ([table] if table is not None else [])
+    return Problem(w.name, case.dtype, wl.kv_flops(case), wl.kv_algorithmic_bytes(case),
+                   inputs_h, inputs_d, [o, lse], launch, 2 if used > 1 else 1, config,
+                   lambda secs: oracle_sample_kvcache(case, secs, seed=12345))
+
+
 def run_gpu_arm(args, rank, local_rank, world):
     import exact_attention_forward_sm_gb300 as fa
     from exact_attention_forward_sm_gb300 import _build
@@ -236,51 +365,15 @@ def run_gpu_arm(args, rank, local_rank, world):
     if not os.environ.get("FA_AB_NOBUILD"):
         _build.build(variant=args.variant)
     fa.load_library()
-    w = wl.BY_NAME[args.workload]
-    w_rank = wl.Workload(**{**w.__dict__, "seed": rank_seed(w.seed, rank)})
-    case = wl.make_workload(w_rank)
-    flops = wl.attention_flops(case)
-    dtype_code = wl.DTYPE_CODE[case.dtype]
     stream = torch.cuda.current_stream(dev)
-
-    q, k, v = (t.to(dev) for t in (case.q, case.k, case.v))
-    cu_q = case.cu_seqlens_q.to(dev) if case.varlen else None
-    cu_k = case.cu_seqlens_k.to(dev) if case.varlen else None
-    o = torch.empty_like(q)
-    lse_shape = (case.Hq, case.Sq) if case.varlen else (case.B, case.Hq, case.Sq)
-    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    make = kvcache_problem if args.workload in wl.CACHE_BY_NAME else attention_problem
+    prob = make(args, fa, rank, dev, stream)
+    flops = prob.flops
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    slopes = case.alibi_slopes.to(dev) if case.alibi_slopes is not None else None
-
-    splits = w.splits if args.splits is None else args.splits
-    launches_per_step = 1
-    if splits >= 0:
-        used, _ = fa.fa_split_plan(case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D,
-                                   case.varlen, splits)
-        if used < 1:
-            raise RuntimeError(f"fa_split_plan: status {-used}")
-        launches_per_step = 2 if used > 1 else 1   # partial pass + combine
-
-    def launch(qq, kk, vv, oo, ll):
-        if splits >= 0:
-            st = fa.fa_fwd_split(qq, kk, vv, oo, ll, case.B, case.Hq, case.Hkv, case.Sq,
-                                 case.Sk, case.D, case.scale, int(case.causal), cu_q, cu_k,
-                                 stream, dtype_code, case.window_left, case.window_right,
-                                 case.softcap, slopes, splits)
-        elif case.has_variants:
-            st = fa.fa_fwd_ex(qq, kk, vv, oo, ll, case.B, case.Hq, case.Hkv, case.Sq, case.Sk,
-                              case.D, case.scale, int(case.causal), cu_q, cu_k, stream,
-                              dtype_code, case.window_left, case.window_right, case.softcap,
-                              slopes)
-        else:
-            st = fa.fa_fwd(qq, kk, vv, oo, ll, case.B, case.Hq, case.Hkv, case.Sq, case.Sk,
-                           case.D, case.scale, int(case.causal), cu_q, cu_k, stream, dtype_code)
-        if st != fa.FA_OK:
-            raise RuntimeError(f"fa_fwd: {fa.fa_status_string(st)}")
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
-        launch(q, k, v, o, lse)
+        prob.launch()
     torch.cuda.synchronize()
     status = fa.fa_get_device_error(stream)
     if status != fa.FA_OK:
@@ -296,7 +389,7 @@ def run_gpu_arm(args, rank, local_rank, world):
         for i in range(args.steps):
             flush.fill_(float(i))             # evict L2 (outside the kernel's events)
             starts[i].record(stream)
-            launch(q, k, v, o, lse)
+            prob.launch()
             ends[i].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t_wall
@@ -310,11 +403,10 @@ def run_gpu_arm(args, rank, local_rank, world):
     clock = clocks.summary()
 
     # -------------------------------------- end to end through the public API
-    h_q, h_k, h_v = (t.pin_memory() for t in (case.q, case.k, case.v))
-    h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    h_l = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
-    d2h = h_o.numel() * h_o.element_size() + h_l.numel() * h_l.element_size()
+    h_in = [t.pin_memory() for t in prob.host_inputs]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in prob.outputs]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     for i in range(args.warmup + args.steps):
@@ -322,12 +414,11 @@ def run_gpu_arm(args, rank, local_rank, world):
             torch.cuda.synchronize()
             barrier(world)
             e_start.record(stream)
-        q.copy_(h_q, non_blocking=True)
-        k.copy_(h_k, non_blocking=True)
-        v.copy_(h_v, non_blocking=True)
-        launch(q, k, v, o, lse)
-        h_o.copy_(o, non_blocking=True)
-        h_l.copy_(lse, non_blocking=True)
+        for d, h in zip(prob.dev_inputs, h_in):
+            d.copy_(h, non_blocking=True)
+        prob.launch()
+        for h, d in zip(h_out, prob.outputs):
+            h.copy_(d, non_blocking=True)
     e_end.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, world)
@@ -337,7 +428,7 @@ def run_gpu_arm(args, rank, local_rank, world):
     dense_key = "bf16_tflops"
     peak = float(peaks.get(dense_key, PEAK_FALLBACK[dense_key]))
     hbm_peak = float(peaks.get("hbm_gbs", PEAK_FALLBACK["hbm_gbs"]))
-    alg_bytes = wl.algorithmic_bytes(case)
+    alg_bytes = prob.alg_bytes
     # below the ridge point (peak FLOP/s / peak bytes/s) the launch is bound by
     # HBM: report algorithmic bytes / time against the measured copy bandwidth
     hbm_bound = flops / alg_bytes < peak * 1e12 / (hbm_peak * 1e9)
@@ -348,10 +439,6 @@ def run_gpu_arm(args, rank, local_rank, world):
         gbs = alg_bytes / (kernel_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(gbs, 2), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(gbs / hbm_peak, 4)}
-    variants = {}
-    if case.has_variants:
-        variants = {"window": [case.window_left, case.window_right], "softcap": case.softcap,
-                    "alibi": "geometric slopes" if case.alibi_slopes is not None else None}
     line = {
         "metric": METRIC,
         "value": round(world * flops / (kernel_ms_max * 1e-3) / 1e12, 3),
@@ -363,22 +450,19 @@ def run_gpu_arm(args, rank, local_rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": case.dtype,
+        "dtype": prob.dtype,
         "data": "synthetic (seeded N(0, sigma^2) draws cast to 16-bit; no dataset)",
         "config": {
-            "workload": w.name, "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv,
-            "Sq": case.Sq, "Sk": case.Sk, "D": case.D, "causal": case.causal,
-            "varlen": case.varlen, **variants, "flops_per_step_per_gpu": flops,
+            **prob.config, "flops_per_step_per_gpu": flops,
             "algorithmic_bytes_per_step_per_gpu": alg_bytes,
             "l2": "flushed before every step (256 MiB write, outside the kernel events)",
             "parallelism": f"replicas x{world} (independent problems, no collective)",
             "wall_ms_per_step_incl_flush": round(wall * 1e3 / args.steps, 4),
             **({"ablation_variant": args.variant} if args.variant else {}),
-            **({"num_splits": splits, "num_splits_used": used} if splits >= 0 else {}),
         },
         "roofline": {
             **roof,
-            "traffic": profiled_traffic(w.name),
+            "traffic": profiled_traffic(prob.name),
             "peak_source": (f"{peak_src} hbm_gbs (copy bandwidth)" if hbm_bound
                             else f"{peak_src} {dense_key} (burst, cuBLAS bf16)"),
             "kernel": "fa_fwd_kernel",
@@ -392,13 +476,13 @@ def run_gpu_arm(args, rank, local_rank, world):
             "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms, 4),
         },
-        "gpu_launches": args.steps * launches_per_step,
+        "gpu_launches": args.steps * prob.launches_per_step,
         "clocks": clock,
     }
     if "bf16_tflops_sustained" in peaks and not hbm_bound:
         line["roofline"]["frac_of_sustained"] = round(
             achieved / float(peaks["bf16_tflops_sustained"]), 4)
-    return line, case
+    return line, prob
 
 
 def barrier(world):
@@ -442,7 +526,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.BY_NAME))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(wl.BY_NAME) + sorted(wl.CACHE_BY_NAME))
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--reference-budget-s", type=float, default=90.0,
@@ -469,9 +554,9 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    line, case = run_gpu_arm(args, rank, local_rank, world)
+    line, prob = run_gpu_arm(args, rank, local_rank, world)
     if rank == 0 and not args.no_cpu_baseline:
-        cb = oracle_sample(case, args.cpu_baseline_s, seed=12345)
+        cb = prob.oracle_sample(args.cpu_baseline_s)
         line["cpu_baseline"] = {
             "value": cb["tflops"], "unit": UNIT, "cores": cb["threads"], "kind": "oracle",
             "sample": (f"{cb['rows']} of {cb['rows_total']} query rows drawn uniformly from "

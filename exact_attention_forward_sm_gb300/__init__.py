@@ -21,7 +21,7 @@ __all__ = [
     "FA_ERR_BAD_SEQLENS", "FA_ERR_SCRATCH_LIMIT", "FA_DTYPE_FP16", "FA_DTYPE_BF16",
     "LibraryMissing", "FaError",
     "library_path", "load_library", "fa_fwd", "fa_fwd_ex", "fa_fwd_split", "fa_split_plan",
-    "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes", "fa_fwd_kvcache", "attention_kvcache",
+    "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes", "fa_fwd_kvcache", "attention_kvcache", "fa_kvcache_plan",
     "fa_get_device_error", "fa_debug_wait_timeout",
     "fa_debug_trace_read",
     "fa_status_string", "fa_version", "attention_forward", "EXPORTED_SYMBOLS",
@@ -39,6 +39,7 @@ FA_DTYPE_BF16 = 1
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_split", "fa_split_plan",
                     "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes", "fa_fwd_kvcache",
+                    "fa_kvcache_plan",
                     "fa_get_device_error", "fa_debug_wait_timeout",
                     "fa_debug_trace_read", "fa_status_string", "fa_version")
 
@@ -91,6 +92,9 @@ def load_library():
         lib.fa_fwd_kvcache.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
                                        vp, vp, i32, i32, i32, vp, i32, i32, i32, f32, vp, i32]
         lib.fa_fwd_kvcache.restype = i32
+        lib.fa_kvcache_plan.argtypes = [i32] * 5 + [ctypes.c_longlong, i32,
+                                                    ctypes.POINTER(ctypes.c_longlong)]
+        lib.fa_kvcache_plan.restype = i32
         lib.fa_noalloc_scratch_bytes.argtypes = []
         lib.fa_noalloc_scratch_bytes.restype = ctypes.c_longlong
         lib.fa_get_device_error.argtypes = [vp]
@@ -182,6 +186,14 @@ def fa_fwd_kvcache(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Sq, D, scale, causal
                               int(max_blocks), int(page_rows), int(num_pages), _stream(stream),
                               int(dtype), int(window_left), int(window_right), float(softcap),
                               _addr(alibi_slopes), int(num_splits))
+
+
+def fa_kvcache_plan(B, Hq, Hkv, Sq, D, capacity, num_splits=0):
+    """(split count or minus a status code, scratch bytes) of ``fa_fwd_kvcache``."""
+    nbytes = ctypes.c_longlong(0)
+    n = load_library().fa_kvcache_plan(int(B), int(Hq), int(Hkv), int(Sq), int(D),
+                                       int(capacity), int(num_splits), ctypes.byref(nbytes))
+    return n, nbytes.value
 
 
 def fa_noalloc_scratch_bytes() -> int:

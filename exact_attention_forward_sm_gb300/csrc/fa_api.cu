@@ -119,6 +119,18 @@ void *fixed_scratch_ptr(int device) {
   return g_fixed_scratch[device];
 }
 
+// Trace builds: point the kernel at the trace buffer.
+bool set_trace(fa::FwdParams &p) {
+#ifdef FA_TRACE
+  void *tr = nullptr;
+  if (cudaGetSymbolAddress(&tr, g_fa_trace) != cudaSuccess) return false;
+  p.trace = static_cast<unsigned long long *>(tr);
+#else
+  (void)p;
+#endif
+  return true;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Tensor map over a [batch, rows, heads, D] (or packed [rows, heads, D]) buffer,
@@ -345,13 +357,7 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   p.wait_limit = kDefaultWaitLimit;
   p.status = status;
   p.trace = nullptr;
-#ifdef FA_TRACE
-  {
-    void *tr = nullptr;
-    if (cudaGetSymbolAddress(&tr, g_fa_trace) != cudaSuccess) return FA_ERR_CUDA;
-    p.trace = static_cast<unsigned long long *>(tr);
-  }
-#endif
+  if (!set_trace(p)) return FA_ERR_CUDA;
   a.grid = (int)grid;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.device = device;
@@ -420,6 +426,7 @@ int forward_kvcache(const void *q, const void *k_cache, const void *v_cache, voi
   int *status = status_ptr(device);
   const int sms = sm_count(device);
   if (!status || sms <= 0) return FA_ERR_CUDA;
+  // split rule of fa_kvcache_plan (capacity stands in for the device-side lengths)
   const int splits = num_splits ? num_splits
                                 : choose_splits(base_units, (capacity + fa::kBlockN - 1) /
                                                                 fa::kBlockN, sms);
@@ -474,6 +481,7 @@ int forward_kvcache(const void *q, const void *k_cache, const void *v_cache, voi
   p.wait_limit = kDefaultWaitLimit;
   p.status = status;
   p.trace = nullptr;
+  if (!set_trace(p)) return FA_ERR_CUDA;
   a.grid = (int)(units < sms ? units : sms);
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.device = device;
@@ -579,6 +587,33 @@ int fa_split_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int varlen, int
   }
   if (scratch_bytes) {
     const long long rows = (long long)Hq * Sq * (varlen ? 1 : B);
+    *scratch_bytes = splits > 1 ? (long long)splits * rows * (D + 1) * 4 : 0;
+  }
+  return splits;
+}
+
+int fa_kvcache_plan(int B, int Hq, int Hkv, int Sq, int D, long long capacity, int num_splits,
+                    long long *scratch_bytes) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Hq % Hkv != 0 || capacity <= 0)
+    return -FA_ERR_INVALID_ARG;
+  if (num_splits < 0 || num_splits > kMaxSplits) return -FA_ERR_INVALID_ARG;
+  const int group = Hq / Hkv;
+  if ((D != 64 && D != 128) || group > fa::kBlockM || fa::kBlockM % group != 0)
+    return -FA_ERR_UNSUPPORTED;
+  int splits = num_splits;
+  if (B == 0 || Sq == 0) {
+    splits = 1;
+  } else if (splits == 0) {
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return -FA_ERR_CUDA;
+    const int sms = sm_count(device);
+    if (sms <= 0) return -FA_ERR_CUDA;
+    const int tok_per_tile = fa::kBlockM / group;
+    const int64_t units = (int64_t)B * Hkv * ((Sq + tok_per_tile - 1) / tok_per_tile);
+    splits = choose_splits(units, (capacity + fa::kBlockN - 1) / fa::kBlockN, sms);
+  }
+  if (scratch_bytes) {
+    const long long rows = (long long)B * Hq * Sq;
     *scratch_bytes = splits > 1 ? (long long)splits * rows * (D + 1) * 4 : 0;
   }
   return splits;

@@ -143,17 +143,21 @@ constexpr int kTraceEntries = 2048;
   } while (0)
 #endif
 
-template <int D>
+template <int D, bool KVC = false>
 struct Smem {
   static constexpr int kChunks = D / 64;                    // 64-element swizzle chunks
   static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (D == 128) ? 4 : 8;         // K/V ring depth
+  // KV-cache units hold one Q tile (both tiles read the same rows) and store
+  // O row by row, so that room goes to a deeper K/V ring
+  static constexpr int kQBufs = KVC ? 1 : 2;
+  static constexpr int kStages = KVC ? (D == 128 ? 5 : 12) : (D == 128 ? 4 : 8);  // K/V ring depth
   static constexpr uint32_t kQOff = 0;
-  static constexpr uint32_t kKVOff = 2 * kTileBytes;
-  // output staging for the TMA store of the epilogue: 128 rows x 64 columns
-  // (128B-swizzled) per query tile
+  static constexpr uint32_t kKVOff = kQBufs * kTileBytes;
+  // plain: output staging for the TMA store of the epilogue, 128 rows x 64
+  // columns (128B-swizzled) per query tile; KV cache: the row max / sum
+  // exchange of the two tiles (2 x 2 x 128 floats)
   static constexpr uint32_t kStageOff = kKVOff + kStages * kTileBytes;
-  static constexpr uint32_t kBarOff = kStageOff + 2 * kChunkBytes;
+  static constexpr uint32_t kBarOff = kStageOff + (KVC ? 2048 : 2 * kChunkBytes);
   // barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2],
   //           p_half[2][2], o_ready[2], o_free[2], drain
   static constexpr int kNumBars = 4 + 2 * kStages + 11;
@@ -452,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams p) {
-  using L = Smem<D>;
+  using L = Smem<D, KVC>;
   using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -472,6 +476,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
   volatile int *mma_turn = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 8);
+  // K/V loads the producer has issued (KV-cache units): an issuer waits on a
+  // ring slot's barrier only once its load is issued, so it never waits a
+  // whole lap ahead of the slot (the free-running issuers of KV-cache units
+  // share slots, and an mbarrier parity wait cannot tell laps k and k - 2 apart)
+  volatile int *kv_issued = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 12);
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
 
   const int tid = threadIdx.x;
@@ -483,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     for (int t = 0; t < 2; ++t) {
       mbar_init(q_full(t), 1);
-      mbar_init(q_empty(t), 1);
+      mbar_init(q_empty(t), KVC ? 2 : 1);  // KV cache: both tiles read Q buffer 0
       mbar_init(s_full(t), 1);
       mbar_init(p_half(t, 0), 4);  // one arrival per softmax warp
       mbar_init(p_half(t, 1), 4);
@@ -496,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain_bar, 2);      // one per MMA issuer
     *mma_turn = 0;
+    *kv_issued = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -535,7 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             int &q_loads = t ? q_loads1 : q_loads0;
-            if (w.n_kv[t] == 0 || !ok) continue;
+            if (KVC && t == 1) continue;  // one Q tile serves both
+            if ((KVC ? w.n_max : w.n_kv[t]) == 0 || !ok) continue;
             // the previous unit's Q_t is free once its last S_t = Q_t K^T is done
             if (q_loads > 0 && !wait(q_empty(t), (q_loads - 1) & 1)) {
               ok = false;
@@ -547,41 +558,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                           q_full(t), c * 64, w.head[t], w.q_row0 + w.m0[t], w.map_b, pol_q);
             ++q_loads;
           }
-          // KV cache: the page of the next K/V tile is read one tile ahead
-          int next_page = 0;
-          auto page_of = [&](int kt) {
-            int pg = w.map_b;
-            if (p.block_table) {
-              pg = __ldg(p.block_table + (int64_t)w.b * p.max_blocks + (kt * kBlockN) / p.page_rows);
-              if (pg < 0 || pg >= p.num_pages) {
-                record_status(p.status, 5);
-                pg = 0;
-              }
+          // one K or V tile of unit tile j (which: 0 K, 1 V) into the next ring slot
+          auto issue = [&](int which, int j, int page) {
+            const int idx = issued;
+            const int s = idx % L::kStages;
+            if (idx >= L::kStages && !wait(kv_empty(s), ((idx / L::kStages) + 1) & 1)) {
+              ok = false;
+              return;
             }
-            return pg;
-          };
-          if (KVC && w.n_max > 0) next_page = page_of(w.kv_ub);
-          for (int j = 0; j < w.n_max && ok; ++j) {
             int k_row = w.k_row0 + (w.kv_ub + j) * kBlockN, k_b = w.map_b;
             if (KVC) {
-              k_b = next_page;
               k_row = ((w.kv_ub + j) * kBlockN) % p.page_rows;
-              if (j + 1 < w.n_max) next_page = page_of(w.kv_ub + j + 1);
+              k_b = page;
             }
-            for (int which = 0; which < 2; ++which) {
-              const int idx = issued;
-              const int s = idx % L::kStages;
-              if (idx >= L::kStages && !wait(kv_empty(s), ((idx / L::kStages) + 1) & 1)) {
-                ok = false;
-                break;
+            FA_TRACE_AT(idx < 256, 1536 + idx);
+            mbar_arrive_expect_tx(kv_full(s), L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_4d(sbase + L::kKVOff + s * L::kTileBytes + c * kChunkBytes,
+                          which == 0 ? &tm_k : &tm_v, kv_full(s), c * 64, w.hkv, k_row, k_b,
+                          pol_kv);
+            issued = idx + 1;
+            if (KVC) *kv_issued = issued;
+          };
+          if constexpr (KVC) {
+            // K runs one tile ahead of V: K0, K1, V0, K2, V1, ..., K(n-1), V(n-2),
+            // V(n-1), so a K slot is refilled as soon as its S = Q K^T is done
+            auto page_of = [&](int j) {
+              int pg = w.map_b;
+              if (p.block_table) {
+                pg = __ldg(p.block_table + (int64_t)w.b * p.max_blocks +
+                           ((w.kv_ub + j) * kBlockN) / p.page_rows);
+                if (pg < 0 || pg >= p.num_pages) {
+                  record_status(p.status, 5);
+                  pg = 0;
+                }
               }
-              const CUtensorMap *tm = which == 0 ? &tm_k : &tm_v;
-              FA_TRACE_AT(idx < 256, 1536 + idx);
-              mbar_arrive_expect_tx(kv_full(s), L::kTileBytes);
-              for (int c = 0; c < L::kChunks; ++c)
-                tma_load_4d(sbase + L::kKVOff + s * L::kTileBytes + c * kChunkBytes, tm,
-                            kv_full(s), c * 64, w.hkv, k_row, k_b, pol_kv);
-              issued = idx + 1;
+              return pg;
+            };
+            int pg_cur = w.n_max > 0 ? page_of(0) : 0;
+            if (w.n_max > 0 && ok) issue(0, 0, pg_cur);
+            for (int j = 0; j < w.n_max && ok; ++j) {
+              int pg_next = pg_cur;
+              if (j + 1 < w.n_max) {
+                pg_next = page_of(j + 1);
+                issue(0, j + 1, pg_next);
+              }
+              if (ok) issue(1, j, pg_cur);
+              pg_cur = pg_next;
+            }
+          } else {
+            for (int j = 0; j < w.n_max && ok; ++j) {
+              issue(0, j, 0);
+              if (ok) issue(1, j, 0);
             }
           }
         }
@@ -611,7 +639,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = make_idesc_f16(BF16, kBlockM, kBlockN, false);
       constexpr uint32_t idesc_pv = make_idesc_f16(BF16, kBlockM, D, true);
       // descriptors built once; each MMA adds a compile-time offset
-      const uint64_t q_desc = make_sdesc_sw128(sbase + L::kQOff + T * L::kTileBytes, 16, 1024);
+      const uint64_t q_desc =
+          make_sdesc_sw128(sbase + L::kQOff + (KVC ? 0 : T) * L::kTileBytes, 16, 1024);
       const uint64_t kv_desc0 = make_sdesc_sw128(sbase + L::kKVOff, 16, 1024);
       const uint64_t v_desc0 = make_sdesc_sw128(sbase + L::kKVOff, kChunkBytes, 1024);
       const uint32_t d_s = tmem + T * 128, d_o = tmem + 256 + T * D;
@@ -638,6 +667,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts_acc(d_o, a + kk * 8, vd + ((kk * 2048) >> 4), idesc_pv);
       };
       auto kv_par = [&](int idx) { return (uint32_t)((idx / L::kStages) & 1); };
+      // bounded spin until the producer has issued ring load idx (KV cache)
+      auto issued_past = [&](int idx) {
+        if (*kv_issued > idx) return true;
+        const long long t0 = clock64();
+        while (*kv_issued <= idx) {
+          if (*abort_flag) return false;
+          if (clock64() - t0 > limit) {
+            record_status(p.status, 4);
+            *abort_flag = 1;
+            return false;
+          }
+        }
+        return true;
+      };
       // bounded spin for this issuer's turn (the other one is issuing)
       auto take_turn = [&]() {
         if (*mma_turn == T) return true;
@@ -669,7 +712,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (unit >= p.total_units) break;
         const Work w = (KVC ? decode_work_kvc(p, unit, lane) : decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane));
         if (!w.valid || w.n_max == 0) continue;
-        if (lane == 0) {
+        if (lane == 0 && KVC) {
+          // KV-cache units: each tile owns every other load and the tensor
+          // pipe is far from busy, so the issuers run free (no turns), and
+          // O += P V of a tile's previous load is issued and its V slot
+          // released before waiting for the next K: the producer refills the
+          // ring without waiting for a K load to land first
+          const int n = w.n_kv[T], nm = w.n_max;
+          const int off = w.kv_begin[T] - w.kv_ub;
+          // ring positions of the unit's loads (the producer's K-ahead order)
+          auto kpos = [&](int u) { return u == 0 ? 0 : 2 * u - 1; };
+          auto vpos = [&](int u) { return u + 1 < nm ? 2 * u + 2 : 2 * nm - 1; };
+          if (nm > 0 && n == 0) {
+            // reads no Q this unit: release it, but only once it has landed,
+            // so the arrival cannot count towards the previous unit's phase
+            ok = wait(q_full(0), q_used & 1);
+            if (ok) mbar_arrive(q_empty(0));
+          }
+          for (int jq = 0; jq <= n && ok; ++jq) {
+            const int u = off + 2 * jq;
+            const int kidx = used + kpos(u), vidx = used + vpos(u - 2);
+            if (jq >= 1) {
+              ok = issued_past(vidx) && wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
+                   (jq > 1 || o_done == 0 || wait(o_free(T), (o_done - 1) & 1)) &&
+                   wait(p_half(T, 0), p_seen & 1);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv_half(vidx, 0, jq == 1);
+              if (!wait(p_half(T, 1), p_seen & 1)) {
+                ok = false;
+                break;
+              }
+              ++p_seen;
+              tc_fence_after();
+              issue_pv_half(vidx, 1, false);
+              if (jq == n) {
+                tc_commit(o_ready(T));
+                ++o_done;
+              }
+              release(vidx, false);
+            }
+            if (jq < n) {
+              if (jq == 0) ok = wait(q_full(0), q_used & 1);
+              ok = ok && issued_past(kidx) && wait(kv_full(kidx % L::kStages), kv_par(kidx));
+              if (!ok) break;
+              tc_fence_after();
+              issue_qk(kidx);
+              tc_commit(s_full(T));
+              if (jq == n - 1) tc_commit(q_empty(0));
+              release(kidx, false);
+            }
+          }
+          if (nm > 0) ++q_used;  // one Q load per unit with keys
+          used += 2 * w.n_max;
+        } else if (lane == 0) {
           const int n = w.n_kv[T], n_other = w.n_kv[1 - T];
           // bracket u = 0 .. n_max of the unit: O_T += P_T V(u-1) if this
           // tile read load u-1, then S_T = Q_T K(u)^T if it reads load u.
@@ -898,12 +994,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < D; ++k) orr[k] = 0u;
       if constexpr (KVC) {
         // both tiles hold the same rows over even / odd K/V tiles: tile 1
-        // hands its row max and sum to tile 0 through shared memory (tile 1's
-        // unused output staging buffer, double-buffered by unit), tile 0 reads
+        // hands its row max and sum to tile 0 through shared memory
+        // (double-buffered by unit), tile 0 reads
         // both accumulators out of tensor memory and merges them:
         //   M = max(m0, m1), O = O0 2^(m0 - M) + O1 2^(m1 - M), l likewise
-        float *xm = reinterpret_cast<float *>(smem + L::kStageOff + kChunkBytes) +
-                    (x_units & 1) * 256;
+        float *xm = reinterpret_cast<float *>(smem + L::kStageOff) + (x_units & 1) * 256;
         float *xl = xm + 128;
         ++x_units;
         if (n_kv > 0 && ok) {
@@ -980,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   : -INFINITY;
       // a packed tile cut by its sequence end would spill into the next
       // sequence through the tensor map, so it is stored row by row instead
-      const bool use_tma = !VARLEN || (m0 + kBlockM <= lq);
+      const bool use_tma = !KVC && (!VARLEN || (m0 + kBlockM <= lq));
       if (EXT && p.num_splits > 1) {
         // split-KV partial: normalised fp32 O_s and LSE_s of this split
         if (row_valid && ok) {

@@ -23,11 +23,11 @@ cudaError_t launch_fwd(const LaunchArgs &a) {
   const unsigned long long bit = 1ull << (a.device & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Smem<D>::kAlloc);
+                                         (int)Smem<D, KVC>::kAlloc);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  kern<<<a.grid, kThreads, Smem<D>::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
+  kern<<<a.grid, kThreads, Smem<D, KVC>::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
   return cudaGetLastError();
 }
 

@@ -266,3 +266,112 @@ def algorithmic_bytes(case: Case) -> int:
     el = 2
     return (case.q.numel() + case.k.numel() + case.v.numel() + case.q.numel()) * el \
         + case.lse_rows() * 4
+
+
+# ----------------------------------------------------------------- KV caches
+
+@dataclass(frozen=True)
+class CacheWorkload:
+    """Decoding over a KV cache: Sq new tokens per sequence against a cache of
+    cache_seqlens[b] keys, drawn uniformly in [min_len, capacity] (all equal to
+    capacity when min_len is 0); paged with page_rows rows per page (pages in a
+    random order) or contiguous (page_rows 0)."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    D: int
+    dtype: str
+    causal: bool
+    capacity: int
+    page_rows: int = 0
+    min_len: int = 0
+    seed: int = 0
+    splits: int = 0        # split-KV chunks: 0 = chosen by the library
+
+
+@dataclass
+class KVCase:
+    """Drawn decoding problem: q [B, Sq, Hq, D]; cache [pages, page_rows, Hkv, D]
+    (contiguous: pages = B, page_rows = capacity); int32 seqlens / block table (CPU)."""
+    q: torch.Tensor
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    cache_seqlens: torch.Tensor
+    block_table: Optional[torch.Tensor]
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    D: int
+    scale: float
+    causal: bool
+    dtype: str
+    page_rows: int
+    num_pages: int
+    max_blocks: int
+    meta: dict = field(default_factory=dict)
+
+    def lse_rows(self) -> int:
+        return self.B * self.Hq * self.Sq
+
+
+CACHE_WORKLOADS = [
+    CacheWorkload("decode_b64_hq32_hkv8_sq1_d128_bf16_paged256_len2k4k", 64, 32, 8, 1, 128,
+                  "bf16", True, capacity=4096, page_rows=256, min_len=2048, seed=1300),
+    CacheWorkload("decode_b8_hq64_hkv8_sq1_d128_bf16_len16k", 8, 64, 8, 1, 128, "bf16", True,
+                  capacity=16384, seed=1301),
+    CacheWorkload("decode_b32_hq32_hkv8_sq4_d128_bf16_paged256_len4k", 32, 32, 8, 4, 128,
+                  "bf16", True, capacity=4096, page_rows=256, seed=1302),
+]
+CACHE_BY_NAME = {w.name: w for w in CACHE_WORKLOADS}
+
+
+def make_cache_workload(w: CacheWorkload, seed=None) -> KVCase:
+    """Draw the lengths, then q, then the cache pages, then the page order."""
+    g = torch.Generator().manual_seed(int(w.seed if seed is None else seed))
+    if w.min_len:
+        lens = torch.randint(w.min_len, w.capacity + 1, (w.B,), generator=g)
+    else:
+        lens = torch.full((w.B,), w.capacity, dtype=torch.int64)
+    q = _draw((w.B, w.Sq, w.Hq, w.D), 1.0, w.dtype, g)
+    if w.page_rows:
+        max_blocks = (w.capacity + w.page_rows - 1) // w.page_rows
+        pages = w.B * max_blocks
+        shape = (pages, w.page_rows, w.Hkv, w.D)
+    else:
+        max_blocks, pages = 1, w.B
+        shape = (w.B, w.capacity, w.Hkv, w.D)
+    kc = _draw(shape, 1.0, w.dtype, g)
+    vc = _draw(shape, 1.0, w.dtype, g)
+    table = None
+    if w.page_rows:
+        table = torch.randperm(pages, generator=g).reshape(w.B, max_blocks).to(torch.int32)
+    case = KVCase(q, kc, vc, lens.to(torch.int32), table, w.B, w.Hq, w.Hkv, w.Sq, w.D,
+                  1.0 / math.sqrt(w.D), w.causal, w.dtype, w.page_rows or w.capacity, pages,
+                  max_blocks)
+    case.meta["workload"] = w.name
+    return case
+
+
+def kv_visible_per_row(c: KVCase):
+    """Visible keys of every row in [B, Hq, Sq] order (bottom-right causal)."""
+    out = []
+    for lk in c.cache_seqlens.tolist():
+        i = torch.arange(c.Sq, dtype=torch.int64)
+        n = (i + lk - c.Sq + 1).clamp(min=0, max=lk) if c.causal else torch.full_like(i, lk)
+        out.append(n.repeat(c.Hq))
+    return torch.cat(out)
+
+
+def kv_flops(c: KVCase) -> int:
+    """4 * D * (visible (query row, key) pairs over all query heads)."""
+    return 4 * c.D * int(kv_visible_per_row(c).sum())
+
+
+def kv_algorithmic_bytes(c: KVCase) -> int:
+    """q and o (16-bit), LSE (fp32), and every cache row some query token of its
+    sequence sees, K and V, once per K/V head."""
+    rows = sum(c.cache_seqlens.tolist())  # the newest token sees every key, causal or not
+    return 2 * 2 * c.q.numel() + 4 * c.lse_rows() + 2 * 2 * rows * c.Hkv * c.D

@@ -210,6 +210,16 @@ int fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache, void
                    const float *alibi_slopes, int num_splits);
 
 /*
+ * fa_kvcache_plan — the split count fa_fwd_kvcache would use for these sizes
+ * (capacity = cache keys a sequence can hold: page_rows without a block
+ * table, max_blocks * page_rows with one) and its scratch bytes (written to
+ * *scratch_bytes if non-NULL).  Returns the split count (>= 1) or minus a
+ * status code.
+ */
+int fa_kvcache_plan(int B, int Hq, int Hkv, int Sq, int D, long long capacity,
+                    int num_splits, long long *scratch_bytes);
+
+/*
  * fa_fwd_split_noalloc — fa_fwd_split that allocates nothing.  It has no
  * counterpart in the pages: it exists for callers that must not allocate
  * device memory per call.  Arguments, results and status codes are those of

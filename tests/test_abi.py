@@ -113,6 +113,13 @@ def test_kvcache_arguments_rejected_without_launch(lib, bad):
     assert _kvc(**bad) == fa.FA_ERR_INVALID_ARG
 
 
+def test_kvcache_plan_forced_counts_and_scratch(lib):
+    assert fa.fa_kvcache_plan(8, 32, 8, 1, 128, 4096, 5) == (5, 5 * 8 * 32 * 1 * 129 * 4)
+    assert fa.fa_kvcache_plan(8, 32, 8, 1, 128, 4096, 1) == (1, 0)
+    assert fa.fa_kvcache_plan(8, 12, 4, 1, 128, 4096, 1)[0] == -fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_kvcache_plan(8, 32, 8, 1, 128, 0, 1)[0] == -fa.FA_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("Hq,Hkv,D", [(6, 2, 64), (4, 2, 96), (256, 1, 64)])
 def test_kvcache_unsupported(lib, Hq, Hkv, D):
     assert _kvc(Hq=Hq, Hkv=Hkv, D=D) == fa.FA_ERR_UNSUPPORTED

@@ -132,6 +132,14 @@ def test_splits(num_splits):
     check_kvcache(c, o, lse, False, scale, f"splits {num_splits}")
 
 
+def test_auto_split_plan_fills_the_gpu():
+    n, nbytes = fa.fa_kvcache_plan(8, 64, 8, 1, 128, 16384, 0)
+    assert n > 1 and nbytes == n * 8 * 64 * 129 * 4
+    c = make_cache_case(2, 16, 2, 1, 128, "bf16", [7000, 3000], capacity=8192, seed=58)
+    o, lse = run_kvcache(c, True, 0.1, num_splits=0)
+    check_kvcache(c, o, lse, True, 0.1, "auto splits")
+
+
 def test_empty_and_tiny_caches():
     c = make_cache_case(4, 4, 2, 1, 64, "bf16", [0, 1, 2, 127], capacity=200, seed=53)
     o, lse = run_kvcache(c, True, 0.125)
@@ -175,6 +183,27 @@ def test_bad_cache_seqlens_and_table_reported():
     # the context is still usable
     o2, lse2 = run_kvcache(c, False, 0.125)
     check_kvcache(c, o2, lse2, False, 0.125, "after bad inputs")
+
+
+@pytest.mark.parametrize("num_splits", [1, 2])
+def test_many_units_per_cta(num_splits):
+    """512+ units over the persistent grid: each CTA walks several long units
+    whose two tiles share ring slots and run their MMA issue independently."""
+    B, Hq, Hkv, D = 64, 32, 8, 128
+    g = torch.Generator().manual_seed(59)
+    lens = torch.randint(600, 1400, (B,), generator=g).tolist()
+    c = make_cache_case(B, Hq, Hkv, 1, D, "bf16", lens, page_rows=256, seed=60)
+    scale = 1 / math.sqrt(D)
+    o, lse = run_kvcache(c, True, scale, num_splits=num_splits)
+    o2, lse2 = run_kvcache(c, True, scale, num_splits=num_splits)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    # compare a spread of sequences against the oracle
+    pick = [0, 1, 17, 33, 62, 63]
+    sub = dict(c)
+    sub["q"] = c["q"][pick]
+    sub["lens"] = c["lens"][pick]
+    sub["table"] = c["table"][pick]
+    check_kvcache(sub, o[pick], lse[pick], True, scale, f"many units splits {num_splits}")
 
 
 def test_deterministic():
