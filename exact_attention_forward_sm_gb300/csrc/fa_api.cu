@@ -175,10 +175,11 @@ int choose_splits(int64_t units, int64_t kv_tiles, int sms) {
 }
 
 // Split count chosen for num_splits = 0 (sizes already validated).
-int auto_splits(int B, int Hq, int Hkv, int Sq, int Sk, bool varlen, int sms) {
-  const bool pair_heads = ((Hq / Hkv) % 2) == 0;
+int auto_splits(int B, int Hq, int Hkv, int Sq, int Sk, int D, bool varlen, int sms) {
+  // head dim 256: one 128-row query tile per unit
+  const bool pair_heads = D != 256 && ((Hq / Hkv) % 2) == 0;
   const int head_units = pair_heads ? Hq / 2 : Hq;
-  const int rows_per_unit = pair_heads ? fa::kBlockM : 2 * fa::kBlockM;
+  const int rows_per_unit = (pair_heads || D == 256) ? fa::kBlockM : 2 * fa::kBlockM;
   const int64_t row_units = (Sq + rows_per_unit - 1) / rows_per_unit;
   // K/V tiles of a sequence: dense Sk, packed the mean length
   const int64_t per_seq = varlen ? (Sk + B - 1) / B : Sk;
@@ -260,7 +261,7 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   if (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)) return FA_ERR_INVALID_ARG;
   const bool varlen = cu_seqlens_q != nullptr;
   if (varlen != (cu_seqlens_k != nullptr)) return FA_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0) return FA_OK;  // no query rows
   if (!q || !o) return FA_ERR_INVALID_ARG;
   if (Sk > 0 && (!k || !v)) return FA_ERR_INVALID_ARG;  // k / v unused when there are no keys
@@ -279,9 +280,12 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   if (causal) win_r = 0;
 
   const int group = Hq / Hkv;
-  const bool pair_heads = (group % 2) == 0;
+  // head dim 256: one 128-row query tile per unit (tensor memory holds one
+  // 256-column O accumulator next to its scores)
+  const bool wide = D == 256;
+  const bool pair_heads = !wide && (group % 2) == 0;
   const int head_units = pair_heads ? Hq / 2 : Hq;
-  const int rows_per_unit = pair_heads ? fa::kBlockM : 2 * fa::kBlockM;
+  const int rows_per_unit = (pair_heads || wide) ? fa::kBlockM : 2 * fa::kBlockM;
   const int64_t row_units = (Sq + rows_per_unit - 1) / rows_per_unit;
   // packed problems: each sequence rounds its row count up once, so this
   // bounds the number of units; the kernel skips the ones past the last
@@ -295,7 +299,7 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   const int sms = sm_count(device);
   if (!status || sms <= 0) return FA_ERR_CUDA;
 
-  const int splits = num_splits ? num_splits : auto_splits(B, Hq, Hkv, Sq, Sk, varlen, sms);
+  const int splits = num_splits ? num_splits : auto_splits(B, Hq, Hkv, Sq, Sk, D, varlen, sms);
   // the instances with score variants also carry the split-KV path
   const bool ext =
       win_l >= 0 || win_r > 0 || softcap > 0.f || alibi_slopes != nullptr || splits > 1;
@@ -363,6 +367,12 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   a.device = device;
 
   auto launch = [&](const fa::LaunchArgs &la) {
+    if (wide) {
+      if (ext)
+        return bf16 ? fa::launch_ext_d256_bf16(la, varlen) : fa::launch_ext_d256_fp16(la, varlen);
+      return bf16 ? fa::launch_d256_bf16(la, plain_causal, varlen)
+                  : fa::launch_d256_fp16(la, plain_causal, varlen);
+    }
     if (ext) {
       if (D == 64)
         return bf16 ? fa::launch_ext_d64_bf16(la, varlen) : fa::launch_ext_d64_fp16(la, varlen);
@@ -574,7 +584,7 @@ int fa_split_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int varlen, int
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || Hq % Hkv != 0) return -FA_ERR_INVALID_ARG;
   if (varlen != 0 && varlen != 1) return -FA_ERR_INVALID_ARG;
   if (num_splits < 0 || num_splits > kMaxSplits) return -FA_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return -FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return -FA_ERR_UNSUPPORTED;
   int splits = num_splits;
   if (B == 0 || Sq == 0) {
     splits = 1;
@@ -583,7 +593,7 @@ int fa_split_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int varlen, int
     if (cudaGetDevice(&device) != cudaSuccess) return -FA_ERR_CUDA;
     const int sms = sm_count(device);
     if (sms <= 0) return -FA_ERR_CUDA;
-    splits = auto_splits(B, Hq, Hkv, Sq, Sk, varlen != 0, sms);
+    splits = auto_splits(B, Hq, Hkv, Sq, Sk, D, varlen != 0, sms);
   }
   if (scratch_bytes) {
     const long long rows = (long long)Hq * Sq * (varlen ? 1 : B);

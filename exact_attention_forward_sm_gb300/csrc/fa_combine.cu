@@ -24,7 +24,7 @@ namespace {
 
 template <int N, bool BF16>
 __device__ __forceinline__ void store_row(void *dst, const float (&x)[N]) {
-  static_assert(N == 2 || N == 4, "values per lane");
+  static_assert(N == 2 || N == 4 || N == 8, "values per lane");
   uint32_t w[N / 2];
 #pragma unroll
   for (int k = 0; k < N / 2; ++k) {
@@ -36,7 +36,9 @@ __device__ __forceinline__ void store_row(void *dst, const float (&x)[N]) {
       w[k] = *reinterpret_cast<uint32_t *>(&h);
     }
   }
-  if constexpr (N == 4)
+  if constexpr (N == 8)
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  else if constexpr (N == 4)
     *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
   else
     *reinterpret_cast<uint32_t *>(dst) = w[0];
@@ -79,7 +81,18 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const CombineParams p) 
         const float w = ex2((p.lse_part[s * p.rows + r] - m) * 1.4426950408889634f);
         wsum += w;
         const float *src = p.o_part + (s * p.rows + r) * D + lane * N;
-        if constexpr (N == 4) {
+        if constexpr (N == 8) {
+          const float4 x = *reinterpret_cast<const float4 *>(src);
+          const float4 y = *reinterpret_cast<const float4 *>(src + 4);
+          acc[0] = fmaf(w, x.x, acc[0]);
+          acc[1] = fmaf(w, x.y, acc[1]);
+          acc[2] = fmaf(w, x.z, acc[2]);
+          acc[3] = fmaf(w, x.w, acc[3]);
+          acc[4] = fmaf(w, y.x, acc[4]);
+          acc[5] = fmaf(w, y.y, acc[5]);
+          acc[6] = fmaf(w, y.z, acc[6]);
+          acc[7] = fmaf(w, y.w, acc[7]);
+        } else if constexpr (N == 4) {
           const float4 x = *reinterpret_cast<const float4 *>(src);
           acc[0] = fmaf(w, x.x, acc[0]);
           acc[1] = fmaf(w, x.y, acc[1]);
@@ -115,6 +128,11 @@ cudaError_t launch_combine(const CombineParams &p, int D, bool bf16, int sms,
       fa_combine_kernel<64, true><<<grid, block, 0, stream>>>(p);
     else
       fa_combine_kernel<64, false><<<grid, block, 0, stream>>>(p);
+  } else if (D == 256) {
+    if (bf16)
+      fa_combine_kernel<256, true><<<grid, block, 0, stream>>>(p);
+    else
+      fa_combine_kernel<256, false><<<grid, block, 0, stream>>>(p);
   } else {
     if (bf16)
       fa_combine_kernel<128, true><<<grid, block, 0, stream>>>(p);

@@ -302,7 +302,8 @@ __device__ inline Work decode_work_kvc(const FwdParams &p, int unit, int lane) {
   return w;
 }
 
-template <bool CAUSAL, bool VARLEN, bool EXT>
+// WIDE (head dim 256): one 128-row query tile per unit; tile 1 is left empty.
+template <bool CAUSAL, bool VARLEN, bool EXT, bool WIDE = false>
 __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
   Work w;
   w.valid = 0;
@@ -372,7 +373,11 @@ __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
   }
   if (CAUSAL || (EXT && p.reverse_rows)) ru = n_ru - 1 - ru;  // heavier (later) rows first
   w.b = b;
-  if (p.pair_heads) {
+  if (WIDE) {
+    w.head[0] = w.head[1] = hu;
+    w.m0[0] = ru * kBlockM;
+    w.m0[1] = w.lq;  // no rows
+  } else if (p.pair_heads) {
     w.head[0] = 2 * hu;
     w.head[1] = 2 * hu + 1;
     w.m0[0] = w.m0[1] = ru * kBlockM;

@@ -63,6 +63,11 @@ cudaError_t launch_ext_d64_fp16(const LaunchArgs &a, bool varlen);
 cudaError_t launch_ext_d64_bf16(const LaunchArgs &a, bool varlen);
 cudaError_t launch_ext_d128_fp16(const LaunchArgs &a, bool varlen);
 cudaError_t launch_ext_d128_bf16(const LaunchArgs &a, bool varlen);
+// Head dim 256 (one query tile per unit, see fa_fwd_wide.cuh).
+cudaError_t launch_d256_fp16(const LaunchArgs &a, bool causal, bool varlen);
+cudaError_t launch_d256_bf16(const LaunchArgs &a, bool causal, bool varlen);
+cudaError_t launch_ext_d256_fp16(const LaunchArgs &a, bool varlen);
+cudaError_t launch_ext_d256_bf16(const LaunchArgs &a, bool varlen);
 cudaError_t launch_kvc_d64_fp16(const LaunchArgs &a);
 cudaError_t launch_kvc_d64_bf16(const LaunchArgs &a);
 cudaError_t launch_kvc_d128_fp16(const LaunchArgs &a);

@@ -95,7 +95,14 @@ SPLIT_WORKLOADS = [
     Workload("b8_h8_sq1_sk8192_d128_bf16_decode", 8, 8, 8, 1, 128, "bf16", True,
              seed=1201, Sk=8192, splits=0),
 ]
-BY_NAME = {w.name: w for w in WORKLOADS + VARIANT_WORKLOADS + SPLIT_WORKLOADS}
+# Head dim 256 (the fork's v1.7 notes validate D = 256 in section 4.3).  Seeds
+# 1400 + index.
+D256_WORKLOADS = [
+    Workload("b2_h16_s4096_d256_bf16_causal", 2, 16, 16, 4096, 256, "bf16", True, seed=1400),
+    Workload("b1_h8_s16384_d256_bf16_noncausal", 1, 8, 8, 16384, 256, "bf16", False,
+             seed=1401),
+]
+BY_NAME = {w.name: w for w in WORKLOADS + VARIANT_WORKLOADS + SPLIT_WORKLOADS + D256_WORKLOADS}
 
 
 @dataclass

@@ -80,7 +80,7 @@ enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 };
  *   Hq, Hkv     query / key-value heads; Hq % Hkv == 0 (grouped-query
  *               attention: query head h reads K/V head h / (Hq / Hkv)).
  *   Sq, Sk      sequence lengths (dense) or packed totals (packed), >= 0.
- *   D           head dimension: 64 or 128.
+ *   D           head dimension: 64, 128 or 256.
  *   scale       score scale (commonly 1 / sqrt(D)); finite and > 0.
  *   causal      0 or 1.  With causal = 1 key j is visible to query i iff
  *               j <= i + (Lk - Lq) (diagonal aligned to the bottom-right; for

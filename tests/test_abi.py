@@ -130,7 +130,7 @@ def test_variant_empty_problems_are_noops(lib):
     assert _call_ex(Sq=0, alibi_slopes=16) == fa.FA_OK
 
 
-@pytest.mark.parametrize("D", [32, 96, 256])
+@pytest.mark.parametrize("D", [32, 96, 192, 512])
 def test_unbuilt_head_dims_unsupported(lib, D):
     assert _call(D=D) == fa.FA_ERR_UNSUPPORTED
 

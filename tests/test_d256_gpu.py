@@ -1,0 +1,102 @@
+"""GPU parity of head dim 256 (one 128-row query tile per work unit, both
+softmax warpgroups splitting each row's scores).  The fork's v1.7 notes
+validate D = 256 in their 10-shape sweep (section 4.3); the method is the same
+as for D <= 128, so the gates are the same: O rel_Linf <= 2e-2 (fp16) / 1e-2
+(bf16), cosine >= 0.9995, LSE abs <= 1e-3."""
+import zlib
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines too
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import exact_attention_forward_sm_gb300 as fa  # noqa: E402
+from exact_attention_forward_sm_gb300 import workloads as wl  # noqa: E402
+from tests.gpu_util import check, run_gpu, sample_rows  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from exact_attention_forward_sm_gb300 import _build
+    _build.build()
+    fa.load_library()
+
+
+def _seed(*key):
+    return zlib.crc32(repr(key).encode()) % 100000
+
+
+SHAPES = [
+    # B, Hq, Hkv, Sq, Sk, dtype, causal
+    (1, 1, 1, 128, 128, "bf16", False),
+    (1, 2, 2, 300, 300, "fp16", True),
+    (2, 4, 4, 257, 257, "bf16", True),
+    (1, 8, 2, 513, 513, "bf16", True),     # GQA 4:1
+    (2, 3, 1, 200, 200, "fp16", False),    # odd group
+    (1, 2, 2, 100, 600, "bf16", True),     # Sq < Sk
+    (1, 2, 2, 600, 100, "fp16", True),     # Sq > Sk: rows without keys
+    (1, 2, 2, 1, 1, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "b{}_hq{}_hkv{}_sq{}_sk{}_{}_{}".format(
+    *s[:6], "causal" if s[6] else "full"))
+def test_d256_all_rows(shape):
+    B, Hq, Hkv, Sq, Sk, dtype, causal = shape
+    case = wl.make_case(B, Hq, Hkv, Sq, Sk, 256, dtype, causal, seed=_seed(shape))
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag=f"d256 {shape}")
+
+
+def test_d256_rising_bias_rescales():
+    case = wl.make_case(1, 2, 2, 1024, 1024, 256, "bf16", True, seed=71, rising_bias=True)
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag="d256 rising bias")
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_d256_packed(dtype):
+    case = wl.make_case(0, 4, 2, 0, 0, 256, dtype, True, seed=_seed("packed", dtype),
+                        seqlens_q=[1, 130, 300, 0, 257], seqlens_k=[5, 130, 300, 9, 400])
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag=f"d256 packed {dtype}")
+
+
+def test_d256_variants_and_splits():
+    Hq = 4
+    case = wl.make_case(1, Hq, 2, 300, 900, 256, "bf16", True, seed=72, sigma=2.0,
+                        window=(400, 0), softcap=25.0,
+                        alibi_slopes=wl.alibi_slopes_geometric(Hq))
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag="d256 variants")
+    o2, lse2 = run_gpu(case, num_splits=3)
+    check(case, o2, lse2, tag="d256 variants split3")
+
+
+def test_d256_split_plain():
+    case = wl.make_case(1, 2, 2, 128, 2000, 256, "fp16", False, seed=73)
+    o, lse = run_gpu(case, num_splits=5)
+    check(case, o, lse, tag="d256 split5")
+
+
+def test_d256_window_00_gives_v():
+    case = wl.make_case(1, 2, 2, 300, 300, 256, "bf16", False, seed=74, window=(0, 0))
+    o, _ = run_gpu(case)
+    assert torch.equal(o.cpu(), case.v)
+
+
+def test_d256_deterministic():
+    case = wl.make_case(2, 4, 4, 700, 700, 256, "bf16", True, seed=75)
+    a = run_gpu(case)
+    b = run_gpu(case)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_d256_full_size_sampled_rows():
+    """b2 h16 s4096 d256 bf16 causal in the benchmark's launch configuration."""
+    case = wl.make_workload(wl.BY_NAME["b2_h16_s4096_d256_bf16_causal"])
+    o, lse = run_gpu(case)
+    check(case, o, lse, rows=sample_rows(case, per_head=64, seed=9), tag="d256 full size")
