@@ -41,7 +41,7 @@ typedef struct CUstream_st *fa_stream_t;
 enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,  /* a size, pointer, flag or alignment is invalid; nothing launched */
-  FA_ERR_UNSUPPORTED = 2,  /* valid but not built (e.g. head dim other than 64 / 128)      */
+  FA_ERR_UNSUPPORTED = 2,  /* valid but not built (e.g. head dim other than 64, 128, 256)  */
   FA_ERR_CUDA = 3,         /* a CUDA runtime / driver call failed (no device, launch error) */
   FA_ERR_TIMEOUT = 4,      /* device: a pipeline wait exceeded its limit; outputs invalid    */
   FA_ERR_BAD_SEQLENS = 5,  /* device: cu_seqlens not monotone or beyond Sq / Sk; rows skipped */
