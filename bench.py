@@ -40,7 +40,13 @@ UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = wl.WORKLOADS[1].name   # hdim-128 bf16 causal, B4 H16 S2048
 L2_FLUSH_BYTES = 256 << 20
 PEAK_FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-KERNEL_SOURCES = ["fa_fwd_kernel.cuh", "fa_ptx.cuh", "fa_launch.cuh"]
+# sources each attention kernel is compiled from (a profile summary is only
+# used while their hash matches the one recorded in it)
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ["fa_fwd_kernel.cuh", "fa_ptx.cuh", "fa_launch.cuh"],
+    "fa_fwd_wide_kernel": ["fa_fwd_wide.cuh", "fa_fwd_kernel.cuh", "fa_ptx.cuh",
+                           "fa_launch.cuh"],
+}
 
 
 # --------------------------------------------------------------- host helpers
@@ -75,18 +81,18 @@ def load_peaks():
     return dict(PEAK_FALLBACK), "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(kernel="fa_fwd_kernel"):
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "exact_attention_forward_sm_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
+def profiled_traffic(workload, kernel="fa_fwd_kernel"):
     """DRAM bytes per launch from the committed ncu summary of this workload,
     if it was taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"fa_fwd_kernel_{workload}.txt")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     if not os.path.exists(path):
         return None
     fields = {}
@@ -95,7 +101,7 @@ def profiled_traffic(workload):
             if ":" in line:
                 k, v = line.split(":", 1)
                 fields[k.strip()] = v.strip()
-    if fields.get("kernel_source_sha256_16") != kernel_source_hash():
+    if fields.get("kernel_source_sha256_16") != kernel_source_hash(kernel):
         return None
     try:
         return int(float(fields["dram_bytes_per_launch"]))
@@ -257,12 +263,13 @@ class Problem:
     e2e leg), outputs, a launch closure and the work it does per step."""
 
     def __init__(self, name, dtype, flops, alg_bytes, host_inputs, dev_inputs, outputs, launch,
-                 launches_per_step, config, oracle_sample):
+                 launches_per_step, config, oracle_sample, kernel="fa_fwd_kernel"):
         self.name, self.dtype = name, dtype
         self.flops, self.alg_bytes = flops, alg_bytes
         self.host_inputs, self.dev_inputs, self.outputs = host_inputs, dev_inputs, outputs
         self.launch, self.launches_per_step = launch, launches_per_step
         self.config, self.oracle_sample = config, oracle_sample
+        self.kernel = kernel  # the attention kernel the roofline describes
 
 
 def attention_problem(args, fa, rank, dev, stream):
@@ -315,7 +322,8 @@ def attention_problem(args, fa, rank, dev, stream):
               **({"num_splits": splits, "num_splits_used": used} if splits >= 0 else {})}
     return Problem(w.name, case.dtype, wl.attention_flops(case), wl.algorithmic_bytes(case),
                    [case.q, case.k, case.v], [q, k, v], [o, lse], launch, launches_per_step,
-                   config, lambda secs: oracle_sample(case, secs, seed=12345))
+                   config, lambda secs: oracle_sample(case, secs, seed=12345),
+                   kernel="fa_fwd_wide_kernel" if case.D == 256 else "fa_fwd_kernel")
 
 
 def kvcache_problem(args, fa, rank, dev, stream):
@@ -462,10 +470,10 @@ def run_gpu_arm(args, rank, local_rank, world):
         },
         "roofline": {
             **roof,
-            "traffic": profiled_traffic(prob.name),
+            "traffic": profiled_traffic(prob.name, prob.kernel),
             "peak_source": (f"{peak_src} hbm_gbs (copy bandwidth)" if hbm_bound
                             else f"{peak_src} {dense_key} (burst, cuBLAS bf16)"),
-            "kernel": "fa_fwd_kernel",
+            "kernel": prob.kernel,
             "kernel_ms_mean": round(kernel_ms, 5),
             "kernel_ms_min": round(min(times_ms), 5),
         },
