@@ -856,9 +856,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t s_addr = lane_base + t * 128;
     const uint32_t o_addr = lane_base + 256 + t * D;
-    // plain kernels keep raw scores and fold scale * log2(e) into the exps;
-    // kernels with score variants turn every score into log2 units first
-    const float scale_log2 = EXT ? 1.f : p.scale_log2;
+    // raw scores (plain kernels, and local windows alone) fold scale * log2(e)
+    // into the exps; a soft cap or ALiBi turns every score into log2 units
+    // first, and so does the KV-cache path, whose two-tile merge works in log2
+    // units
+    const bool raw_scores = !EXT || (!KVC && p.cap_k == 0.f && p.alibi == nullptr);
+    const float scale_log2 = raw_scores ? p.scale_log2 : 1.f;
     const float neg_thr = -p.threshold;
     // every lane of a warp must agree before the warp-wide tcgen05.ld / st
     auto warp_wait = [&](uint32_t bar, uint32_t parity) {
@@ -907,22 +910,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           // scores in log2 units: soft cap c tanh(scale s / c), written as
           // c (1 - 2 / (1 + e^(2 scale s / c))) with the hardware exp2 and
           // reciprocal, then the ALiBi penalty -slope |diag - key|
+          const int last_row = min(m0 + (KVC ? p.tok_per_tile : kBlockM), lq) - 1;
           if (p.cap_k != 0.f) {
             const float ck = p.cap_k, cl = p.cap_l2;
 #pragma unroll
             for (int c = 0; c < kBlockN; ++c)
               s[c] = fmaf(rcp_approx(1.f + ex2(s[c] * ck)), -2.f * cl, cl);
-          } else {
+          } else if (!raw_scores && !p.alibi) {
             const float sl2 = p.scale_log2;
 #pragma unroll
             for (int c = 0; c < kBlockN; ++c) s[c] *= sl2;
           }
           if (p.alibi) {
+            // after the soft cap the scores are in log2 units already
+            const float mul = p.cap_k != 0.f ? 1.f : p.scale_log2;
             const float d0 = (float)(diag - k0);
+            const int first_diag = m0 + lk - lq, last_diag = last_row + lk - lq;
+            if (k0 + kBlockN - 1 <= first_diag || k0 >= last_diag) {
+              // the whole tile lies on one side of every row's diagonal, where
+              // -slope |d0 - c| = sg (c - d0) is linear in the key: two packed
+              // FMAs per key pair
+              const float sg = k0 >= last_diag ? -slope_l2 : slope_l2;
+              const float base = -sg * d0;
 #pragma unroll
-            for (int c = 0; c < kBlockN; ++c) s[c] = fmaf(-slope_l2, fabsf(d0 - (float)c), s[c]);
+              for (int c = 0; c < kBlockN; c += 2) {
+                float b0, b1;
+                fma_f32x2(b0, b1, sg, sg, (float)c, (float)(c + 1), base, base);
+                fma_f32x2(s[c], s[c + 1], s[c], s[c + 1], mul, mul, b0, b1);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < kBlockN; ++c)
+                s[c] = fmaf(-slope_l2, fabsf(d0 - (float)c), s[c] * mul);
+            }
           }
-          const int last_row = min(m0 + (KVC ? p.tok_per_tile : kBlockM), lq) - 1;
           const bool need_mask = (k0 + kBlockN > lk) ||
                                  (p.win_r >= 0 && k0 + kBlockN - 1 > m0 + lk - lq + p.win_r) ||
                                  (p.win_l >= 0 && k0 < last_row + lk - lq - p.win_l);
