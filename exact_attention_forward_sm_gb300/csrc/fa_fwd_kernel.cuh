@@ -202,7 +202,6 @@ struct Work {
   int n_kv[2];       // K/V tiles each query tile visits ...
   int kv_begin[2];   // ... starting at this K/V tile of the sequence
   int kv_ub;         // first K/V tile loaded for the unit (min over its tiles)
-  int kv_stride;     // a tile reads every kv_stride-th loaded K/V tile (1, or 2 in KV-cache units)
   int n_max;         // K/V tiles loaded for the unit (the union of both ranges)
 };
 
@@ -291,7 +290,6 @@ __device__ inline Work decode_work_kvc(const FwdParams &p, int unit, int lane) {
   int n = window_kv_range(p, w.m0[0], w.lq, w.lk, &lo, p.tok_per_tile);
   if (p.num_splits > 1) split_range(p, w.split, lk, &lo, &n);
   // tile 0 reads K/V tiles lo, lo + 2, ...; tile 1 reads lo + 1, lo + 3, ...
-  w.kv_stride = 2;
   w.kv_ub = lo;
   w.n_max = n;
   w.kv_begin[0] = lo;
@@ -308,7 +306,6 @@ __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
   Work w;
   w.valid = 0;
   w.split = 0;
-  w.kv_stride = 1;
   if (EXT && p.num_splits > 1) {  // splits of one unit are adjacent: heavy units stay first
     w.split = unit % p.num_splits;
     unit /= p.num_splits;
@@ -770,28 +767,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (nm > 0) ++q_used;  // one Q load per unit with keys
           used += 2 * w.n_max;
-        } else if (lane == 0) {
+        } else if (!KVC && lane == 0) {
           const int n = w.n_kv[T], n_other = w.n_kv[1 - T];
           // bracket u = 0 .. n_max of the unit: O_T += P_T V(u-1) if this
           // tile read load u-1, then S_T = Q_T K(u)^T if it reads load u.
           // Both issuers walk every bracket, so the turns stay paired even
           // when the tiles' K/V ranges differ (local windows).
-          // (KV-cache units: the tiles take every other load, so a bracket
-          // holds work for one of them and the brackets run to n_max + 1)
-          const int st = KVC ? w.kv_stride : 1;
           const int off = w.kv_begin[T] - w.kv_ub;
           const int off_other = w.kv_begin[1 - T] - w.kv_ub;
-          auto reads = [&](int u, int o, int cnt) {
-            const int d = u - o;
-            return d >= 0 && (st == 1 || (d & 1) == 0) && d / st < cnt;
+          auto other_reads = [&](int u) {
+            const int d = u - off_other;
+            return d >= 0 && d < n_other;
           };
-          auto other_reads = [&](int u) { return reads(u, off_other, n_other); };
-          for (int u = 0; u <= w.n_max + st - 1 && ok; ++u) {
-            const int d = u - off;
-            const bool mine = d >= 0 && (st == 1 || (d & 1) == 0);
-            const int jq = d / st;  // this tile's step: S_T = Q_T K(jq)^T
-            const bool qk = mine && jq < n, pv = mine && jq >= 1 && jq <= n;
-            const int kidx = used + 2 * u, vidx = used + 2 * (u - st) + 1;
+          for (int u = 0; u <= w.n_max && ok; ++u) {
+            const int jq = u - off;  // this tile's step: S_T = Q_T K(jq)^T
+            const bool qk = jq >= 0 && jq < n, pv = jq >= 1 && jq <= n;
+            const int kidx = used + 2 * u, vidx = used + 2 * (u - 1) + 1;
             if (qk && jq == 0) {  // first S_T of the unit: Q_T must have landed
               ok = wait(q_full(T), q_used & 1);
               ++q_used;
@@ -829,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit(o_ready(T));  // tile T of this unit is complete
                 ++o_done;
               }
-              release(vidx, other_reads(u - st));
+              release(vidx, other_reads(u - 1));
             }
             if (qk) {
               tc_commit(s_full(T));
