@@ -137,18 +137,21 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // box = 128 rows x 64 elements of one head, 128-byte swizzle.  Out-of-range
 // rows read as zero.
 bool make_map(CUtensorMap *m, const void *base, bool bf16, int D, int heads, int64_t rows,
-              int64_t batch, int box_heads = 1, int box_rows = 128) {
+              int64_t batch, int box_heads = 1, int box_rows = 128, int box_cols = 64) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows,
                               (cuuint64_t)batch};
   const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2,
                                  (cuuint64_t)rows * heads * D * 2};
-  const cuuint32_t box[4] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows, 1};
+  // 64-column boxes (128-byte rows) take the 128-byte swizzle, 32-column
+  // boxes (64-byte rows) the 64-byte one
+  const cuuint32_t box[4] = {(cuuint32_t)box_cols, (cuuint32_t)box_heads, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -317,7 +320,10 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   const int64_t q_rows = Sq, k_rows = Sk;
   const int64_t q_batch = varlen ? 1 : B, k_batch = varlen ? 1 : B;
   if (!make_map(&a.tm_q, q, bf16, D, Hq, q_rows, q_batch)) return FA_ERR_CUDA;
-  if (!make_map(&a.tm_o, o, bf16, D, Hq, q_rows, q_batch)) return FA_ERR_CUDA;
+  // the prefill kernels store O in 32-column quarters, the head-dim-256
+  // kernel in 64-column halves
+  if (!make_map(&a.tm_o, o, bf16, D, Hq, q_rows, q_batch, 1, 128, wide ? 64 : 32))
+    return FA_ERR_CUDA;
   if (Sk > 0) {
     if (!make_map(&a.tm_k, k, bf16, D, Hkv, k_rows, k_batch)) return FA_ERR_CUDA;
     if (!make_map(&a.tm_v, v, bf16, D, Hkv, k_rows, k_batch)) return FA_ERR_CUDA;

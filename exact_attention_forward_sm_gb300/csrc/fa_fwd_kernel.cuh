@@ -544,22 +544,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Work w = (KVC ? decode_work_kvc(p, unit, lane) : decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane));
         if (!w.valid) continue;
         if (lane == 0) {
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
+          auto load_q = [&](int t) {
             int &q_loads = t ? q_loads1 : q_loads0;
-            if (KVC && t == 1) continue;  // one Q tile serves both
-            if ((KVC ? w.n_max : w.n_kv[t]) == 0 || !ok) continue;
+            if ((KVC ? w.n_max : w.n_kv[t]) == 0 || !ok) return;
             // the previous unit's Q_t is free once its last S_t = Q_t K^T is done
             if (q_loads > 0 && !wait(q_empty(t), (q_loads - 1) & 1)) {
               ok = false;
-              continue;
+              return;
             }
             mbar_arrive_expect_tx(q_full(t), L::kTileBytes);
             for (int c = 0; c < L::kChunks; ++c)
               tma_load_4d(sbase + L::kQOff + t * L::kTileBytes + c * kChunkBytes, &tm_q,
                           q_full(t), c * 64, w.head[t], w.q_row0 + w.m0[t], w.map_b, pol_q);
             ++q_loads;
-          }
+          };
           // one K or V tile of unit tile j (which: 0 K, 1 V) into the next ring slot
           auto issue = [&](int which, int j, int page) {
             const int idx = issued;
@@ -597,6 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               return pg;
             };
+            load_q(0);  // one Q tile serves both
             int pg_cur = w.n_max > 0 ? page_of(0) : 0;
             if (w.n_max > 0 && ok) issue(0, 0, pg_cur);
             for (int j = 0; j < w.n_max && ok; ++j) {
@@ -609,8 +608,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               pg_cur = pg_next;
             }
           } else {
+            // Q0, K0, Q1, V0, K1, V1, ...: tile 0's first S needs only Q0 and
+            // K0, and K0 does not wait behind the previous unit's last S1
+            load_q(0);
+            if (w.n_max > 0 && ok) issue(0, 0, 0);
+            load_q(1);
             for (int j = 0; j < w.n_max && ok; ++j) {
-              issue(0, j, 0);
+              if (j > 0) issue(0, j, 0);
               if (ok) issue(1, j, 0);
             }
           }
@@ -1107,26 +1111,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.lse_part[slot] = lse;
         }
       } else if (use_tma) {
+        // O leaves in 32-column quarters through the two 8 KB halves of the
+        // tile's staging buffer, quarter q through half q % 2.  Before the
+        // warpgroup meets after writing a quarter, the elected thread waits
+        // until the store from the other half has read it, so the next
+        // quarter can be written there while this one is being read; the
+        // last store of a unit is only waited for when its half is next
+        // written.
 #pragma unroll
-        for (int half = 0; half < D / 64; ++half) {
-          named_barrier_sync(1 + t, 128);  // staging buffer free
+        for (int qd = 0; qd < D / 32; ++qd) {
+          const uint32_t buf = stage + (qd & 1) * (kChunkBytes / 2);
           if (ok) {
-            // row `row`, 16-byte chunk c at swizzled position c ^ (row % 8)
+            // row `row`, 16-byte chunk c at swizzled position c ^ ((row / 2) % 4)
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int k = half * 32 + 4 * c;
-              st_shared_v4(stage + row * 128 + ((c ^ (row & 7)) << 4), packed(k), packed(k + 1),
-                           packed(k + 2), packed(k + 3));
+            for (int c = 0; c < 4; ++c) {
+              const int k = qd * 16 + 4 * c;
+              st_shared_v4(buf + row * 64 + ((c ^ ((row >> 1) & 3)) << 4), packed(k),
+                           packed(k + 1), packed(k + 2), packed(k + 3));
             }
             fence_proxy_async_smem();
           }
-          named_barrier_sync(1 + t, 128);  // staging buffer full
-          if (elected) {
-            if (ok) {
-              tma_store_4d(&tm_o, stage, half * 64, w.head[t], w.q_row0 + m0, w.map_b);
-              bulk_commit_group();
-            }
-            bulk_wait_group_read0();
+          if (elected) bulk_wait_group_read0();  // the other half is free again
+          named_barrier_sync(1 + t, 128);
+          if (elected && ok) {
+            tma_store_4d(&tm_o, buf, qd * 32, w.head[t], w.q_row0 + m0, w.map_b);
+            bulk_commit_group();
           }
         }
       } else if (row_valid && ok) {
