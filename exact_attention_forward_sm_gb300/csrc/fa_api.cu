@@ -367,6 +367,7 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   p.wait_limit = kDefaultWaitLimit;
   p.status = status;
   p.trace = nullptr;
+  fa::set_divisors(p);
   if (!set_trace(p)) return FA_ERR_CUDA;
   a.grid = (int)grid;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -497,6 +498,7 @@ int forward_kvcache(const void *q, const void *k_cache, const void *v_cache, voi
   p.wait_limit = kDefaultWaitLimit;
   p.status = status;
   p.trace = nullptr;
+  fa::set_divisors(p);
   if (!set_trace(p)) return FA_ERR_CUDA;
   a.grid = (int)(units < sms ? units : sms);
   a.stream = reinterpret_cast<cudaStream_t>(stream);

@@ -73,6 +73,33 @@ constexpr int kMmaWarp2 = 10; // issues tile 1's MMAs
 constexpr int kTmemCols = 512;
 constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 64 elements x 2 bytes
 
+// n / d for 0 <= n < 2^31 as a multiply-high and a shift (Granlund and
+// Montgomery's division by invariant integers, round-up reciprocal): with
+// p = 31 + ceil(log2 d) and m = ceil(2^p / d) < 2^32, the error of n m / 2^p
+// against n / d is below 2^(31 - p) <= 1 / d, which never reaches the next
+// integer, so floor(n / d) = floor(n m / 2^p).  d = 1 passes n through.
+struct FastDiv {
+  int d;
+  uint32_t mul;
+  uint32_t shift;  // p - 32
+};
+
+inline FastDiv make_fast_div(int d) {
+  FastDiv f{d, 0u, 0u};
+  if (d > 1) {
+    int l = 0;
+    while ((1ll << l) < d) ++l;
+    const int p = 31 + l;
+    f.mul = (uint32_t)(((1ull << p) + (uint64_t)d - 1) / (uint64_t)d);
+    f.shift = (uint32_t)(p - 32);
+  }
+  return f;
+}
+
+__device__ __forceinline__ int fast_div(const FastDiv &f, int n) {
+  return f.d == 1 ? n : (int)(__umulhi((uint32_t)n, f.mul) >> f.shift);
+}
+
 struct FwdParams {
   void *o;
   float *lse;
@@ -117,10 +144,21 @@ struct FwdParams {
   int num_pages;            // pages in the cache
   int tok_per_tile;         // 128 / group
   int tok_blocks;           // ceil(Sq / tok_per_tile)
+  // the divisors of the unit index, set by set_divisors() once the fields
+  // above are final
+  FastDiv div_splits, div_head_units, div_B, div_Hkv, div_tok_blocks;
   long long wait_limit;     // bounded-wait limit in SM clock cycles
   int *status;              // device status word (first error wins)
   unsigned long long *trace;  // clock64 pipeline trace (trace builds only)
 };
+
+inline void set_divisors(FwdParams &p) {
+  p.div_splits = make_fast_div(p.num_splits > 1 ? p.num_splits : 1);
+  p.div_head_units = make_fast_div(p.head_units > 0 ? p.head_units : 1);
+  p.div_B = make_fast_div(p.B > 0 ? p.B : 1);
+  p.div_Hkv = make_fast_div(p.Hkv > 0 ? p.Hkv : 1);
+  p.div_tok_blocks = make_fast_div(p.tok_blocks > 0 ? p.tok_blocks : 1);
+}
 
 // Pipeline trace (compiled in with -DFA_TRACE): CTA 0 records SM clock stamps
 // of the K/V steps of its first unit into a 2048-entry buffer.
@@ -262,13 +300,14 @@ __device__ inline Work decode_work_kvc(const FwdParams &p, int unit, int lane) {
   w.valid = 0;
   w.split = 0;
   if (p.num_splits > 1) {
-    w.split = unit % p.num_splits;
-    unit /= p.num_splits;
+    const int u = fast_div(p.div_splits, unit);
+    w.split = unit - u * p.num_splits;
+    unit = u;
   }
-  const int hkv = unit % p.Hkv;
-  unit /= p.Hkv;
-  const int tb = unit % p.tok_blocks;
-  const int b = unit / p.tok_blocks;
+  const int u_h = fast_div(p.div_Hkv, unit);
+  const int hkv = unit - u_h * p.Hkv;
+  const int b = fast_div(p.div_tok_blocks, u_h);
+  const int tb = u_h - b * p.tok_blocks;
   if (b >= p.B) return w;
   const int lk = p.cache_seqlens[b];
   const int64_t cap = p.block_table ? (int64_t)p.max_blocks * p.page_rows : p.page_rows;
@@ -307,15 +346,17 @@ __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
   w.valid = 0;
   w.split = 0;
   if (EXT && p.num_splits > 1) {  // splits of one unit are adjacent: heavy units stay first
-    w.split = unit % p.num_splits;
-    unit /= p.num_splits;
+    const int u = fast_div(p.div_splits, unit);
+    w.split = unit - u * p.num_splits;
+    unit = u;
   }
-  const int hu = unit % p.head_units;
+  const int u_hu = fast_div(p.div_head_units, unit);  // unit / head_units
+  const int hu = unit - u_hu * p.head_units;
   int b = 0, ru = 0, n_ru = 0;
   if (!VARLEN) {
-    const int per_ru = p.B * p.head_units;
-    ru = unit / per_ru;
-    b = (unit % per_ru) / p.head_units;
+    // unit = (ru * B + b) * head_units + hu
+    ru = fast_div(p.div_B, u_hu);
+    b = u_hu - ru * p.B;
     n_ru = p.dense_row_units;
     if (ru >= n_ru) return w;
     w.lq = p.Sq;
@@ -325,7 +366,7 @@ __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
     w.map_b = b;
     w.o_row0 = (int64_t)b * p.Sq;
   } else {
-    const int idx = unit / p.head_units;
+    const int idx = u_hu;
     int base = 0, found = -1, found_ru = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
       const int bb = b0 + lane;
