@@ -490,7 +490,22 @@ def run_gpu_arm(args, rank, local_rank, world):
     if "bf16_tflops_sustained" in peaks and not hbm_bound:
         line["roofline"]["frac_of_sustained"] = round(
             achieved / float(peaks["bf16_tflops_sustained"]), 4)
+    if not hbm_bound:
+        # the stricter denominator: every SM's tensor pipe at its measured dense
+        # rate (an M128 N128 K16 bf16 tcgen05 MMA retires in 64 cycles, 8192
+        # FLOP per cycle per SM) at the median SM clock seen while timing
+        mhz = clock.get("sm_mhz") or clock.get("sm_max_mhz")
+        if mhz:
+            sms = torch.cuda.get_device_properties(0).multi_processor_count
+            theo = sms * TC_FLOP_PER_CYCLE_SM * float(mhz) * 1e6 / 1e12
+            line["roofline"]["theoretical"] = {
+                "peak": round(theo, 1), "unit": UNIT, "frac": round(achieved / theo, 4),
+                "basis": f"{sms} SMs x {TC_FLOP_PER_CYCLE_SM} FLOP/cycle x {mhz} MHz"}
     return line, prob
+
+
+# dense 16-bit tcgen05 rate per SM per cycle, from a micro-benchmark on GB300
+TC_FLOP_PER_CYCLE_SM = 8192
 
 
 def barrier(world):
