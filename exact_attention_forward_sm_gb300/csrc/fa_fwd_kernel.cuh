@@ -227,6 +227,28 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+// Bounded wait like wait_bar, polling the phase without suspending the thread
+// (MMA issuers waiting for P: a suspended thread wakes ~200 cycles after the
+// phase completes, and the tensor pipe, whose MMA queue is about one
+// instruction deep, idles for as long as the issuer is late).
+__device__ __forceinline__ bool wait_bar_spin(uint32_t bar, uint32_t parity,
+                                              volatile int *abort_flag, long long limit,
+                                              int *status) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (mbar_test_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      record_status(status, 4);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 struct Work {
   int valid;
   int split;         // K/V split of the unit (0 without split-KV)
@@ -728,11 +750,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      // bounded spin for this issuer's turn (the other one is issuing)
+      // bounded spin for this issuer's turn (the other one is issuing); the
+      // flag is polled several times per abort / time-limit check, because
+      // the tensor pipe runs dry while this thread waits to see it
       auto take_turn = [&]() {
         if (*mma_turn == T) return true;
         const long long t0 = clock64();
-        while (*mma_turn != T) {
+        while (true) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (*mma_turn == T) return true;
           if (*abort_flag) return false;
           if (clock64() - t0 > limit) {
             record_status(p.status, 4);
@@ -740,9 +767,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             return false;
           }
         }
-        return true;
       };
       auto pass_turn = [&]() { *mma_turn = 1 - T; };
+      // P of the tile is polled (see wait_bar_spin)
+      auto wait_p = [&](int h, uint32_t par) {
+        return wait_bar_spin(p_half(T, h), par, abort_flag, limit, p.status);
+      };
       // every K/V load is released by two arrivals, one per tile; a load the
       // other tile never reads gets both of them from this issuer
       auto release = [&](int idx, bool other_reads) {
@@ -840,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
                    (jq > 1 || o_done == 0 || wait(o_free(T), (o_done - 1) & 1));
             if (ok && qk) ok = wait(kv_full(kidx % L::kStages), kv_par(kidx));
-            if (ok && pv) ok = wait(p_half(T, 0), p_seen & 1);
+            if (ok && pv) ok = wait_p(0, p_seen & 1);
             FA_TRACE_AT(i == 0 && u < 64, 1024 + u * 8 + 2 + 2 * T);
             ok = ok && take_turn();
             if (!ok) break;
@@ -849,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // keys 0-63 go to the tensor pipe while the softmax still works
               // on keys 64-127; the turn is held until the bracket is complete
               issue_pv_half(vidx, 0, jq == 1);
-              if (!wait(p_half(T, 1), p_seen & 1)) {
+              if (!wait_p(1, p_seen & 1)) {
                 ok = false;
                 break;
               }

@@ -205,11 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               // previous unit's epilogue must have read out
               ok = wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
                    (j > 1 || o_done == 0 || wait(o_free, (o_done - 1) & 1)) &&
-                   wait(p_half(0), p_seen & 1);
+                   wait_bar_spin(p_half(0), p_seen & 1, abort_flag, limit, p.status);
               if (!ok) break;
               tc_fence_after();
               issue_pv_half(vidx, 0, j == 1);
-              if (!wait(p_half(1), p_seen & 1)) {
+              if (!wait_bar_spin(p_half(1), p_seen & 1, abort_flag, limit, p.status)) {
                 ok = false;
                 break;
               }
