@@ -28,17 +28,31 @@ __device__ unsigned long long g_fa_trace[fa::kTraceEntries];
 
 namespace fa {
 
-// Kernel used only to exercise the bounded wait: nothing arrives on the barrier.
+// Kernel used only to exercise the bounded waits: nothing arrives on the
+// barrier.  The suspending wait (wait_bar) and the polling one of the MMA
+// issuers (wait_bar_spin) each wait `limit` cycles; FA_ERR_TIMEOUT is recorded
+// only if both gave up and recorded it themselves, anything else records
+// FA_ERR_INVALID_ARG.
 static __global__ void fa_wait_timeout_kernel(long long limit, int *status) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
+  __shared__ int local_status;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bar), 1);
     abort_flag = 0;
+    local_status = 0;
     fence_barrier_init();
   }
   __syncthreads();
-  if (threadIdx.x == 0) wait_bar(smem_u32(&bar), 0, &abort_flag, limit, status);
+  if (threadIdx.x == 0) {
+    const bool got1 = wait_bar(smem_u32(&bar), 0, &abort_flag, limit, &local_status);
+    const int st1 = local_status;
+    abort_flag = 0;
+    local_status = 0;
+    const bool got2 = wait_bar_spin(smem_u32(&bar), 0, &abort_flag, limit, &local_status);
+    const int st2 = local_status;
+    record_status(status, (!got1 && !got2 && st1 == 4 && st2 == 4) ? 4 : 1);
+  }
   __syncthreads();
 }
 

@@ -271,8 +271,10 @@ int fa_get_device_error(fa_stream_t stream);
 /*
  * fa_debug_wait_timeout — self-test of the bounded pipeline waits.  Launches
  * one block that waits on a shared-memory barrier nothing will ever arrive on,
- * with a wait limit of `limit_cycles` SM clock cycles (1 .. 2^34).  The wait
- * gives up, records FA_ERR_TIMEOUT in the device status word and the kernel
+ * once with the suspending wait and once with the polling wait of the MMA
+ * issuers, each with a limit of `limit_cycles` SM clock cycles (1 .. 2^34).
+ * When both give up as designed, FA_ERR_TIMEOUT is recorded in the device
+ * status word (FA_ERR_INVALID_ARG if either wait misbehaved) and the kernel
  * returns normally; the context stays usable.  Returns the launch status.
  */
 int fa_debug_wait_timeout(long long limit_cycles, fa_stream_t stream);
