@@ -475,6 +475,12 @@ __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
   return w;
 }
 
+// Field of tile t of a Work record.  The tile index of a role is a run-time
+// value; indexing the record's arrays with it would place the whole record in
+// local memory (a round trip to L2 at every unit, since shared memory leaves
+// little L1), so the field is selected instead.
+__device__ __forceinline__ int tile_field(const int (&a)[2], int t) { return t ? a[1] : a[0]; }
+
 // 16-bit pair of P values (low half = first key).
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
@@ -609,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           auto load_q = [&](int t) {
             int &q_loads = t ? q_loads1 : q_loads0;
-            if ((KVC ? w.n_max : w.n_kv[t]) == 0 || !ok) return;
+            if ((KVC ? w.n_max : tile_field(w.n_kv, t)) == 0 || !ok) return;
             // the previous unit's Q_t is free once its last S_t = Q_t K^T is done
             if (q_loads > 0 && !wait(q_empty(t), (q_loads - 1) & 1)) {
               ok = false;
@@ -618,7 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(q_full(t), L::kTileBytes);
             for (int c = 0; c < L::kChunks; ++c)
               tma_load_4d(sbase + L::kQOff + t * L::kTileBytes + c * kChunkBytes, &tm_q,
-                          q_full(t), c * 64, w.head[t], w.q_row0 + w.m0[t], w.map_b, pol_q);
+                          q_full(t), c * 64, tile_field(w.head, t),
+                          w.q_row0 + tile_field(w.m0, t), w.map_b, pol_q);
             ++q_loads;
           };
           // one K or V tile of unit tile j (which: 0 K, 1 V) into the next ring slot
@@ -795,8 +802,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O += P V of a tile's previous load is issued and its V slot
           // released before waiting for the next K: the producer refills the
           // ring without waiting for a K load to land first
-          const int n = w.n_kv[T], nm = w.n_max;
-          const int off = w.kv_begin[T] - w.kv_ub;
+          const int n = tile_field(w.n_kv, T), nm = w.n_max;
+          const int off = tile_field(w.kv_begin, T) - w.kv_ub;
           // ring positions of the unit's loads (the producer's K-ahead order)
           auto kpos = [&](int u) { return u == 0 ? 0 : 2 * u - 1; };
           auto vpos = [&](int u) { return u + 1 < nm ? 2 * u + 2 : 2 * nm - 1; };
@@ -843,13 +850,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (nm > 0) ++q_used;  // one Q load per unit with keys
           used += 2 * w.n_max;
         } else if (!KVC && lane == 0) {
-          const int n = w.n_kv[T], n_other = w.n_kv[1 - T];
+          const int n = tile_field(w.n_kv, T), n_other = tile_field(w.n_kv, 1 - T);
           // bracket u = 0 .. n_max of the unit: O_T += P_T V(u-1) if this
           // tile read load u-1, then S_T = Q_T K(u)^T if it reads load u.
           // Both issuers walk every bracket, so the turns stay paired even
           // when the tiles' K/V ranges differ (local windows).
-          const int off = w.kv_begin[T] - w.kv_ub;
-          const int off_other = w.kv_begin[1 - T] - w.kv_ub;
+          const int off = tile_field(w.kv_begin, T) - w.kv_ub;
+          const int off_other = tile_field(w.kv_begin, 1 - T) - w.kv_ub;
           auto other_reads = [&](int u) {
             const int d = u - off_other;
             return d >= 0 && d < n_other;
@@ -948,16 +955,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int unit = unit_of(i);
       if (unit >= p.total_units) break;
       const Work w = (KVC ? decode_work_kvc(p, unit, lane) : decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane));
-      if (!w.valid || w.m0[t] >= w.lq) continue;  // no rows of this tile
-      const int m0 = w.m0[t];        // per-tile fields read once per unit
-      const int n_kv = w.n_kv[t];
+      if (!w.valid || tile_field(w.m0, t) >= w.lq) continue;  // no rows of this tile
+      const int m0 = tile_field(w.m0, t);  // per-tile fields read once per unit
+      const int n_kv = tile_field(w.n_kv, t);
       const int lq = w.lq, lk = w.lk;
       // query row within its sequence and its head (KV-cache tiles pack
       // (token, head) pairs: row r is token m0 + r / group, head r % group)
       const int qi = KVC ? m0 + row / p.group : m0 + row;
-      const int head = KVC ? w.head[t] + row % p.group : w.head[t];
+      const int head_t = tile_field(w.head, t);
+      const int head = KVC ? head_t + row % p.group : head_t;
       const int diag = qi + lk - lq;  // last visible key of this row (causal)
-      [[maybe_unused]] const int kv_begin = w.kv_begin[t];
+      [[maybe_unused]] const int kv_begin = tile_field(w.kv_begin, t);
       [[maybe_unused]] const float slope_l2 =
           (EXT && p.alibi) ? p.alibi[head] * 1.4426950408889634f : 0.f;
       float m = -INFINITY, l = 0.f;
@@ -1079,6 +1087,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------- epilogue
       [[maybe_unused]] const bool tr = i == 0 && quarter == 0 && lane == 0;
       FA_TRACE_AT(tr, (t * 64 + 63) * 8 + 5);
+#ifndef FA_EPI_REDECODE
+#define FA_EPI_REDECODE 1
+#endif
+      // The fields only the epilogue needs (sequence, output row base, tensor
+      // map coordinates, split) are decoded again here from an opaque copy of
+      // the unit index, so they hold no registers through the K/V loop.
+      int unit_e = unit;
+      if (FA_EPI_REDECODE) asm volatile("mov.b32 %0, %1;" : "=r"(unit_e) : "r"(unit));
+      const Work we = FA_EPI_REDECODE
+                          ? (KVC ? decode_work_kvc(p, unit_e, lane)
+                                 : decode_work<CAUSAL, VARLEN, EXT>(p, unit_e, lane))
+                          : w;
       // O_t of this unit (zero when no key is visible), read out of tensor
       // memory and released first so the next unit's O += P V can start
       uint32_t orr[D];
@@ -1106,7 +1126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_barrier_sync(3, 256);
         tc_fence_after();
-        const int n1 = w.n_kv[1];
+        const int n1 = we.n_kv[1];
         const float m1 = xm[row], l1 = xl[row];
         const float mine = l > 0.f ? m : -INFINITY;
         const float mx = fmaxf(mine, m1);
@@ -1156,13 +1176,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const bool row_valid = qi < lq;
-      const int64_t tok = w.o_row0 + qi;
+      const int64_t tok = we.o_row0 + qi;
       auto packed = [&](int k) {  // 16-bit pair of normalised O columns 2k, 2k+1
         return pack_p<BF16>(__uint_as_float(orr[2 * k]) * inv_l,
                             __uint_as_float(orr[2 * k + 1]) * inv_l);
       };
       const int64_t li = VARLEN ? (int64_t)head * p.Sq + tok
-                                : ((int64_t)w.b * p.Hq + head) * p.Sq + qi;
+                                : ((int64_t)we.b * p.Hq + head) * p.Sq + qi;
       const float lse = (l > 0.f) ? (m * scale_log2 + log2f(l)) * 0.69314718055994531f
                                   : -INFINITY;
       // a packed tile cut by its sequence end would spill into the next
@@ -1171,7 +1191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (EXT && p.num_splits > 1) {
         // split-KV partial: normalised fp32 O_s and LSE_s of this split
         if (row_valid && ok) {
-          const int64_t slot = (int64_t)w.split * p.part_rows + li;
+          const int64_t slot = (int64_t)we.split * p.part_rows + li;
           float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * D);
 #pragma unroll
           for (int k = 0; k < D / 4; ++k)
@@ -1205,7 +1225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (elected) bulk_wait_group_read0();  // the other half is free again
           named_barrier_sync(1 + t, 128);
           if (elected && ok) {
-            tma_store_4d(&tm_o, buf, qd * 32, w.head[t], w.q_row0 + m0, w.map_b);
+            tma_store_4d(&tm_o, buf, qd * 32, head_t, we.q_row0 + m0, we.map_b);
             bulk_commit_group();
           }
         }
