@@ -1093,8 +1093,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The fields only the epilogue needs (sequence, output row base, tensor
       // map coordinates, split) are decoded again here from an opaque copy of
       // the unit index, so they hold no registers through the K/V loop.
-      int unit_e = unit;
-      if (FA_EPI_REDECODE) asm volatile("mov.b32 %0, %1;" : "=r"(unit_e) : "r"(unit));
+      int i_e = i;
+      if (FA_EPI_REDECODE) asm volatile("mov.b32 %0, %1;" : "=r"(i_e) : "r"(i));
+      const int unit_e = unit_of(i_e);
       const Work we = FA_EPI_REDECODE
                           ? (KVC ? decode_work_kvc(p, unit_e, lane)
                                  : decode_work<CAUSAL, VARLEN, EXT>(p, unit_e, lane))
@@ -1225,7 +1226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (elected) bulk_wait_group_read0();  // the other half is free again
           named_barrier_sync(1 + t, 128);
           if (elected && ok) {
-            tma_store_4d(&tm_o, buf, qd * 32, head_t, we.q_row0 + m0, we.map_b);
+            tma_store_4d(&tm_o, buf, qd * 32, tile_field(we.head, t), we.q_row0 + m0, we.map_b);
             bulk_commit_group();
           }
         }
