@@ -819,11 +819,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (jq >= 1) {
               ok = issued_past(vidx) && wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
                    (jq > 1 || o_done == 0 || wait(o_free(T), (o_done - 1) & 1)) &&
-                   wait(p_half(T, 0), p_seen & 1);
+                   wait_p(0, p_seen & 1);
               if (!ok) break;
               tc_fence_after();
               issue_pv_half(vidx, 0, jq == 1);
-              if (!wait(p_half(T, 1), p_seen & 1)) {
+              if (!wait_p(1, p_seen & 1)) {
                 ok = false;
                 break;
               }
