@@ -39,8 +39,11 @@
 // order, so the S_t write of step j happens after the P_t read of step j-1
 // (the same ordering the pages' FA4 Blackwell kernel relies on for its S/P
 // aliasing).  Descriptors are built once and each MMA adds a compile-time
-// offset: the single issuing thread must emit an MMA every ~64 cycles to keep
-// the tensor pipe busy, so the issue stream is kept branch-free.
+// offset: the tensor pipe's MMA queue is about one instruction deep, so the
+// issuing thread must emit the next MMA as soon as one starts, and the issue
+// stream is kept branch-free.  For the same reason the issuers poll the P
+// barriers and the turn flag instead of suspending on them (a suspended thread
+// wakes ~200 cycles after the phase completes).
 //
 // Online softmax (release notes v1.7 section 1.2, v1.2 sections 1-2): row max
 // m in raw score units, scale_log2 = scale * log2(e).  First K/V tile: m = its
