@@ -1090,19 +1090,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------- epilogue
       [[maybe_unused]] const bool tr = i == 0 && quarter == 0 && lane == 0;
       FA_TRACE_AT(tr, (t * 64 + 63) * 8 + 5);
-#ifndef FA_EPI_REDECODE
-#define FA_EPI_REDECODE 1
-#endif
       // The fields only the epilogue needs (sequence, output row base, tensor
       // map coordinates, split) are decoded again here from an opaque copy of
-      // the unit index, so they hold no registers through the K/V loop.
-      int i_e = i;
-      if (FA_EPI_REDECODE) asm volatile("mov.b32 %0, %1;" : "=r"(i_e) : "r"(i));
+      // the unit counter, so they hold no registers through the K/V loop.
+      int i_e;
+      asm volatile("mov.b32 %0, %1;" : "=r"(i_e) : "r"(i));
       const int unit_e = unit_of(i_e);
-      const Work we = FA_EPI_REDECODE
-                          ? (KVC ? decode_work_kvc(p, unit_e, lane)
-                                 : decode_work<CAUSAL, VARLEN, EXT>(p, unit_e, lane))
-                          : w;
+      const Work we = KVC ? decode_work_kvc(p, unit_e, lane)
+                          : decode_work<CAUSAL, VARLEN, EXT>(p, unit_e, lane);
       // O_t of this unit (zero when no key is visible), read out of tensor
       // memory and released first so the next unit's O += P V can start
       uint32_t orr[D];
