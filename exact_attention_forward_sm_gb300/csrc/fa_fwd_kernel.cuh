@@ -37,8 +37,9 @@
 // alternating tiles, so tile 0's softmax runs while the tensor pipe works on
 // tile 1 and vice versa.  The tensor pipe executes one CTA's MMAs in issue
 // order, so the S_t write of step j happens after the P_t read of step j-1
-// (the same ordering the pages' FA4 Blackwell kernel relies on for its S/P
-// aliasing).  Descriptors are built once and each MMA adds a compile-time
+// (the ordering upstream's FA4 Blackwell kernel relies on for its S/P
+// aliasing, per the upstream code survey's FA4 section and the FA4
+// changelog's S/P ping-pong note).  Descriptors are built once and each MMA adds a compile-time
 // offset: the tensor pipe's MMA queue is about one instruction deep, so the
 // issuing thread must emit the next MMA as soon as one starts, and the issue
 // stream is kept branch-free.  For the same reason the issuers poll the P

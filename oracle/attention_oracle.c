@@ -47,10 +47,10 @@
  *                             oracle_attention() is this function with every
  *                             variant switched off.
  *
- * Readings of points the pages leave open (each is also listed in the design
- * notes): LSE is the natural log over the scaled scores; causal masking with
- * Sq != Sk is aligned bottom-right (key j visible iff j <= i + Lk - Lq); a row
- * with no visible key gets O = 0 and LSE = -inf.  For the variants, with
+ * Readings of points the pages leave open: LSE is the natural log over the
+ * scaled scores; causal masking with Sq != Sk is aligned bottom-right (key j
+ * visible iff j <= i + Lk - Lq); a row with no visible key gets O = 0 and
+ * LSE = -inf.  For the variants, with
  * diag = i + Lk - Lq the bottom-right aligned diagonal of row i:
  *   window (left, right): key j visible iff diag - left <= j <= diag + right,
  *     a negative bound meaning unbounded on that side (so window (0, 0) with
