@@ -23,7 +23,7 @@ __all__ = [
     "library_path", "load_library", "fa_fwd", "fa_fwd_ex", "fa_fwd_split", "fa_split_plan",
     "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes", "fa_fwd_kvcache", "attention_kvcache", "fa_kvcache_plan",
     "fa_get_device_error", "fa_debug_wait_timeout",
-    "fa_debug_trace_read",
+    "fa_debug_trace_read", "fa_shutdown",
     "fa_status_string", "fa_version", "attention_forward", "EXPORTED_SYMBOLS",
 ]
 
@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_split", "fa_split_plan",
                     "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes", "fa_fwd_kvcache",
                     "fa_kvcache_plan",
                     "fa_get_device_error", "fa_debug_wait_timeout",
-                    "fa_debug_trace_read", "fa_status_string", "fa_version")
+                    "fa_debug_trace_read", "fa_shutdown", "fa_status_string", "fa_version")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -103,6 +103,8 @@ def load_library():
         lib.fa_debug_wait_timeout.restype = i32
         lib.fa_debug_trace_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i32]
         lib.fa_debug_trace_read.restype = i32
+        lib.fa_shutdown.argtypes = []
+        lib.fa_shutdown.restype = i32
         lib.fa_status_string.argtypes = [i32]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_version.argtypes = []
@@ -221,6 +223,12 @@ def fa_debug_trace_read(n=2048):
     buf = (ctypes.c_ulonglong * n)()
     st = load_library().fa_debug_trace_read(buf, n)
     return st, list(buf)
+
+
+def fa_shutdown() -> int:
+    """Drop the library's cached per-device state (status-word and scratch
+    addresses, SM counts, shared-memory opt-ins); later calls set it up again."""
+    return load_library().fa_shutdown()
 
 
 def fa_status_string(status) -> str:

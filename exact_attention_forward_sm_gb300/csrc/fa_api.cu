@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -27,6 +28,11 @@ __device__ unsigned long long g_fa_trace[fa::kTraceEntries];
 #endif
 
 namespace fa {
+
+std::atomic<unsigned> &launch_epoch() {
+  static std::atomic<unsigned> epoch{0};
+  return epoch;
+}
 
 // Kernel used only to exercise the bounded waits: nothing arrives on the
 // barrier.  The suspending wait (wait_bar) and the polling one of the MMA
@@ -110,13 +116,27 @@ int *status_ptr(int device) {
   std::lock_guard<std::mutex> lock(g_status_mu);
   if (!g_status_ptr[device]) {
     void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_fa_status) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fa_status) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
     g_status_ptr[device] = static_cast<int *>(ptr);
   }
   return g_status_ptr[device];
 }
 
 void *g_fixed_scratch[kMaxDevices] = {};
+
+// Forget every cached per-device value (fa_shutdown).
+void reset_device_caches() {
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  for (int d = 0; d < kMaxDevices; ++d) {
+    g_status_ptr[d] = nullptr;
+    g_sm_count[d] = 0;
+    g_fixed_scratch[d] = nullptr;
+  }
+  fa::launch_epoch().fetch_add(1, std::memory_order_acq_rel);
+}
 
 // Device address of g_fa_fixed_scratch on `device` (looked up once per device).
 void *fixed_scratch_ptr(int device) {
@@ -204,10 +224,10 @@ int auto_splits(int B, int Hq, int Hkv, int Sq, int Sk, int D, bool varlen, int 
                        (per_seq + fa::kBlockN - 1) / fa::kBlockN, sms);
 }
 
-// Caller-chosen split-KV scratch (fa_fwd_split_noalloc): used instead of a
-// stream-ordered allocation.
+// The library's fixed split-KV scratch (fa_fwd_split_noalloc), used instead
+// of a stream-ordered allocation.  Its device address is looked up only when
+// a call really splits, after every argument has been checked.
 struct FixedScratch {
-  void *ptr;
   size_t bytes;
 };
 
@@ -225,7 +245,8 @@ int run_split(fa::LaunchArgs &a, int splits, int64_t lse_rows, int D, bool bf16,
     char *base = nullptr;
     if (fixed) {
       if (o_bytes + l_bytes > fixed->bytes) return FA_ERR_SCRATCH_LIMIT;
-      base = static_cast<char *>(fixed->ptr);
+      base = static_cast<char *>(fixed_scratch_ptr(a.device));
+      if (!base) return FA_ERR_CUDA;
     } else {
       if (cudaMallocAsync(&scratch, o_bytes + l_bytes, a.stream) != cudaSuccess) {
         cudaGetLastError();
@@ -577,12 +598,8 @@ int fa_fwd_split_noalloc(const void *q, const void *k, const void *v, void *o, f
                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                          fa_stream_t stream, int dtype, int window_left, int window_right,
                          float softcap, const float *alibi_slopes, int num_splits) {
-  int device = 0;
-  if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
   FixedScratch fixed;
-  fixed.ptr = fixed_scratch_ptr(device);
   fixed.bytes = kFixedScratchBytes;
-  if (!fixed.ptr) return FA_ERR_CUDA;
   return forward(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, cu_seqlens_q,
                  cu_seqlens_k, stream, dtype, window_left, window_right, softcap, alibi_slopes,
                  num_splits, &fixed);
@@ -600,6 +617,11 @@ int fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache, void
 }
 
 long long fa_noalloc_scratch_bytes(void) { return (long long)kFixedScratchBytes; }
+
+int fa_shutdown(void) {
+  reset_device_caches();
+  return FA_OK;
+}
 
 int fa_split_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int varlen, int num_splits,
                   long long *scratch_bytes) {

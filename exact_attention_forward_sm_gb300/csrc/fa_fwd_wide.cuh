@@ -479,14 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool BF16, bool CAUSAL, bool VARLEN, bool EXT>
 cudaError_t launch_wide(const LaunchArgs &a) {
   auto kern = fa_fwd_wide_kernel<BF16, CAUSAL, VARLEN, EXT>;
-  static std::atomic<unsigned long long> configured{0};
-  const unsigned long long bit = 1ull << (a.device & 63);
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SmemWide::kAlloc);
-    if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
-  }
+  static SmemOptIn opt_in;
+  const cudaError_t e = opt_in.ensure(kern, (int)SmemWide::kAlloc, a.device);
+  if (e != cudaSuccess) return e;
   kern<<<a.grid, kThreads, SmemWide::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
   return cudaGetLastError();
 }

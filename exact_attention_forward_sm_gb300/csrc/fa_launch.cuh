@@ -15,18 +15,39 @@ struct LaunchArgs {
   int device;
 };
 
+// Generation of the per-device launch state (defined in fa_api.cu).
+// fa_shutdown() advances it, so every kernel sets its shared-memory attribute
+// again on its next launch on each device.
+std::atomic<unsigned> &launch_epoch();
+
+// A kernel's opt-in to its large dynamic shared memory, made once per device
+// and epoch: `bits` has bit (device % 64) set once the attribute is set.
+struct SmemOptIn {
+  std::atomic<unsigned long long> bits{0};
+  std::atomic<unsigned> epoch{0};
+
+  template <class Kernel>
+  cudaError_t ensure(Kernel kern, int bytes, int device) {
+    const unsigned ep = launch_epoch().load(std::memory_order_acquire);
+    if (epoch.load(std::memory_order_acquire) != ep) {
+      bits.store(0, std::memory_order_release);
+      epoch.store(ep, std::memory_order_release);
+    }
+    const unsigned long long bit = 1ull << (device & 63);
+    if (bits.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) bits.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+  }
+};
+
 template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT = false, bool KVC = false>
 cudaError_t launch_fwd(const LaunchArgs &a) {
   auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN, EXT, KVC>;
-  // opt in to the large dynamic shared memory once per device
-  static std::atomic<unsigned long long> configured{0};
-  const unsigned long long bit = 1ull << (a.device & 63);
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Smem<D, KVC>::kAlloc);
-    if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
-  }
+  static SmemOptIn opt_in;
+  const cudaError_t e = opt_in.ensure(kern, (int)Smem<D, KVC>::kAlloc, a.device);
+  if (e != cudaSuccess) return e;
   kern<<<a.grid, kThreads, Smem<D, KVC>::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
   return cudaGetLastError();
 }

@@ -234,9 +234,10 @@ int fa_kvcache_plan(int B, int Hq, int Hkv, int Sq, int D, long long capacity,
  * array.  Nothing in the array has to start at zero: every partial slot the
  * merge reads is written by the same call first.
  *
- * The first call on a device looks up the array's device address with
- * cudaGetSymbolAddress (and fails with FA_ERR_CUDA if that lookup fails);
- * make that first call before any stream capture.  Calls that may overlap in
+ * The first call on a device that splits (after every argument check) looks
+ * up the array's device address with cudaGetSymbolAddress (and fails with
+ * FA_ERR_CUDA if that lookup fails); make that first call before any stream
+ * capture.  Calls that may overlap in
  * time on one device (different streams, or different host threads) share
  * the array and race: their outputs are then undefined.  Serialise them on
  * one stream, or use fa_fwd_split.
@@ -288,6 +289,24 @@ int fa_debug_wait_timeout(long long limit_cycles, fa_stream_t stream);
  * Product builds return FA_ERR_UNSUPPORTED.
  */
 int fa_debug_trace_read(unsigned long long *host_out, int n);
+
+/*
+ * fa_shutdown — forget the library's per-device state on every device.
+ *
+ * The library keeps, per device and created lazily by the first call there:
+ * the device addresses of its status word and of the fixed scratch array of
+ * fa_fwd_split_noalloc (both static device symbols of the library's module),
+ * the multiprocessor count, and each kernel's opt-in to its large dynamic
+ * shared memory.  It allocates no device or host memory, and tensor maps are
+ * built per call, so there is nothing to free.  fa_shutdown() drops those
+ * cached values; the next call on a device looks them up again.  Call it
+ * after cudaDeviceReset() (which invalidates the cached addresses) or before
+ * unloading the library.  It does not wait for queued work and must not run
+ * while another host thread is inside a call of this library.  The pages
+ * describe no such call: it belongs to this library's own lazily created
+ * per-device state.  Returns FA_OK.
+ */
+int fa_shutdown(void);
 
 /* Human-readable name of a status code (static string). */
 const char *fa_status_string(int status);

@@ -159,3 +159,30 @@ def test_product_package_does_not_import_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "oracle." not in src.replace(
                     "the oracle", ""), f
+
+
+def test_shutdown_without_a_gpu_is_ok(lib):
+    # fa_shutdown only drops cached host-side values: no CUDA call is made
+    assert fa.fa_shutdown() == fa.FA_OK
+    assert fa.fa_shutdown() == fa.FA_OK
+
+
+def _call_noalloc(num_splits=4, **kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=None, B=1, Hq=2, Hkv=2, Sq=8, Sk=8, D=64,
+                scale=0.125, causal=0, cu_seqlens_q=None, cu_seqlens_k=None, stream=None,
+                dtype=fa.FA_DTYPE_BF16)
+    args.update(kw)
+    return fa.fa_fwd_split_noalloc(**args, window_left=-1, window_right=-1, softcap=0.0,
+                                   alibi_slopes=None, num_splits=num_splits)
+
+
+@pytest.mark.parametrize("bad", [dict(B=-1), dict(Hq=3, Hkv=2), dict(D=0), dict(q=8),
+                                 dict(num_splits=-1), dict(num_splits=129)])
+def test_no_alloc_checks_arguments_before_any_cuda_call(lib, bad):
+    # argument errors come back as such, before the fixed array is looked up
+    assert _call_noalloc(**bad) == fa.FA_ERR_INVALID_ARG
+
+
+def test_no_alloc_empty_problem_is_a_no_op(lib):
+    assert _call_noalloc(B=0) == fa.FA_OK
+    assert _call_noalloc(Sq=0) == fa.FA_OK

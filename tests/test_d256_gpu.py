@@ -15,7 +15,7 @@ if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines t
 
 import exact_attention_forward_sm_gb300 as fa  # noqa: E402
 from exact_attention_forward_sm_gb300 import workloads as wl  # noqa: E402
-from tests.gpu_util import check, run_gpu, sample_rows  # noqa: E402
+from tests.gpu_util import check, run_gpu  # noqa: E402
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -95,8 +95,9 @@ def test_d256_deterministic():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_d256_full_size_sampled_rows():
-    """b2 h16 s4096 d256 bf16 causal in the benchmark's launch configuration."""
+def test_d256_full_size_all_rows():
+    """b2 h16 s4096 d256 bf16 causal in the benchmark's launch configuration,
+    every row against the oracle."""
     case = wl.make_workload(wl.BY_NAME["b2_h16_s4096_d256_bf16_causal"])
     o, lse = run_gpu(case)
-    check(case, o, lse, rows=sample_rows(case, per_head=64, seed=9), tag="d256 full size")
+    check(case, o, lse, tag="d256 full size")

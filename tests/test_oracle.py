@@ -310,6 +310,37 @@ def test_rising_bias_workload_exercises_skip_and_rescale():
     np.testing.assert_allclose(lse, lse_n, rtol=1e-12, atol=1e-9)
 
 
+def test_rising_bias_named_workload_exercises_skip_and_rescale():
+    """The named rising-bias workload itself (B2 Hq32 Hkv8 S4096 D128 bf16
+    causal, its bias carried in bf16 channel D-1) gives both outcomes of the
+    threshold-8 decision, walked in ascending 128-key blocks: a row sample over
+    every (batch, head) pair records skipped and performed rescales, P stays
+    <= 256 (v1.7 notes 1.2: threshold 8 with lagging bounds P by 2^8), and the
+    online path equals the plain definition on those rows."""
+    w = wl.BY_NAME["b2_hq32_hkv8_s4096_d128_bf16_causal_risingbias"]
+    case = wl.make_workload(w)
+    assert (case.B, case.Hq, case.Hkv, case.Sq, case.D, case.dtype) == (2, 32, 8, 4096, 128,
+                                                                      "bf16")
+    rng = np.random.default_rng(3)
+    rows = []
+    for b in range(case.B):
+        for h in range(case.Hq):
+            i = np.unique(np.concatenate([[0, 127, 128, 4095],
+                                          rng.integers(0, case.Sq, size=12)]))
+            rows.append(oracle.row_index_dense(b, h, i, case.Hq, case.Sq))
+    all_rows = np.concatenate(rows)
+    o_n, lse_n = _run(case, rows=all_rows)
+    o, lse, st = _run_online(case, rows=all_rows, block_n=128, threshold=8.0, lagging=True)
+    assert st["skips"] > 0 and st["rescales"] > 0, st
+    assert 1.0 < st["max_p"] <= 256.0, st
+    np.testing.assert_allclose(o, o_n, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_n, rtol=1e-12, atol=1e-9)
+    # each (batch, head) pair on its own sees both outcomes as well
+    for r in rows:
+        _, _, st_p = _run_online(case, rows=r, block_n=128, threshold=8.0, lagging=True)
+        assert st_p["skips"] > 0 and st_p["rescales"] > 0, (r[:2], st_p)
+
+
 def test_negative_control_keep_new_max_fails_the_gate():
     """The superseded skip rule (keep the new max) must fail the bf16 gate on
     the rising-bias inputs, so the suite can see the bug max lagging fixes."""

@@ -20,7 +20,7 @@ if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines t
 
 import exact_attention_forward_sm_gb300 as fa  # noqa: E402
 from exact_attention_forward_sm_gb300 import workloads as wl  # noqa: E402
-from tests.gpu_util import check, run_gpu, sample_rows, to_device  # noqa: E402
+from tests.gpu_util import check, run_gpu, to_device  # noqa: E402
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -97,16 +97,16 @@ def test_packed_gqa_unequal_lengths_noncausal():
 
 @pytest.mark.parametrize("idx", range(len(wl.WORKLOADS)), ids=[w.name for w in wl.WORKLOADS])
 def test_named_workload_full_size(idx):
+    """Each of the five named workloads at full size, in the launch
+    configuration the benchmark times, against the oracle on EVERY output row
+    (the fp64 oracle takes seconds to about a minute and a half on 16 host
+    cores for the largest one)."""
     w = wl.WORKLOADS[idx]
     case = wl.make_workload(w)
     o, lse = run_gpu(case)
-    if case.lse_rows() <= 300_000 and case.Sq <= 4096 and w.D * case.lse_rows() < 2e8 \
-            and idx <= 1:
-        check(case, o, lse, tag=w.name)  # every row
-    else:
-        heads = range(case.Hq) if case.Hq <= 8 else [0, 1, case.Hq // 2, case.Hq - 1]
-        rows = sample_rows(case, per_head=512, heads=heads, seed=idx)
-        check(case, o, lse, rows=rows, tag=w.name)
+    # every row of these workloads sees at least one key: O and LSE finite
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all(), w.name
+    check(case, o, lse, tag=w.name)
 
 
 # ---------------------------------------------------------- properties / edges

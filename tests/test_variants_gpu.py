@@ -22,7 +22,7 @@ if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines t
 
 import exact_attention_forward_sm_gb300 as fa  # noqa: E402
 from exact_attention_forward_sm_gb300 import workloads as wl  # noqa: E402
-from tests.gpu_util import check, run_gpu, sample_rows, to_device  # noqa: E402
+from tests.gpu_util import check, run_gpu, to_device  # noqa: E402
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -119,12 +119,11 @@ def test_variants_off_match_plain_bitwise():
     assert torch.equal(o0, o1) and torch.equal(l0, l1)
 
 
-def test_window_full_size_sampled_rows():
+def test_window_full_size_all_rows():
     """A sliding-window causal problem at the size of the causal benchmark
     (b4 h16 s2048 d128 bf16) with ALiBi, in the benchmark's launch
-    configuration; sampled rows against the oracle."""
+    configuration; every row against the oracle."""
     case = wl.make_case(4, 16, 16, 2048, 2048, 128, "bf16", True, seed=1101,
                         window=(256, 0), alibi_slopes=wl.alibi_slopes_geometric(16))
     o, lse = run_gpu(case)
-    rows = sample_rows(case, per_head=96, seed=3)
-    check(case, o, lse, rows=rows, tag="window256 alibi b4h16s2048")
+    check(case, o, lse, tag="window256 alibi b4h16s2048")

@@ -12,7 +12,7 @@ if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines t
 
 import exact_attention_forward_sm_gb300 as fa  # noqa: E402
 from exact_attention_forward_sm_gb300 import workloads as wl  # noqa: E402
-from tests.gpu_util import check, sample_rows, to_device  # noqa: E402
+from tests.gpu_util import check, to_device  # noqa: E402
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -25,8 +25,8 @@ def _built():
 def _call(fn, case, num_splits, stream):
     q, k, v, cu_q, cu_k = to_device(case)
     o = torch.full_like(q, float("nan"))
-    lse = torch.full((case.B, case.Hq, case.Sq), float("nan"), dtype=torch.float32,
-                     device=q.device)
+    shape = (case.Hq, case.Sq) if case.varlen else (case.B, case.Hq, case.Sq)
+    lse = torch.full(shape, float("nan"), dtype=torch.float32, device=q.device)
     st = fn(q, k, v, o, lse, case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D, case.scale,
             int(case.causal), cu_q, cu_k, stream, wl.DTYPE_CODE[case.dtype],
             num_splits=num_splits)
@@ -50,7 +50,7 @@ def test_two_calls_in_a_row_match_the_allocating_entry_point(num_splits):
     for case, (st0, o0, l0), (st1, o1, l1) in zip(cases, ref, got):
         assert st0 == fa.FA_OK and st1 == fa.FA_OK
         assert torch.equal(o0, o1) and torch.equal(l0, l1)
-        check(case, o1, l1, rows=sample_rows(case, per_head=32, seed=1), tag="noalloc")
+        check(case, o1, l1, tag="noalloc")
 
 
 def test_oversize_is_rejected_with_nothing_launched():
@@ -71,4 +71,39 @@ def test_unsplit_call_needs_no_scratch():
     st0, o0, l0 = _call(fa.fa_fwd_split, case, 1, stream)
     st1, o1, l1 = _call(fa.fa_fwd_split_noalloc, case, 1, stream)
     assert st0 == st1 == fa.FA_OK
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+
+
+def test_splits_without_keys_overwrite_stale_partials():
+    """A split that sees no key must still write its slot (weight zero) even
+    though an earlier call left finite partials in the shared array: first a
+    call that fills the array, then one with more splits than key tiles, and a
+    packed problem whose sequences have very different key counts."""
+    stream = torch.cuda.current_stream()
+    filler = wl.make_case(1, 8, 8, 256, 8192, 128, "bf16", False, seed=45)
+    st, _, _ = _call(fa.fa_fwd_split_noalloc, filler, 8, stream)
+    assert st == fa.FA_OK
+    cases = [
+        (wl.make_case(1, 2, 2, 200, 300, 128, "bf16", False, seed=46), 16),  # 3 K/V tiles
+        (wl.make_case(0, 4, 2, 0, 0, 64, "fp16", True, seed=47,
+                      seqlens_q=[1, 130, 64, 0, 300], seqlens_k=[900, 130, 2000, 5, 301]), 6),
+    ]
+    for case, splits in cases:
+        st0, o0, l0 = _call(fa.fa_fwd_split, case, splits, stream)
+        st1, o1, l1 = _call(fa.fa_fwd_split_noalloc, case, splits, stream)
+        assert st0 == fa.FA_OK and st1 == fa.FA_OK
+        assert fa.fa_get_device_error(stream) == fa.FA_OK
+        assert torch.equal(o0, o1) and torch.equal(l0, l1)
+        check(case, o1, l1, tag=f"noalloc split{splits} after a filled array")
+
+
+def test_shutdown_then_no_alloc_call_sets_up_again():
+    """fa_shutdown() drops the cached array address; the next call looks it up
+    again and still matches the allocating path."""
+    stream = torch.cuda.current_stream()
+    case = wl.make_case(1, 8, 8, 256, 4096, 64, "bf16", True, seed=48)
+    _, o0, l0 = _call(fa.fa_fwd_split, case, 4, stream)
+    assert fa.fa_shutdown() == fa.FA_OK
+    st, o1, l1 = _call(fa.fa_fwd_split_noalloc, case, 4, stream)
+    assert st == fa.FA_OK and fa.fa_get_device_error(stream) == fa.FA_OK
     assert torch.equal(o0, o1) and torch.equal(l0, l1)
