@@ -294,7 +294,7 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(softcap) || softcap < 0.f) return FA_ERR_INVALID_ARG;
-  const float cap_k = softcap > 0.f ? 2.f * scale * 1.4426950408889634f / softcap : 0.f;
+  const float cap_k = softcap > 0.f ? scale / softcap : 0.f;
   if (!std::isfinite(cap_k)) return FA_ERR_INVALID_ARG;
   if (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)) return FA_ERR_INVALID_ARG;
   const bool varlen = cu_seqlens_q != nullptr;
@@ -443,7 +443,7 @@ int forward_kvcache(const void *q, const void *k_cache, const void *v_cache, voi
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(softcap) || softcap < 0.f) return FA_ERR_INVALID_ARG;
-  const float cap_k = softcap > 0.f ? 2.f * scale * 1.4426950408889634f / softcap : 0.f;
+  const float cap_k = softcap > 0.f ? scale / softcap : 0.f;
   if (!std::isfinite(cap_k)) return FA_ERR_INVALID_ARG;
   if (num_splits < 0 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
   if (page_rows <= 0) return FA_ERR_INVALID_ARG;

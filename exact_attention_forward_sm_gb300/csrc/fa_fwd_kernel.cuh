@@ -20,7 +20,9 @@
 //   warp  8     TMEM allocation; lane 0 issues tile 0's tcgen05.mma
 //   warp  9     lane 0 issues every TMA load
 //   warp  10    lane 0 issues tile 1's tcgen05.mma
-//   warp  11    idle
+//   warp  11    zeroes the V rows past a sequence's last key in the last K/V
+//               tile of a unit (packed sequences, KV caches), where the tile
+//               reads other data
 // After set-up the third warpgroup gives registers back (setmaxnreg) so the
 // softmax warpgroups can hold a full 128-column score row: 2 x 128 x 192 +
 // 128 x 96 = 61440 <= 384 x 168 registers granted at launch.
@@ -74,6 +76,7 @@ constexpr int kThreads = 384;
 constexpr int kMmaWarp = 8;   // issues tile 0's MMAs (and owns the TMEM allocation)
 constexpr int kTmaWarp = 9;
 constexpr int kMmaWarp2 = 10; // issues tile 1's MMAs
+constexpr int kFixWarp = 11;  // zeroes V rows past a sequence's keys
 constexpr int kTmemCols = 512;
 constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 64 elements x 2 bytes
 
@@ -122,7 +125,7 @@ struct FwdParams {
   int win_l, win_r;         // local window around the diagonal, -1 = unbounded;
                             // a causal mask arrives here as win_r = 0
   int reverse_rows;         // later row blocks see more keys: schedule them first
-  float cap_k;              // soft cap c: 2 * scale * log2(e) / c, 0 = no soft cap
+  float cap_k;              // soft cap c: scale / c, 0 = no soft cap
   float cap_l2;             // soft cap c: c * log2(e)
   const float *alibi;       // ALiBi slope per query head (natural-log units) or null
   // split-KV (instances with score variants only): each unit of the problem
@@ -185,7 +188,9 @@ constexpr int kTraceEntries = 2048;
   } while (0)
 #endif
 
-template <int D, bool KVC = false>
+// FIX: the kernel reads K/V tiles that may reach past a sequence's keys into
+// other data (packed sequences, KV caches) and carries the v_fixed barriers.
+template <int D, bool KVC = false, bool FIX = false>
 struct Smem {
   static constexpr int kChunks = D / 64;                    // 64-element swizzle chunks
   static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
@@ -201,8 +206,8 @@ struct Smem {
   static constexpr uint32_t kStageOff = kKVOff + kStages * kTileBytes;
   static constexpr uint32_t kBarOff = kStageOff + (KVC ? 2048 : 2 * kChunkBytes);
   // barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2],
-  //           p_half[2][2], o_ready[2], o_free[2], drain
-  static constexpr int kNumBars = 4 + 2 * kStages + 11;
+  //           p_half[2][2], o_ready[2], o_free[2], drain, v_fixed[S] (FIX)
+  static constexpr int kNumBars = 4 + (FIX ? 3 : 2) * kStages + 11;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -479,6 +484,19 @@ __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
   return w;
 }
 
+// Keys of the unit's last K/V tile that belong to the sequence, when the tile
+// reaches past the sequence's last key into memory that holds other data --
+// the next packed sequence, or cache rows past the cached length -- and 0
+// otherwise (dense problems: rows past the tensor read as zero).  Masked keys
+// get P = 0, but 0 * Inf or 0 * NaN in O += P V would still be NaN, so those
+// V rows are zeroed in shared memory before the tile is used.
+template <bool VARLEN, bool KVC>
+__device__ __forceinline__ int v_tail_rows(const Work &w) {
+  if (!(VARLEN || KVC) || !w.valid || w.n_max == 0) return 0;
+  const int valid = w.lk - (w.kv_ub + w.n_max - 1) * kBlockN;
+  return valid < kBlockN ? valid : 0;
+}
+
 // Field of tile t of a Work record.  The tile index of a role is a run-time
 // value; indexing the record's arrays with it would place the whole record in
 // local memory (a round trip to L2 at every unit, since shared memory leaves
@@ -531,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams p) {
-  using L = Smem<D, KVC>;
+  using L = Smem<D, KVC, VARLEN || KVC>;
   using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -548,13 +566,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto o_ready = [&](int t) { return bar0 + 8u * (10 + 2 * L::kStages + t); };
   auto o_free = [&](int t) { return bar0 + 8u * (12 + 2 * L::kStages + t); };
   const uint32_t drain_bar = bar0 + 8u * (14 + 2 * L::kStages);
+  // the V tile in ring slot s has had its rows past the sequence's keys zeroed
+  auto v_fixed = [&](int s) { return bar0 + 8u * (15 + 2 * L::kStages + s); };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
   volatile int *mma_turn = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 8);
-  // K/V loads the producer has issued (KV-cache units): an issuer waits on a
+  // K/V loads the producer has issued: a role that may run ahead of the ring
+  // (the free-running issuers of KV-cache units, the V-row fixer) waits on a
   // ring slot's barrier only once its load is issued, so it never waits a
-  // whole lap ahead of the slot (the free-running issuers of KV-cache units
-  // share slots, and an mbarrier parity wait cannot tell laps k and k - 2 apart)
+  // whole lap ahead of the slot (an mbarrier parity wait cannot tell laps k
+  // and k - 2 apart)
   volatile int *kv_issued = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 12);
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
 
@@ -577,6 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 2);  // one release per query tile
+      if (VARLEN || KVC) mbar_init(v_fixed(s), 1);
     }
     mbar_init(drain_bar, 2);      // one per MMA issuer
     *mma_turn = 0;
@@ -652,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           which == 0 ? &tm_k : &tm_v, kv_full(s), c * 64, w.hkv, k_row, k_b,
                           pol_kv);
             issued = idx + 1;
-            if (KVC) *kv_issued = issued;
+            if (VARLEN || KVC) *kv_issued = issued;
           };
           if constexpr (KVC) {
             // K runs one tile ahead of V: K0, K1, V0, K2, V1, ..., K(n-1), V(n-2),
@@ -794,12 +816,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_used = 0;  // Q tiles consumed
       int p_seen = 0;  // P tiles consumed (p_half phases)
       int o_done = 0;  // finished O accumulations (o_ready / o_free phases)
+      uint32_t vpar = 0;  // bit s: phase parity of v_fixed(s)
       bool ok = true;
       for (int i = 0; ok; ++i) {
         const int unit = unit_of(i);
         if (unit >= p.total_units) break;
         const Work w = (KVC ? decode_work_kvc(p, unit, lane) : decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane));
         if (!w.valid || w.n_max == 0) continue;
+        // the unit's last load is a V tile whose rows past the sequence's keys
+        // are zeroed by the fixer warp: whoever reads it also waits for that
+        // (each issuer tracks every fix's phase, read or not)
+        const bool vfix = v_tail_rows<VARLEN, KVC>(w) > 0;
+        const int fix_idx = vfix ? used + 2 * w.n_max - 1 : -1;
+        const int fix_slot = vfix ? fix_idx % L::kStages : 0;
+        const uint32_t fix_par = (vpar >> fix_slot) & 1u;
+        if (vfix) vpar ^= 1u << fix_slot;
         if (lane == 0 && KVC) {
           // KV-cache units: each tile owns every other load and the tensor
           // pipe is far from busy, so the issuers run free (no turns), and
@@ -822,6 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kidx = used + kpos(u), vidx = used + vpos(u - 2);
             if (jq >= 1) {
               ok = issued_past(vidx) && wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
+                   (vidx != fix_idx || wait(v_fixed(fix_slot), fix_par)) &&
                    (jq > 1 || o_done == 0 || wait(o_free(T), (o_done - 1) & 1)) &&
                    wait_p(0, p_seen & 1);
               if (!ok) break;
@@ -879,6 +911,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // trip that now hides behind the wait for this tile's softmax
             if (ok && pv)
               ok = wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
+                   (vidx != fix_idx || wait(v_fixed(fix_slot), fix_par)) &&
                    (jq > 1 || o_done == 0 || wait(o_free(T), (o_done - 1) & 1));
             if (ok && qk) ok = wait(kv_full(kidx % L::kStages), kv_par(kidx));
             if (ok && pv) ok = wait_p(0, p_seen & 1);
@@ -923,6 +956,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(drain_bar);
         wait_bar(drain_bar, 0, abort_flag, limit, p.status, false);
       }
+    } else if (warp == kFixWarp && (VARLEN || KVC)) {
+      // ------------------------------------------------- V rows past the keys
+      // For each unit whose last K/V tile reaches past the sequence's keys:
+      // once that V tile has landed, zero its rows past the last key (whole
+      // 128-byte rows of each 64-column chunk, so the swizzle does not
+      // matter), make the writes visible to the tensor core's proxy and
+      // signal v_fixed of the slot.  The issuers hold the slot until then.
+      int used = 0;
+      bool ok = true;
+      for (int i = 0; ok; ++i) {
+        const int unit = unit_of(i);
+        if (unit >= p.total_units) break;
+        const Work w = (KVC ? decode_work_kvc(p, unit, lane) : decode_work<CAUSAL, VARLEN, EXT>(p, unit, lane));
+        if (!w.valid || w.n_max == 0) continue;
+        const int valid = v_tail_rows<VARLEN, KVC>(w);
+        if (valid > 0) {
+          const int idx = used + 2 * w.n_max - 1;  // ring index of the unit's last V load
+          const int s = idx % L::kStages;
+          // wait for the producer to issue the load (never a lap ahead of the
+          // slot), then for the load itself
+          const long long t0 = clock64();
+          while (ok && *kv_issued <= idx) {
+            __nanosleep(256);  // far ahead of the load: sleep, keep issue slots free
+            if (*abort_flag) ok = false;
+            if (clock64() - t0 > limit) {
+              record_status(p.status, 4);
+              *abort_flag = 1;
+              ok = false;
+            }
+          }
+          ok = __all_sync(0xffffffffu, ok && wait(kv_full(s), (idx / L::kStages) & 1));
+          if (ok) {
+            const uint32_t tile = sbase + L::kKVOff + s * L::kTileBytes;
+#pragma unroll 1
+            for (int c = 0; c < L::kChunks; ++c)
+#pragma unroll 1
+              for (uint32_t b = (uint32_t)valid * 128u + lane * 16u; b < kChunkBytes; b += 512u)
+                st_shared_v4(tile + c * kChunkBytes + b, 0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(v_fixed(s));
+          }
+        }
+        used += 2 * w.n_max;
+      }
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
@@ -938,7 +1016,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // first, and so does the KV-cache path, whose two-tile merge works in log2
     // units
     const bool raw_scores = !EXT || (!KVC && p.cap_k == 0.f && p.alibi == nullptr);
-    const float scale_log2 = raw_scores ? p.scale_log2 : 1.f;
+    // a soft cap alone keeps tanh(scale s / c) as the score and folds its
+    // factor c log2(e) into the exps, as the plain path folds scale log2(e)
+    const bool cap_folded = EXT && !KVC && p.cap_k != 0.f && p.alibi == nullptr;
+    const float scale_log2 = raw_scores ? p.scale_log2 : (cap_folded ? p.cap_l2 : 1.f);
     const float neg_thr = -p.threshold;
     // every lane of a warp must agree before the warp-wide tcgen05.ld / st
     auto warp_wait = [&](uint32_t bar, uint32_t parity) {
@@ -985,15 +1066,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         FA_TRACE_AT(tr, (t * 64 + j) * 8 + 1);
         const int k0 = (EXT ? kv_begin + (KVC ? 2 * j : j) : j) * kBlockN;
         if constexpr (EXT) {
-          // scores in log2 units: soft cap c tanh(scale s / c), written as
-          // c (1 - 2 / (1 + e^(2 scale s / c))) with the hardware exp2 and
-          // reciprocal, then the ALiBi penalty -slope |diag - key|
+          // scores in log2 units: soft cap c tanh(scale s / c) with the
+          // hardware tanh (one special-function op per score next to the
+          // softmax's exp2), then the ALiBi penalty -slope |diag - key|
           const int last_row = min(m0 + (KVC ? p.tok_per_tile : kBlockM), lq) - 1;
-          if (p.cap_k != 0.f) {
+          if (cap_folded) {
+            const float ck = p.cap_k;
+#pragma unroll
+            for (int c = 0; c < kBlockN; ++c) s[c] = tanh_approx(s[c] * ck);
+          } else if (p.cap_k != 0.f) {
             const float ck = p.cap_k, cl = p.cap_l2;
 #pragma unroll
-            for (int c = 0; c < kBlockN; ++c)
-              s[c] = fmaf(rcp_approx(1.f + ex2(s[c] * ck)), -2.f * cl, cl);
+            for (int c = 0; c < kBlockN; ++c) s[c] = cl * tanh_approx(s[c] * ck);
           } else if (!raw_scores && !p.alibi) {
             const float sl2 = p.scale_log2;
 #pragma unroll

@@ -20,12 +20,17 @@
 //     S = Q K(j+1)^T as sixteen M128 N128 K16 steps.
 // The K/V ring holds one K and one V tile (64 KB each).  The epilogue adds the
 // two partial row sums through shared memory; each warpgroup normalises and
-// stores its 128 columns of O.
+// stores its 128 columns of O.  For packed sequences warp 10 zeroes the V rows
+// of a unit's last K/V tile that lie past the sequence's last key (they hold
+// the next sequence's data) before that tile is used.
 #pragma once
 
 #include "fa_launch.cuh"
 
 namespace fa {
+
+// 384 threads: two softmax warpgroups and one control warpgroup.
+constexpr int kWideThreads = 384;
 
 struct SmemWide {
   static constexpr int kChunks = 4;                          // 256 / 64
@@ -39,15 +44,15 @@ struct SmemWide {
   static constexpr uint32_t kXchOff = kStageOff + 2 * kChunkBytes;
   static constexpr uint32_t kBarOff = kXchOff + 2 * 128 * 4;
   // barriers: q_full, q_empty, kv_full[2], kv_empty[2], s_full, p_half[2],
-  //           o_ready, o_free, drain
-  static constexpr int kNumBars = 12;
+  //           o_ready, o_free, drain, v_fixed[2]
+  static constexpr int kNumBars = 14;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
 template <bool BF16, bool CAUSAL, bool VARLEN, bool EXT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kWideThreads, 1)
     fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -66,8 +71,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_full = bar0 + 8u * 6;
   auto p_half = [&](int h) { return bar0 + 8u * (7 + h); };
   const uint32_t o_ready = bar0 + 8u * 9, o_free = bar0 + 8u * 10, drain_bar = bar0 + 8u * 11;
+  auto v_fixed = [&](int s) { return bar0 + 8u * (12 + s); };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+  // K/V loads the producer has issued (the V-row fixer never waits a lap ahead)
+  volatile int *kv_issued = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 8);
   float *xch = reinterpret_cast<float *>(smem + L::kXchOff);  // [2][128]
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
 
@@ -82,7 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
+      mbar_init(v_fixed(s), 1);
     }
+    *kv_issued = 0;
     mbar_init(s_full, 1);
     mbar_init(p_half(0), 4);  // one arrival per softmax warp of the half
     mbar_init(p_half(1), 4);
@@ -147,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             which == 0 ? &tm_k : &tm_v, kv_full(s), c * 64, w.hkv,
                             w.k_row0 + (w.kv_begin[0] + j) * kBlockN, w.map_b, pol_kv);
               issued = idx + 1;
+              *kv_issued = issued;
             }
           }
         }
@@ -190,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto kv_par = [&](int idx) { return (uint32_t)((idx / L::kStages) & 1); };
       int used = 0, q_used = 0, p_seen = 0, o_done = 0;
+      uint32_t vpar = 0;  // bit s: phase parity of v_fixed(s)
       bool ok = true;
       for (int i = 0; ok; ++i) {
         const int unit = unit_of(i);
@@ -197,6 +209,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Work w = decode_work<CAUSAL, VARLEN, EXT, true>(p, unit, lane);
         const int n = w.n_kv[0];
         if (!w.valid || n == 0) continue;
+        // the unit's last V tile has rows past the sequence's keys: wait
+        // until the fixer warp has zeroed them
+        const bool vfix = v_tail_rows<VARLEN, false>(w) > 0;
+        const int fix_idx = vfix ? used + 2 * n - 1 : -1;
+        const int fix_slot = vfix ? fix_idx % L::kStages : 0;
+        const uint32_t fix_par = (vpar >> fix_slot) & 1u;
+        if (vfix) vpar ^= 1u << fix_slot;
         if (lane == 0) {
           for (int j = 0; j <= n && ok; ++j) {
             const int kidx = used + 2 * j, vidx = used + 2 * j - 1;
@@ -204,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // O += P V(j-1); the unit's first one overwrites O, which the
               // previous unit's epilogue must have read out
               ok = wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
+                   (vidx != fix_idx || wait(v_fixed(fix_slot), fix_par)) &&
                    (j > 1 || o_done == 0 || wait(o_free, (o_done - 1) & 1)) &&
                    wait_bar_spin(p_half(0), p_seen & 1, abort_flag, limit, p.status);
               if (!ok) break;
@@ -244,6 +264,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         // no MMA may still be running when tensor memory is released
         tc_commit(drain_bar);
         wait_bar(drain_bar, 0, abort_flag, limit, p.status, false);
+      }
+    } else if (warp == 10 && VARLEN) {
+      // ------------------------------------------------- V rows past the keys
+      // (see the D <= 128 kernel): zero the rows of a unit's last V tile past
+      // the sequence's last key once it has landed, then signal v_fixed
+      int used = 0;
+      bool ok = true;
+      for (int i = 0; ok; ++i) {
+        const int unit = unit_of(i);
+        if (unit >= p.total_units) break;
+        const Work w = decode_work<CAUSAL, VARLEN, EXT, true>(p, unit, lane);
+        const int n = w.n_kv[0];
+        if (!w.valid || n == 0) continue;
+        const int valid = v_tail_rows<VARLEN, false>(w);
+        if (valid > 0) {
+          const int idx = used + 2 * n - 1;  // ring index of the unit's last V load
+          const int s = idx % L::kStages;
+          const long long t0 = clock64();
+          while (ok && *kv_issued <= idx) {
+            __nanosleep(256);  // far ahead of the load: sleep, keep issue slots free
+            if (*abort_flag) ok = false;
+            if (clock64() - t0 > limit) {
+              record_status(p.status, 4);
+              *abort_flag = 1;
+              ok = false;
+            }
+          }
+          ok = __all_sync(0xffffffffu, ok && wait(kv_full(s), (idx / L::kStages) & 1));
+          if (ok) {
+            const uint32_t tile = sbase + L::kKVOff + s * L::kTileBytes;
+#pragma unroll 1
+            for (int c = 0; c < L::kChunks; ++c)
+#pragma unroll 1
+              for (uint32_t b = (uint32_t)valid * 128u + lane * 16u; b < kChunkBytes; b += 512u)
+                st_shared_v4(tile + c * kChunkBytes + b, 0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(v_fixed(s));
+          }
+        }
+        used += 2 * n;
       }
     }
   } else {
@@ -306,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.cap_k != 0.f) {
             const float ck = p.cap_k, cl = p.cap_l2;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) s[c] = fmaf(rcp_approx(1.f + ex2(s[c] * ck)), -2.f * cl, cl);
+            for (int c = 0; c < 64; ++c) s[c] = cl * tanh_approx(s[c] * ck);
           } else {
             const float sl2 = p.scale_log2;
 #pragma unroll
@@ -480,9 +541,9 @@ template <bool BF16, bool CAUSAL, bool VARLEN, bool EXT>
 cudaError_t launch_wide(const LaunchArgs &a) {
   auto kern = fa_fwd_wide_kernel<BF16, CAUSAL, VARLEN, EXT>;
   static SmemOptIn opt_in;
-  const cudaError_t e = opt_in.ensure(kern, (int)SmemWide::kAlloc, a.device);
+  const cudaError_t e = opt_in.ensure(kern, (int)SmemWide::kAlloc, a.device, 168);
   if (e != cudaSuccess) return e;
-  kern<<<a.grid, kThreads, SmemWide::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
+  kern<<<a.grid, kWideThreads, SmemWide::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
   return cudaGetLastError();
 }
 

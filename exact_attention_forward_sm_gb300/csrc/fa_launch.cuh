@@ -21,13 +21,17 @@ struct LaunchArgs {
 std::atomic<unsigned> &launch_epoch();
 
 // A kernel's opt-in to its large dynamic shared memory, made once per device
-// and epoch: `bits` has bit (device % 64) set once the attribute is set.
+// and epoch: `bits` has bit (device % 64) set once the attribute is set.  The
+// same first launch checks that the kernel was built with `regs` registers
+// per thread: its warp roles trade registers with setmaxnreg on the basis of
+// that launch count, and a different count would leave a role waiting for
+// registers that never come free, so such a build is refused instead.
 struct SmemOptIn {
   std::atomic<unsigned long long> bits{0};
   std::atomic<unsigned> epoch{0};
 
   template <class Kernel>
-  cudaError_t ensure(Kernel kern, int bytes, int device) {
+  cudaError_t ensure(Kernel kern, int bytes, int device, int regs) {
     const unsigned ep = launch_epoch().load(std::memory_order_acquire);
     if (epoch.load(std::memory_order_acquire) != ep) {
       bits.store(0, std::memory_order_release);
@@ -35,8 +39,11 @@ struct SmemOptIn {
     }
     const unsigned long long bit = 1ull << (device & 63);
     if (bits.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    const cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs != regs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess) bits.fetch_or(bit, std::memory_order_acq_rel);
     return e;
   }
@@ -46,9 +53,9 @@ template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT = false, bool KVC
 cudaError_t launch_fwd(const LaunchArgs &a) {
   auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN, EXT, KVC>;
   static SmemOptIn opt_in;
-  const cudaError_t e = opt_in.ensure(kern, (int)Smem<D, KVC>::kAlloc, a.device);
+  const cudaError_t e = opt_in.ensure(kern, (int)Smem<D, KVC, VARLEN || KVC>::kAlloc, a.device, 65536 / kThreads / 8 * 8);
   if (e != cudaSuccess) return e;
-  kern<<<a.grid, kThreads, Smem<D, KVC>::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
+  kern<<<a.grid, kThreads, Smem<D, KVC, VARLEN || KVC>::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
   return cudaGetLastError();
 }
 

@@ -64,10 +64,11 @@ enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 };
  *     cu_seqlens_q / cu_seqlens_k are int32 device arrays of B + 1 prefix
  *     offsets: sequence b owns q rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) and
  *     k/v rows [cu_seqlens_k[b], cu_seqlens_k[b+1]).  Rows of q/o that belong
- *     to no sequence are neither read for any output nor written.  Every k/v row
- *     inside [0, Sk) must hold finite values (a tile of one sequence may read
- *     the first rows of the next one; those keys are masked, their values are
- *     multiplied by an exact zero weight).
+ *     to no sequence are neither read for any output nor written.  A
+ *     sequence's output depends only on its own q/k/v rows: k/v rows of other
+ *     sequences (or of none) may hold any values, Inf and NaN included (a
+ *     tile reaching past a sequence's last key masks those keys and zeroes
+ *     their v rows in shared memory before they are used).
  *
  * Arguments:
  *   q, k, v     inputs (16-byte aligned); k and v may be NULL when Sk == 0.
@@ -187,6 +188,8 @@ int fa_fwd_split(const void *q, const void *k, const void *v, void *o, float *ls
  *     multiple of 128.
  *   cache_seqlens  int32 [B] (device): keys of each sequence, 0 ..
  *     capacity (page_rows without a table, max_blocks * page_rows with one).
+ *     Cache rows past a sequence's length may hold any values, Inf and NaN
+ *     included: they never reach the output.
  * Query token i of sequence b sits at position i + (cache_seqlens[b] - Sq)
  * of its sequence: causal = 1 makes key j visible iff j <= i +
  * cache_seqlens[b] - Sq (the bottom-right diagonal of fa_fwd).  window_left,

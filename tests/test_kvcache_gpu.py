@@ -147,6 +147,49 @@ def test_empty_and_tiny_caches():
     check_kvcache(c, o, lse, True, 0.125, "tiny caches")
 
 
+def _poison_cache_tail(c):
+    """Cache rows past each sequence's length (and pages no sequence uses) hold
+    NaN keys and Inf values; they must never reach the output."""
+    kc, vc, lens = c["kc"].clone(), c["vc"].clone(), c["lens"].tolist()
+    if c["table"] is None:
+        for b, n in enumerate(lens):
+            kc[b, n:] = float("nan")
+            vc[b, n:] = float("inf")
+    else:
+        used = set()
+        pr = c["page_rows"]
+        for b, n in enumerate(lens):
+            for blk in range(c["max_blocks"]):
+                pg = int(c["table"][b, blk])
+                used.add(pg)
+                first = max(0, n - blk * pr)
+                if first < pr:
+                    kc[pg, first:] = float("nan")
+                    vc[pg, first:] = float("inf")
+        for pg in range(kc.shape[0]):
+            if pg not in used:
+                kc[pg] = float("nan")
+                vc[pg] = float("-inf")
+    c = dict(c)
+    c["kc"], c["vc"] = kc, vc
+    return c
+
+
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("D,dtype", [(64, "fp16"), (128, "bf16")])
+def test_cache_rows_past_the_length_hold_nan_and_inf(paged, D, dtype):
+    lens = [1500, 333, 129, 1]
+    if paged:
+        c = make_cache_case(4, 16, 4, 3, D, dtype, lens, page_rows=256, seed=_seed("poison", D))
+    else:
+        c = make_cache_case(4, 16, 4, 3, D, dtype, lens, capacity=1700, seed=_seed("poison", D))
+    c = _poison_cache_tail(c)
+    scale = 1 / math.sqrt(D)
+    for splits in (1, 3):
+        o, lse = run_kvcache(c, True, scale, num_splits=splits)
+        check_kvcache(c, o, lse, True, scale, f"poisoned cache tail paged={paged} D{D} s{splits}")
+
+
 def test_variants_over_paged_cache():
     Hq = 8
     c = make_cache_case(2, Hq, 2, 3, 128, "bf16", [1800, 600], page_rows=128, seed=54,

@@ -168,6 +168,40 @@ def test_nan_canary_outside_tensors_and_sequences():
     check(case, o[:tot].contiguous(), lse[:, :tot].contiguous(), tag="canary")
 
 
+def _poison_packed_rows(t, cu, seqs, values):
+    """Fill the rows of the given packed sequences with the given values in turn."""
+    t = t.clone()
+    for n, b in enumerate(seqs):
+        t[int(cu[b]):int(cu[b + 1])] = values[n % len(values)]
+    return t
+
+
+@pytest.mark.parametrize("D,dtype,causal,splits", [
+    (64, "fp16", True, None), (128, "bf16", True, None), (128, "bf16", False, None),
+    (128, "fp16", True, 3), (256, "bf16", True, None), (256, "bf16", False, None),
+])
+def test_packed_neighbour_keys_hold_inf_and_nan(D, dtype, causal, splits):
+    """Sequences 1 and 3 of a packed batch hold Inf / NaN keys and values.  The
+    other sequences' last K/V tiles reach into those rows; their outputs must
+    still match the oracle (the rows past a sequence's keys are masked and
+    their values zeroed before O += P V; the upstream FA4 beta changelog
+    reports the same hazard as V garbage producing NaN at seqlen_k)."""
+    lens = [300, 129, 1000, 64, 257]
+    case = wl.make_case(0, 4, 2, 0, 0, D, dtype, causal, seed=D + 2 * causal + (splits or 0),
+                        seqlens_q=lens)
+    cu = case.cu_seqlens_k
+    case.k = _poison_packed_rows(case.k, cu, [1, 3], [float("nan"), float("inf")])
+    case.v = _poison_packed_rows(case.v, cu, [1, 3], [float("inf"), float("nan")])
+    o, lse = run_gpu(case, num_splits=splits)
+    clean = [0, 2, 4]
+    starts = case.cu_seqlens_q.tolist()
+    rows = np.concatenate([np.arange(h * case.Sq + starts[b], h * case.Sq + starts[b + 1])
+                           for h in range(case.Hq) for b in clean])
+    tok = np.concatenate([np.arange(starts[b], starts[b + 1]) for b in clean])
+    assert bool(torch.isfinite(o[torch.as_tensor(tok, device=o.device)]).all())
+    check(case, o, lse, rows=rows, tag=f"poisoned neighbours D{D}", whole_tensor=False)
+
+
 def test_bad_seqlens_reported_and_context_survives():
     case = wl.make_case(0, 2, 2, 0, 0, 64, "fp16", False, seed=45, seqlens_q=[64, 64])
     q, k, v, cu_q, cu_k = to_device(case)
