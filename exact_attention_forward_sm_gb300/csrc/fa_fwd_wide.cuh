@@ -2,23 +2,36 @@
 //
 // At D = 256 an O accumulator takes 256 of the 512 tensor-memory columns, so
 // a CTA holds ONE 128-row query tile per unit (the D <= 128 kernel holds two):
-//   tensor memory  S [0, 128)   O [128, 384)
+//   tensor memory  S_even [0, 128)   O [128, 384)   S_odd [384, 512)
 // and both softmax warpgroups work on that tile's rows: warpgroup w owns score
 // columns [64 w, 64 w + 64) (keys of the K/V tile) and O columns
-// [128 w, 128 w + 128).  Per K/V tile j:
+// [128 w, 128 w + 128).  The scores of K/V tiles j and j + 1 go to different
+// buffers, so the MMA thread issues S(j + 1) = Q K(j + 1)^T before O += P(j)
+// V(j) and the tensor pipe works on it while the softmax works on S(j):
+//   S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ...
+// (one tile per unit has no second tile to alternate with).  A rescale of O at
+// tile j waits until O += P(j - 1) V(j - 1) has completed (pv_done).  Per K/V
+// tile j:
 //   * each warpgroup loads its half of S_j, takes its half-row max and hands it
 //     to the other through shared memory (named barrier 3 over 256 threads);
 //     both then hold the same row max and take the same lazy-rescale decision
 //     (threshold 8 log2 units, max lagging, first tile sets the max), so each
 //     rescales its own half of O and its own partial row sum;
-//   * warpgroup w writes P of its 64 keys as 16-bit pairs into S columns
-//     [32 w, 32 w + 32) and signals p_half[w]; warpgroup 1 writes only after
-//     the barrier, i.e. after warpgroup 0 has read its S columns 32-63;
+//   * warpgroup w writes P of its 64 keys as 16-bit pairs into columns
+//     [32 w, 32 w + 32) of the tile's score buffer and signals p_half[b][w]
+//     of that buffer b (the softmax may finish tile j + 1, whose scores are
+//     ready early, before O += P(j) V(j) is issued: full / ready barriers per
+//     buffer keep the phases of consecutive tiles apart);
+//     warpgroup 1 writes only after the barrier, i.e. after warpgroup 0 has
+//     read its S columns 32-63;
 //   * one MMA thread issues O += P V in two halves (keys 0-63 as soon as
 //     warpgroup 0's P is stored, keys 64-127 after warpgroup 1's), each four
 //     M128 N256 K16 steps with P straight from tensor memory, then
-//     S = Q K(j+1)^T as sixteen M128 N128 K16 steps.
-// The K/V ring holds one K and one V tile (64 KB each).  The epilogue adds the
+//     S = Q K(j+2)^T into the same buffer as sixteen M128 N128 K16 steps (the
+//     tensor pipe runs one CTA's MMAs in issue order, so that S is written
+//     after P(j) has been read).
+// The K/V ring holds two 64 KB tiles, loaded in the order the MMAs read them:
+// K(0), K(1), V(0), K(2), V(1), ..., K(n-1), V(n-2), V(n-1).  The epilogue adds the
 // two partial row sums through shared memory; each warpgroup normalises and
 // stores its 128 columns of O.  For packed sequences warp 10 zeroes the V rows
 // of a unit's last K/V tile that lie past the sequence's last key (they hold
@@ -43,9 +56,9 @@ struct SmemWide {
   // half-row maxima / partial row sums exchanged between the warpgroups
   static constexpr uint32_t kXchOff = kStageOff + 2 * kChunkBytes;
   static constexpr uint32_t kBarOff = kXchOff + 2 * 128 * 4;
-  // barriers: q_full, q_empty, kv_full[2], kv_empty[2], s_full, p_half[2],
-  //           o_ready, o_free, drain, v_fixed[2]
-  static constexpr int kNumBars = 14;
+  // barriers: q_full, q_empty, kv_full[2], kv_empty[2], s_full[2], p_half[2][2],
+  //           o_ready, o_free, drain, v_fixed[2], pv_done
+  static constexpr int kNumBars = 18;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -68,10 +81,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const uint32_t q_full = bar0, q_empty = bar0 + 8;
   auto kv_full = [&](int s) { return bar0 + 8u * (2 + s); };
   auto kv_empty = [&](int s) { return bar0 + 8u * (4 + s); };
-  const uint32_t s_full = bar0 + 8u * 6;
-  auto p_half = [&](int h) { return bar0 + 8u * (7 + h); };
-  const uint32_t o_ready = bar0 + 8u * 9, o_free = bar0 + 8u * 10, drain_bar = bar0 + 8u * 11;
-  auto v_fixed = [&](int s) { return bar0 + 8u * (12 + s); };
+  // score buffer b is full / holds P of keys [64 h, 64 h + 64)
+  auto s_full = [&](int b) { return bar0 + 8u * (15 + b); };
+  auto p_half = [&](int b, int h) { return bar0 + 8u * (6 + 2 * b + h); };
+  const uint32_t o_ready = bar0 + 8u * 10, o_free = bar0 + 8u * 11, drain_bar = bar0 + 8u * 12;
+  auto v_fixed = [&](int s) { return bar0 + 8u * (13 + s); };
+  const uint32_t pv_done = bar0 + 8u * 17;  // O += P(j) V(j) has completed
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
   // K/V loads the producer has issued (the V-row fixer never waits a lap ahead)
@@ -93,12 +108,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       mbar_init(v_fixed(s), 1);
     }
     *kv_issued = 0;
-    mbar_init(s_full, 1);
-    mbar_init(p_half(0), 4);  // one arrival per softmax warp of the half
-    mbar_init(p_half(1), 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(p_half(b, 0), 4);  // one arrival per softmax warp of the half
+      mbar_init(p_half(b, 1), 4);
+    }
     mbar_init(o_ready, 1);
     mbar_init(o_free, 8);     // every softmax warp has read its O columns
     mbar_init(drain_bar, 1);
+    mbar_init(pv_done, 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -144,21 +162,27 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                           w.q_row0 + w.m0[0], w.map_b, pol_q);
             ++q_loads;
           }
-          for (int j = 0; j < w.n_kv[0] && ok; ++j) {
-            for (int which = 0; which < 2 && ok; ++which) {
-              const int idx = issued, s = idx % L::kStages;
-              if (idx >= L::kStages && !wait(kv_empty(s), ((idx / L::kStages) + 1) & 1)) {
-                ok = false;
-                break;
-              }
-              mbar_arrive_expect_tx(kv_full(s), L::kTileBytes);
-              for (int c = 0; c < L::kChunks; ++c)
-                tma_load_4d(sbase + L::kKVOff + s * L::kTileBytes + c * kChunkBytes,
-                            which == 0 ? &tm_k : &tm_v, kv_full(s), c * 64, w.hkv,
-                            w.k_row0 + (w.kv_begin[0] + j) * kBlockN, w.map_b, pol_kv);
-              issued = idx + 1;
-              *kv_issued = issued;
+          // one K or V tile (which: 0 K, 1 V) of unit tile j into the next slot
+          auto issue = [&](int which, int j) {
+            const int idx = issued, s = idx % L::kStages;
+            if (idx >= L::kStages && !wait(kv_empty(s), ((idx / L::kStages) + 1) & 1)) {
+              ok = false;
+              return;
             }
+            mbar_arrive_expect_tx(kv_full(s), L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_4d(sbase + L::kKVOff + s * L::kTileBytes + c * kChunkBytes,
+                          which == 0 ? &tm_k : &tm_v, kv_full(s), c * 64, w.hkv,
+                          w.k_row0 + (w.kv_begin[0] + j) * kBlockN, w.map_b, pol_kv);
+            issued = idx + 1;
+            *kv_issued = issued;
+          };
+          // K runs one tile ahead of V: K(0), K(1), V(0), K(2), V(1), ...
+          const int n = w.n_kv[0];
+          if (ok) issue(0, 0);
+          for (int j = 0; j < n && ok; ++j) {
+            if (j + 1 < n) issue(0, j + 1);
+            if (ok) issue(1, j);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -177,20 +201,22 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       const uint64_t q_desc = make_sdesc_sw128(sbase + L::kQOff, 16, 1024);
       const uint64_t kv_desc0 = make_sdesc_sw128(sbase + L::kKVOff, 16, 1024);
       const uint64_t v_desc0 = make_sdesc_sw128(sbase + L::kKVOff, kChunkBytes, 1024);
-      const uint32_t d_s = tmem, d_o = tmem + 128;
-      auto issue_qk = [&](int kidx) {
+      // score buffer of unit tile j: columns [0, 128) for even j, [384, 512) for odd j
+      auto d_s = [&](int j) { return tmem + ((j & 1) ? 384u : 0u); };
+      const uint32_t d_o = tmem + 128;
+      auto issue_qk = [&](int kidx, uint32_t ds) {
         const uint64_t kd = kv_desc0 + (((kidx % L::kStages) * L::kTileBytes) >> 4);
-        mma_ss(d_s, q_desc, kd, idesc_qk, 0u);
+        mma_ss(ds, q_desc, kd, idesc_qk, 0u);
 #pragma unroll
         for (int kk = 1; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss_acc(d_s, q_desc + off, kd + off, idesc_qk);
+          mma_ss_acc(ds, q_desc + off, kd + off, idesc_qk);
         }
       };
-      // O += P V for keys [64 h, 64 h + 64): P from S columns [32 h, 32 h + 32)
-      auto issue_pv_half = [&](int vidx, int h, bool first) {
+      // O += P V for keys [64 h, 64 h + 64): P from buffer columns [32 h, 32 h + 32)
+      auto issue_pv_half = [&](int vidx, uint32_t ds, int h, bool first) {
         const uint64_t vd = v_desc0 + (((vidx % L::kStages) * L::kTileBytes + h * 4 * 2048) >> 4);
-        const uint32_t a = d_s + h * 32;
+        const uint32_t a = ds + h * 32;
         if (h == 0)
           mma_ts(d_o, a, vd, idesc_pv, first ? 0u : 1u);
         else
@@ -200,7 +226,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           mma_ts_acc(d_o, a + kk * 8, vd + ((kk * 2048) >> 4), idesc_pv);
       };
       auto kv_par = [&](int idx) { return (uint32_t)((idx / L::kStages) & 1); };
-      int used = 0, q_used = 0, p_seen = 0, o_done = 0;
+      int used = 0, q_used = 0, o_done = 0;
+      int p_seen0 = 0, p_seen1 = 0;  // P tiles consumed per score buffer
       uint32_t vpar = 0;  // bit s: phase parity of v_fixed(s)
       bool ok = true;
       for (int i = 0; ok; ++i) {
@@ -217,44 +244,53 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         const uint32_t fix_par = (vpar >> fix_slot) & 1u;
         if (vfix) vpar ^= 1u << fix_slot;
         if (lane == 0) {
-          for (int j = 0; j <= n && ok; ++j) {
-            const int kidx = used + 2 * j, vidx = used + 2 * j - 1;
-            if (j >= 1) {
-              // O += P V(j-1); the unit's first one overwrites O, which the
-              // previous unit's epilogue must have read out
-              ok = wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
-                   (vidx != fix_idx || wait(v_fixed(fix_slot), fix_par)) &&
-                   (j > 1 || o_done == 0 || wait(o_free, (o_done - 1) & 1)) &&
-                   wait_bar_spin(p_half(0), p_seen & 1, abort_flag, limit, p.status);
-              if (!ok) break;
-              tc_fence_after();
-              issue_pv_half(vidx, 0, j == 1);
-              if (!wait_bar_spin(p_half(1), p_seen & 1, abort_flag, limit, p.status)) {
-                ok = false;
-                break;
-              }
-              ++p_seen;
-              tc_fence_after();
-              issue_pv_half(vidx, 1, false);
-              if (j == n) {
-                tc_commit(o_ready);
-                ++o_done;
-              }
-              tc_commit(kv_empty(vidx % L::kStages));
+          // ring positions of the unit's loads (K one tile ahead of V)
+          auto kpos = [&](int j) { return used + (j == 0 ? 0 : 2 * j - 1); };
+          auto vpos = [&](int j) { return used + (j + 1 < n ? 2 * j + 2 : 2 * n - 1); };
+          // S(j) = Q K(j)^T into buffer j % 2
+          auto issue_s = [&](int j) {
+            if (j == 0) {
+              ok = wait(q_full, q_used & 1);
+              ++q_used;
             }
-            if (j < n) {
-              if (j == 0) {
-                ok = wait(q_full, q_used & 1);
-                ++q_used;
-              }
-              ok = ok && wait(kv_full(kidx % L::kStages), kv_par(kidx));
-              if (!ok) break;
-              tc_fence_after();
-              issue_qk(kidx);
-              tc_commit(s_full);
-              if (j == n - 1) tc_commit(q_empty);  // last S of this unit issued
-              tc_commit(kv_empty(kidx % L::kStages));
+            const int kidx = kpos(j);
+            ok = ok && wait(kv_full(kidx % L::kStages), kv_par(kidx));
+            if (!ok) return;
+            tc_fence_after();
+            issue_qk(kidx, d_s(j));
+            tc_commit(s_full(j & 1));
+            if (j == n - 1) tc_commit(q_empty);  // last S of this unit issued
+            tc_commit(kv_empty(kidx % L::kStages));
+          };
+          issue_s(0);
+          if (n > 1 && ok) issue_s(1);
+          for (int j = 0; j < n && ok; ++j) {
+            // O += P(j) V(j); the unit's first one overwrites O, which the
+            // previous unit's epilogue must have read out
+            const int vidx = vpos(j), b = j & 1;
+            int &p_seen = b ? p_seen1 : p_seen0;
+            ok = wait(kv_full(vidx % L::kStages), kv_par(vidx)) &&
+                 (vidx != fix_idx || wait(v_fixed(fix_slot), fix_par)) &&
+                 (j > 0 || o_done == 0 || wait(o_free, (o_done - 1) & 1)) &&
+                 wait_bar_spin(p_half(b, 0), p_seen & 1, abort_flag, limit, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv_half(vidx, d_s(j), 0, j == 0);
+            if (!wait_bar_spin(p_half(b, 1), p_seen & 1, abort_flag, limit, p.status)) {
+              ok = false;
+              break;
             }
+            ++p_seen;
+            tc_fence_after();
+            issue_pv_half(vidx, d_s(j), 1, false);
+            tc_commit(pv_done);
+            if (j == n - 1) {
+              tc_commit(o_ready);
+              ++o_done;
+            }
+            tc_commit(kv_empty(vidx % L::kStages));
+            // S(j + 2) reuses this buffer: the pipe runs it after P(j) is read
+            if (j + 2 < n) issue_s(j + 2);
           }
           used += 2 * n;
         }
@@ -314,9 +350,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const int quarter = warp & 3;   // TMEM lane quarter
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t s_addr = lane_base + wg * 64;         // this half's score columns
-    const uint32_t p_addr = lane_base + wg * 32;         // this half's P columns
-    const uint32_t o_addr = lane_base + 128 + wg * 128;  // this half's O columns
+    // this half's score / P columns in the buffer of unit tile j, O columns
+    auto s_addr = [&](int j) { return lane_base + ((j & 1) ? 384u : 0u) + wg * 64; };
+    auto p_addr = [&](int j) { return lane_base + ((j & 1) ? 384u : 0u) + wg * 32; };
+    const uint32_t o_addr = lane_base + 128 + wg * 128;
     const float scale_log2 = EXT ? 1.f : p.scale_log2;
     const float neg_thr = -p.threshold;
     auto warp_wait = [&](uint32_t bar, uint32_t parity) {
@@ -324,7 +361,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       return __all_sync(0xffffffffu, got);
     };
     float *x_mine = xch + wg * 128, *x_other = xch + (1 - wg) * 128;
-    int s_seen = 0, o_seen = 0;
+    int s_seen0 = 0, s_seen1 = 0, o_seen = 0;  // score tiles consumed per buffer
+    int pv_base = 0;  // O += P V products of earlier units (pv_done phases)
     const bool elected = quarter == 0 && lane == 0;
     const uint32_t stage = sbase + L::kStageOff + wg * kChunkBytes;
     // Both warpgroups meet at named barrier 3 every K/V tile and twice per
@@ -344,17 +382,18 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           (EXT && p.alibi) ? p.alibi[head] * 1.4426950408889634f : 0.f;
       float m = -INFINITY, l = 0.f;  // row max (shared), partial row sum (this half)
       for (int j = 0; j < n_kv; ++j) {
-        bool got = ok && warp_wait(s_full, s_seen & 1);
+        int &s_seen = (j & 1) ? s_seen1 : s_seen0;
+        bool got = ok && warp_wait(s_full(j & 1), s_seen & 1);
         ++s_seen;
         float s[64];
         if (got) {
           tc_fence_after();
           uint32_t sr[32];
-          tmem_ld32(s_addr, sr);
+          tmem_ld32(s_addr(j), sr);
           tmem_wait_ld32(sr);
 #pragma unroll
           for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(sr[c]);
-          tmem_ld32(s_addr + 32, sr);
+          tmem_ld32(s_addr(j) + 32, sr);
           tmem_wait_ld32(sr);
 #pragma unroll
           for (int c = 0; c < 32; ++c) s[32 + c] = __uint_as_float(sr[c]);
@@ -413,16 +452,24 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           }
         }
         if (got && __any_sync(0xffffffffu, rescale)) {
-          // O holds P V up to tile j-1 (S(j) was committed after that PV)
+          // O += P(j-1) V(j-1), issued after S(j), may still be running: wait
+          // until it has completed.  S(j) has completed, so P(j-2) V(j-2) has
+          // too, and the parity names the product's phase unambiguously.
           l *= alpha;
+          if (warp_wait(pv_done, (pv_base + j - 1) & 1)) {
+            tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 128 / 32; ++c) {
-            uint32_t orr[32];
-            tmem_ld32_wait(o_addr + c * 32, orr);
+            for (int c = 0; c < 128 / 32; ++c) {
+              uint32_t orr[32];
+              tmem_ld32_wait(o_addr + c * 32, orr);
 #pragma unroll
-            for (int k = 0; k < 32; ++k)
-              orr[k] = __float_as_uint(__uint_as_float(orr[k]) * alpha);
-            tmem_st32(o_addr + c * 32, orr);
+              for (int k = 0; k < 32; ++k)
+                orr[k] = __float_as_uint(__uint_as_float(orr[k]) * alpha);
+              tmem_st32(o_addr + c * 32, orr);
+            }
+          } else {
+            got = false;
+            ok = false;
           }
         } else if (rescale) {
           l *= alpha;
@@ -431,19 +478,20 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
         if (got) {
-          softmax_chunk<BF16>(s, scale_log2, ms, acc, p_addr);
-          softmax_chunk<BF16>(s + 32, scale_log2, ms, acc, p_addr + 16);
+          softmax_chunk<BF16>(s, scale_log2, ms, acc, p_addr(j));
+          softmax_chunk<BF16>(s + 32, scale_log2, ms, acc, p_addr(j) + 16);
           tmem_st_wait();
           tc_fence_before();
         }
         __syncwarp();
-        if (got && lane == 0) mbar_arrive(p_half(wg));
+        if (got && lane == 0) mbar_arrive(p_half(j & 1, wg));
         if (!got) ok = false;
         add_f32x2(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
         add_f32x2(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
         add_f32x2(acc[0].x, acc[0].y, acc[2].x, acc[2].y);
         l += acc[0].x + acc[0].y;
       }
+      pv_base += n_kv;
       // ------------------------------------------------------------- epilogue
       uint32_t orr[128];
 #pragma unroll
