@@ -4,6 +4,6 @@
 
 namespace fa {
 cudaError_t launch_ext_d256_bf16(const LaunchArgs &a, bool varlen) {
-  return varlen ? launch_wide<true, false, true, true>(a) : launch_wide<true, false, false, true>(a);
+  return varlen ? launch_wide<256, true, false, true, true>(a) : launch_wide<256, true, false, false, true>(a);
 }
 }  // namespace fa

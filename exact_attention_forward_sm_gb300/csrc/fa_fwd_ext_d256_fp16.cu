@@ -4,6 +4,6 @@
 
 namespace fa {
 cudaError_t launch_ext_d256_fp16(const LaunchArgs &a, bool varlen) {
-  return varlen ? launch_wide<false, false, true, true>(a) : launch_wide<false, false, false, true>(a);
+  return varlen ? launch_wide<256, false, false, true, true>(a) : launch_wide<256, false, false, false, true>(a);
 }
 }  // namespace fa

@@ -45,33 +45,38 @@ namespace fa {
 // 384 threads: two softmax warpgroups and one control warpgroup.
 constexpr int kWideThreads = 384;
 
+template <int D>
 struct SmemWide {
-  static constexpr int kChunks = 4;                          // 256 / 64
-  static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;  // 64 KB
-  static constexpr int kStages = 2;                          // one K and one V tile
+  static constexpr int kChunks = D / 64;                     // 64-element swizzle chunks
+  static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kStages = D == 256 ? 2 : 8;           // K/V ring depth
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKVOff = kTileBytes;
-  // output staging for the TMA store, 128 rows x 64 columns per warpgroup
+  // output staging for the TMA store, 128 rows x kStoreCols columns per
+  // warpgroup (128B swizzle for 64 columns, 64B for 32)
+  static constexpr int kStoreCols = D / 2 < 64 ? D / 2 : 64;
+  static constexpr uint32_t kStageBytes = 128u * kStoreCols * 2u;
   static constexpr uint32_t kStageOff = kKVOff + kStages * kTileBytes;
   // half-row maxima / partial row sums exchanged between the warpgroups
-  static constexpr uint32_t kXchOff = kStageOff + 2 * kChunkBytes;
+  static constexpr uint32_t kXchOff = kStageOff + 2 * kStageBytes;
   static constexpr uint32_t kBarOff = kXchOff + 2 * 128 * 4;
-  // barriers: q_full, q_empty, kv_full[2], kv_empty[2], s_full[2], p_half[2][2],
-  //           o_ready, o_free, drain, v_fixed[2], pv_done
-  static constexpr int kNumBars = 18;
+  // barriers: q_full, q_empty, kv_full[S], kv_empty[S], p_half[2][2], o_ready,
+  //           o_free, drain, v_fixed[S], s_full[2], pv_done (S = kStages)
+  static constexpr int kNumBars = 12 + 3 * kStages;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
-template <bool BF16, bool CAUSAL, bool VARLEN, bool EXT>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT>
 __global__ void __launch_bounds__(kWideThreads, 1)
     fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
-  constexpr int D = 256;
-  using L = SmemWide;
+  static_assert(D == 64 || D == 256, "single-tile kernel: head dim 64 or 256");
+  constexpr int DH = D / 2;  // O columns of one warpgroup
+  using L = SmemWide<D>;
   using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -79,14 +84,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::kBarOff;
   const uint32_t q_full = bar0, q_empty = bar0 + 8;
+  // barrier indices: q_full 0, q_empty 1, kv_full [2, 2 + S), kv_empty
+  // [2 + S, 2 + 2S), p_half [2 + 2S, 6 + 2S), o_ready, o_free, drain,
+  // v_fixed [9 + 2S, 9 + 3S), s_full [9 + 3S, 11 + 3S), pv_done (S = ring stages)
+  constexpr int S = L::kStages;
   auto kv_full = [&](int s) { return bar0 + 8u * (2 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (2 + S + s); };
   // score buffer b is full / holds P of keys [64 h, 64 h + 64)
-  auto s_full = [&](int b) { return bar0 + 8u * (15 + b); };
-  auto p_half = [&](int b, int h) { return bar0 + 8u * (6 + 2 * b + h); };
-  const uint32_t o_ready = bar0 + 8u * 10, o_free = bar0 + 8u * 11, drain_bar = bar0 + 8u * 12;
-  auto v_fixed = [&](int s) { return bar0 + 8u * (13 + s); };
-  const uint32_t pv_done = bar0 + 8u * 17;  // O += P(j) V(j) has completed
+  auto s_full = [&](int b) { return bar0 + 8u * (9 + 3 * S + b); };
+  auto p_half = [&](int b, int h) { return bar0 + 8u * (2 + 2 * S + 2 * b + h); };
+  const uint32_t o_ready = bar0 + 8u * (6 + 2 * S), o_free = bar0 + 8u * (7 + 2 * S);
+  const uint32_t drain_bar = bar0 + 8u * (8 + 2 * S);
+  auto v_fixed = [&](int s) { return bar0 + 8u * (9 + 2 * S + s); };
+  const uint32_t pv_done = bar0 + 8u * (11 + 3 * S);  // O += P(j) V(j) has completed
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
   // K/V loads the producer has issued (the V-row fixer never waits a lap ahead)
@@ -353,7 +363,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     // this half's score / P columns in the buffer of unit tile j, O columns
     auto s_addr = [&](int j) { return lane_base + ((j & 1) ? 384u : 0u) + wg * 64; };
     auto p_addr = [&](int j) { return lane_base + ((j & 1) ? 384u : 0u) + wg * 32; };
-    const uint32_t o_addr = lane_base + 128 + wg * 128;
+    const uint32_t o_addr = lane_base + 128 + wg * DH;
     const float scale_log2 = EXT ? 1.f : p.scale_log2;
     const float neg_thr = -p.threshold;
     auto warp_wait = [&](uint32_t bar, uint32_t parity) {
@@ -364,7 +374,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     int s_seen0 = 0, s_seen1 = 0, o_seen = 0;  // score tiles consumed per buffer
     int pv_base = 0;  // O += P V products of earlier units (pv_done phases)
     const bool elected = quarter == 0 && lane == 0;
-    const uint32_t stage = sbase + L::kStageOff + wg * kChunkBytes;
+    const uint32_t stage = sbase + L::kStageOff + wg * L::kStageBytes;
     // Both warpgroups meet at named barrier 3 every K/V tile and twice per
     // unit; like the other kernel, the role never leaves its unit loop early.
     bool ok = true;
@@ -459,7 +469,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           if (warp_wait(pv_done, (pv_base + j - 1) & 1)) {
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < 128 / 32; ++c) {
+            for (int c = 0; c < DH / 32; ++c) {
               uint32_t orr[32];
               tmem_ld32_wait(o_addr + c * 32, orr);
 #pragma unroll
@@ -493,19 +503,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       }
       pv_base += n_kv;
       // ------------------------------------------------------------- epilogue
-      uint32_t orr[128];
+      uint32_t orr[DH];
 #pragma unroll
-      for (int k = 0; k < 128; ++k) orr[k] = 0u;
+      for (int k = 0; k < DH; ++k) orr[k] = 0u;
       if (n_kv > 0 && ok) {
         ok = warp_wait(o_ready, o_seen & 1);
         ++o_seen;
         if (ok) {
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < DH / 32; ++c)
             tmem_ld32(o_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(orr + 32 * c));
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < DH / 32; ++c)
             tmem_wait_ld32(*reinterpret_cast<uint32_t(*)[32]>(orr + 32 * c));
           tc_fence_before();
         }
@@ -532,9 +542,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       if (EXT && p.num_splits > 1) {
         if (row_valid && ok) {
           const int64_t slot = (int64_t)w.split * p.part_rows + li;
-          float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * D + wg * 128);
+          float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * D + wg * DH);
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
+          for (int k = 0; k < DH / 4; ++k)
             dst[k] = make_float4(__uint_as_float(orr[4 * k]) * inv_l,
                                  __uint_as_float(orr[4 * k + 1]) * inv_l,
                                  __uint_as_float(orr[4 * k + 2]) * inv_l,
@@ -542,14 +552,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           if (wg == 0) p.lse_part[slot] = lse;
         }
       } else if (use_tma) {
+        constexpr int kSC = L::kStoreCols;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int half = 0; half < DH / kSC; ++half) {
           named_barrier_sync(1 + wg, 128);  // staging buffer free
           if (ok) {
+            // row `row`, 16-byte chunk c at its swizzled position: 128B
+            // swizzle (64 columns) c ^ (row % 8), 64B swizzle (32 columns)
+            // c ^ ((row / 2) % 4)
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int k = half * 32 + 4 * c;
-              st_shared_v4(stage + row * 128 + ((c ^ (row & 7)) << 4), packed(k), packed(k + 1),
+            for (int c = 0; c < kSC / 8; ++c) {
+              const int k = half * (kSC / 2) + 4 * c;
+              const int sc = kSC == 64 ? (c ^ (row & 7)) : (c ^ ((row >> 1) & 3));
+              st_shared_v4(stage + row * (kSC * 2) + (sc << 4), packed(k), packed(k + 1),
                            packed(k + 2), packed(k + 3));
             }
             fence_proxy_async_smem();
@@ -557,17 +572,17 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           named_barrier_sync(1 + wg, 128);  // staging buffer full
           if (elected) {
             if (ok) {
-              tma_store_4d(&tm_o, stage, wg * 128 + half * 64, head, w.q_row0 + m0, w.map_b);
+              tma_store_4d(&tm_o, stage, wg * DH + half * kSC, head, w.q_row0 + m0, w.map_b);
               bulk_commit_group();
             }
             bulk_wait_group_read0();
           }
         }
       } else if (row_valid && ok) {
-        elem_t *o = reinterpret_cast<elem_t *>(p.o) + (tok * p.Hq + head) * (int64_t)D + wg * 128;
+        elem_t *o = reinterpret_cast<elem_t *>(p.o) + (tok * p.Hq + head) * (int64_t)D + wg * DH;
         uint4 *dst = reinterpret_cast<uint4 *>(o);
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
+        for (int k = 0; k < DH / 8; ++k)
           dst[k] = make_uint4(packed(4 * k), packed(4 * k + 1), packed(4 * k + 2), packed(4 * k + 3));
       }
       if (wg == 0 && row_valid && ok && p.lse != nullptr && !(EXT && p.num_splits > 1))
@@ -585,13 +600,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   }
 }
 
-template <bool BF16, bool CAUSAL, bool VARLEN, bool EXT>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT>
 cudaError_t launch_wide(const LaunchArgs &a) {
-  auto kern = fa_fwd_wide_kernel<BF16, CAUSAL, VARLEN, EXT>;
+  auto kern = fa_fwd_wide_kernel<D, BF16, CAUSAL, VARLEN, EXT>;
   static SmemOptIn opt_in;
-  const cudaError_t e = opt_in.ensure(kern, (int)SmemWide::kAlloc, a.device, 168);
+  const cudaError_t e = opt_in.ensure(kern, (int)SmemWide<D>::kAlloc, a.device, 168);
   if (e != cudaSuccess) return e;
-  kern<<<a.grid, kWideThreads, SmemWide::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
+  kern<<<a.grid, kWideThreads, SmemWide<D>::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o,
+                                                                 a.p);
   return cudaGetLastError();
 }
 
