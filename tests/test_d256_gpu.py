@@ -57,6 +57,17 @@ def test_d256_rising_bias_rescales():
     check(case, o, lse, tag="d256 rising bias")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_d256_rescales_on_many_units_per_cta(causal):
+    """A rescale of O waits for the previous O += P V, which may still run when
+    the next tile's scores are computed ahead: rising-bias scores (rescales on
+    many K/V tiles) over far more units than CTAs, every row against the oracle."""
+    case = wl.make_case(2, 24, 8, 2048, 2048, 256, "bf16", causal, seed=72 + causal,
+                        rising_bias=True)
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag=f"d256 rising bias many units causal={causal}")
+
+
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 def test_d256_packed(dtype):
     case = wl.make_case(0, 4, 2, 0, 0, 256, dtype, True, seed=_seed("packed", dtype),
