@@ -342,6 +342,9 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   const bool ext =
       win_l >= 0 || win_r > 0 || softcap > 0.f || alibi_slopes != nullptr || splits > 1;
   const bool plain_causal = !ext && win_r == 0;
+  // the score variants that are on pick the instance (each carries only
+  // their code)
+  const int var = (softcap > 0.f ? fa::kVarCap : 0) | (alibi_slopes ? fa::kVarAlibi : 0);
   const int64_t units = base_units * splits;
   if (units > 0x7fffffffll) return FA_ERR_UNSUPPORTED;
   const int64_t lse_rows = (int64_t)Hq * Sq * (varlen ? 1 : B);
@@ -386,7 +389,10 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   p.threshold = FA_RESCALE_THRESHOLD;
   p.win_l = win_l;
   p.win_r = win_r;
-  p.reverse_rows = (win_l < 0 && win_r >= 0) ? 1 : 0;
+  // with a right bound (causal included) a later row block sees at least as
+  // many keys as an earlier one, up to the few rows whose right bound is cut
+  // at the last key: schedule the later ones first
+  p.reverse_rows = win_r >= 0 ? 1 : 0;
   p.cap_k = cap_k;
   p.cap_l2 = softcap * 1.4426950408889634f;
   p.alibi = alibi_slopes;
@@ -417,8 +423,8 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
     }
     if (ext) {
       if (D == 64)
-        return bf16 ? fa::launch_ext_d64_bf16(la, varlen) : fa::launch_ext_d64_fp16(la, varlen);
-      return bf16 ? fa::launch_ext_d128_bf16(la, varlen) : fa::launch_ext_d128_fp16(la, varlen);
+        return bf16 ? fa::launch_ext_d64_bf16(la, varlen, var) : fa::launch_ext_d64_fp16(la, varlen, var);
+      return bf16 ? fa::launch_ext_d128_bf16(la, varlen, var) : fa::launch_ext_d128_fp16(la, varlen, var);
     }
     if (D == 64)
       return bf16 ? fa::launch_d64_bf16(la, plain_causal, varlen)

@@ -544,7 +544,14 @@ __device__ __forceinline__ void softmax_chunk(const float *x, float scale_log2, 
   tmem_st16(p_addr, pk);
 }
 
-template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT, bool KVC = false>
+// Score variants an instance with EXT carries code for (window bounds and
+// split-KV always): a soft cap, ALiBi.  Each instance holds only the code of
+// its own variants; the softmax's instruction stream stays short.
+constexpr int kVarCap = 1;
+constexpr int kVarAlibi = 2;
+
+template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT, bool KVC = false,
+          int VAR = kVarCap | kVarAlibi>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -1015,10 +1022,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // into the exps; a soft cap or ALiBi turns every score into log2 units
     // first, and so does the KV-cache path, whose two-tile merge works in log2
     // units
-    const bool raw_scores = !EXT || (!KVC && p.cap_k == 0.f && p.alibi == nullptr);
+    // the variants this instance carries code for (the others are off)
+    const float cap_k = (VAR & kVarCap) ? p.cap_k : 0.f;
+    const float *const alibi = (VAR & kVarAlibi) ? p.alibi : nullptr;
+    const bool raw_scores = !EXT || (!KVC && cap_k == 0.f && alibi == nullptr);
     // a soft cap alone keeps tanh(scale s / c) as the score and folds its
     // factor c log2(e) into the exps, as the plain path folds scale log2(e)
-    const bool cap_folded = EXT && !KVC && p.cap_k != 0.f && p.alibi == nullptr;
+    const bool cap_folded = EXT && !KVC && cap_k != 0.f && alibi == nullptr;
     const float scale_log2 = raw_scores ? p.scale_log2 : (cap_folded ? p.cap_l2 : 1.f);
     const float neg_thr = -p.threshold;
     // every lane of a warp must agree before the warp-wide tcgen05.ld / st
@@ -1052,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int diag = qi + lk - lq;  // last visible key of this row (causal)
       [[maybe_unused]] const int kv_begin = tile_field(w.kv_begin, t);
       [[maybe_unused]] const float slope_l2 =
-          (EXT && p.alibi) ? p.alibi[head] * 1.4426950408889634f : 0.f;
+          (EXT && alibi) ? alibi[head] * 1.4426950408889634f : 0.f;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n_kv && ok; ++j) {
         if (!warp_wait(s_full(t), s_seen & 1)) { ok = false; break; }
@@ -1067,25 +1077,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int k0 = (EXT ? kv_begin + (KVC ? 2 * j : j) : j) * kBlockN;
         if constexpr (EXT) {
           // scores in log2 units: soft cap c tanh(scale s / c) with the
-          // hardware tanh (one special-function op per score next to the
-          // softmax's exp2), then the ALiBi penalty -slope |diag - key|
+          // hardware tanh, then the ALiBi penalty -slope |diag - key|
           const int last_row = min(m0 + (KVC ? p.tok_per_tile : kBlockM), lq) - 1;
           if (cap_folded) {
-            const float ck = p.cap_k;
-#pragma unroll
-            for (int c = 0; c < kBlockN; ++c) s[c] = tanh_approx(s[c] * ck);
-          } else if (p.cap_k != 0.f) {
-            const float ck = p.cap_k, cl = p.cap_l2;
-#pragma unroll
-            for (int c = 0; c < kBlockN; ++c) s[c] = cl * tanh_approx(s[c] * ck);
-          } else if (!raw_scores && !p.alibi) {
+            soft_cap<kBlockN, false>(s, cap_k, 1.f);
+          } else if (cap_k != 0.f) {
+            soft_cap<kBlockN, true>(s, cap_k, p.cap_l2);
+          } else if (!raw_scores && !alibi) {
             const float sl2 = p.scale_log2;
 #pragma unroll
             for (int c = 0; c < kBlockN; ++c) s[c] *= sl2;
           }
-          if (p.alibi) {
+          if (alibi) {
             // after the soft cap the scores are in log2 units already
-            const float mul = p.cap_k != 0.f ? 1.f : p.scale_log2;
+            const float mul = cap_k != 0.f ? 1.f : p.scale_log2;
             const float d0 = (float)(diag - k0);
             const int first_diag = m0 + lk - lq, last_diag = last_row + lk - lq;
             if (k0 + kBlockN - 1 <= first_diag || k0 >= last_diag) {
@@ -1110,11 +1115,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  (p.win_r >= 0 && k0 + kBlockN - 1 > m0 + lk - lq + p.win_r) ||
                                  (p.win_l >= 0 && k0 < last_row + lk - lq - p.win_l);
           if (need_mask) {
-            // keys [lo, hi) of this tile are visible to the row
+            // keys [lo, hi) of this tile are visible to the row; a warp none
+            // of whose rows has its left bound inside the tile (causal, or a
+            // right bound alone) takes the one-sided select
             const int lo = p.win_l < 0 ? 0 : diag - p.win_l - k0;
             const int hi = min(lk, p.win_r < 0 ? lk : diag + p.win_r + 1) - k0;
+            if (__all_sync(0xffffffffu, lo <= 0)) {
 #pragma unroll
-            for (int c = 0; c < kBlockN; ++c) s[c] = (c >= lo && c < hi) ? s[c] : -INFINITY;
+              for (int c = 0; c < kBlockN; ++c) s[c] = (c < hi) ? s[c] : -INFINITY;
+            } else {
+#pragma unroll
+              for (int c = 0; c < kBlockN; ++c) s[c] = (c >= lo && c < hi) ? s[c] : -INFINITY;
+            }
           }
         } else if ((k0 + kBlockN > lk) || (CAUSAL && (k0 + kBlockN - 1 > m0 + lk - lq))) {
           int lim = lk - k0;  // keys [0, lim) of this tile are visible to the row

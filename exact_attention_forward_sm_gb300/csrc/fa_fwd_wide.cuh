@@ -414,9 +414,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         const int k0 = (w.kv_begin[0] + j) * kBlockN + wg * 64;  // first key of this half
         if constexpr (EXT) {
           if (p.cap_k != 0.f) {
-            const float ck = p.cap_k, cl = p.cap_l2;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) s[c] = cl * tanh_approx(s[c] * ck);
+            soft_cap<64, true>(s, p.cap_k, p.cap_l2);
           } else {
             const float sl2 = p.scale_log2;
 #pragma unroll

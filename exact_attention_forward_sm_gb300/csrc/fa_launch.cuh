@@ -49,9 +49,10 @@ struct SmemOptIn {
   }
 };
 
-template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT = false, bool KVC = false>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool EXT = false, bool KVC = false,
+          int VAR = kVarCap | kVarAlibi>
 cudaError_t launch_fwd(const LaunchArgs &a) {
-  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN, EXT, KVC>;
+  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN, EXT, KVC, VAR>;
   static SmemOptIn opt_in;
   const cudaError_t e = opt_in.ensure(kern, (int)Smem<D, KVC, VARLEN || KVC>::kAlloc, a.device, 65536 / kThreads / 8 * 8);
   if (e != cudaSuccess) return e;
@@ -71,12 +72,20 @@ cudaError_t launch_fwd(const LaunchArgs &a) {
                   : launch_fwd<D, BF16, false, false>(a);                       \
   }
 
-// Kernels with score variants (local window, soft cap, ALiBi): causal masking
-// is folded into the window, so only the packed flag selects the instance.
+// Kernels with score variants (local window, split-KV, soft cap, ALiBi):
+// causal masking is folded into the window; the packed flag and the variants
+// that are on (kVarCap / kVarAlibi bits) select the instance.
+#define FA_EXT_INSTANCE(D, BF16, VAR)                                           \
+  (varlen ? launch_fwd<D, BF16, false, true, true, false, VAR>(a)               \
+          : launch_fwd<D, BF16, false, false, true, false, VAR>(a))
 #define FA_DEFINE_EXT_LAUNCHER(NAME, D, BF16)                                   \
-  cudaError_t NAME(const LaunchArgs &a, bool varlen) {                         \
-    return varlen ? launch_fwd<D, BF16, false, true, true>(a)                   \
-                  : launch_fwd<D, BF16, false, false, true>(a);                 \
+  cudaError_t NAME(const LaunchArgs &a, bool varlen, int var) {                \
+    switch (var) {                                                              \
+      case 0: return FA_EXT_INSTANCE(D, BF16, 0);                               \
+      case kVarCap: return FA_EXT_INSTANCE(D, BF16, kVarCap);                   \
+      case kVarAlibi: return FA_EXT_INSTANCE(D, BF16, kVarAlibi);               \
+      default: return FA_EXT_INSTANCE(D, BF16, kVarCap | kVarAlibi);            \
+    }                                                                           \
   }
 
 // KV-cache decoding instances (score variants included).
@@ -87,10 +96,10 @@ cudaError_t launch_d64_fp16(const LaunchArgs &a, bool causal, bool varlen);
 cudaError_t launch_d64_bf16(const LaunchArgs &a, bool causal, bool varlen);
 cudaError_t launch_d128_fp16(const LaunchArgs &a, bool causal, bool varlen);
 cudaError_t launch_d128_bf16(const LaunchArgs &a, bool causal, bool varlen);
-cudaError_t launch_ext_d64_fp16(const LaunchArgs &a, bool varlen);
-cudaError_t launch_ext_d64_bf16(const LaunchArgs &a, bool varlen);
-cudaError_t launch_ext_d128_fp16(const LaunchArgs &a, bool varlen);
-cudaError_t launch_ext_d128_bf16(const LaunchArgs &a, bool varlen);
+cudaError_t launch_ext_d64_fp16(const LaunchArgs &a, bool varlen, int var);
+cudaError_t launch_ext_d64_bf16(const LaunchArgs &a, bool varlen, int var);
+cudaError_t launch_ext_d128_fp16(const LaunchArgs &a, bool varlen, int var);
+cudaError_t launch_ext_d128_bf16(const LaunchArgs &a, bool varlen, int var);
 // Head dim 256 (one query tile per unit, see fa_fwd_wide.cuh).
 cudaError_t launch_d256_fp16(const LaunchArgs &a, bool causal, bool varlen);
 cudaError_t launch_d256_bf16(const LaunchArgs &a, bool causal, bool varlen);

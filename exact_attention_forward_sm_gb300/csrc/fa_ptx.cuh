@@ -369,4 +369,12 @@ __device__ __forceinline__ float tanh_approx(float x) {
   return y;
 }
 
+// Soft cap of a thread's N scores in place: s <- cl tanh(ck s), or tanh(ck s)
+// when the factor cl is folded into the exps (SCALED false).
+template <int N, bool SCALED>
+__device__ __forceinline__ void soft_cap(float *s, float ck, float cl) {
+#pragma unroll
+  for (int c = 0; c < N; ++c) s[c] = SCALED ? cl * tanh_approx(s[c] * ck) : tanh_approx(s[c] * ck);
+}
+
 }  // namespace fa
