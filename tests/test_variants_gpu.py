@@ -83,6 +83,18 @@ def test_softcap_all_rows(causal, cap, sigma):
     check(case, o, lse, tag=f"softcap {cap} sigma {sigma} causal={causal}")
 
 
+@pytest.mark.parametrize("D,dtype", [(64, "fp16"), (64, "bf16")])
+@pytest.mark.parametrize("win", [(-1, -1), (100, 0)])
+def test_softcap_head_dim_64(D, dtype, win):
+    """Each combination of score variants runs its own kernel instance; this
+    one is the soft cap without ALiBi at head dim 64, with and without a
+    window, rows visiting several K/V tiles with a ragged tail."""
+    case = wl.make_case(2, 6, 3, 333, 333, D, dtype, True, seed=_seed(D, dtype, win),
+                        sigma=2.0, softcap=15.0, window=win)
+    o, lse = run_gpu(case)
+    check(case, o, lse, tag=f"softcap D{D} {dtype} window {win}")
+
+
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("sq,sk,D,dtype", [(512, 512, 128, "bf16"), (300, 700, 64, "fp16"),
                                            (700, 300, 128, "fp16")])
