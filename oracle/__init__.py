@@ -15,6 +15,9 @@ independent rows); this module only builds it with gcc and marshals arrays.
 * :func:`attention_online` — the streaming restatement with the lazy-rescale
   threshold and max lagging of the fork's v1.7 release notes (section 1.2),
   plus its skip / rescale counters and the largest P.
+* :func:`attention_bwd` — the gradients dq, dk, dv of the plain definition
+  for an upstream gradient dO (the backward pass of the v1.7 notes, section
+  4.4), the derivative of softmax written out.
 
 Both take the 16-bit inputs as exact float32 copies and address rows by their
 LSE index (dense: ``(b * Hq + h) * Sq + i``; packed: ``h * total_q + t``).
@@ -70,6 +73,11 @@ def _load():
         lib.oracle_attention_online.argtypes = common + [
             c_int, ctypes.c_double, c_int, i64p, i64p, f64p, c_int]
         lib.oracle_attention_online.restype = c_int
+        lib.oracle_attention_bwd.argtypes = [
+            f32p, f32p, f32p, f32p, f64p, f64p, f64p,
+            c_int, c_int, c_int, c_int, c_int, c_int, ctypes.c_double, c_int,
+            i32p, i32p, c_int]
+        lib.oracle_attention_bwd.restype = c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = c_int
         _lib = lib
@@ -181,6 +189,35 @@ def attention_online(q, k, v, B, Hq, Hkv, Sq, Sk, D, scale, causal,
         raise ValueError(f"oracle_attention_online failed with status {rc}")
     return o, lse, {"skips": n_skip.value, "rescales": n_rescale.value,
                     "max_p": max_p.value}
+
+
+def attention_bwd(q, k, v, dout, B, Hq, Hkv, Sq, Sk, D, scale, causal,
+                  cu_seqlens_q=None, cu_seqlens_k=None, nthreads=0):
+    """Gradients of plain-definition attention (fp64) for upstream gradient ``dout``.
+
+    ``q`` / ``dout`` and ``k`` / ``v`` in the layouts of the C ABI (dense or
+    packed).  Returns ``(dq, dk, dv)`` as float64 arrays shaped like ``q``,
+    ``k`` and ``v``.
+    """
+    lib = _load()
+    q, k, v, cu_q, cu_k, _ = _prep(q, k, v, B, Hq, Hkv, Sq, Sk, D,
+                                   cu_seqlens_q, cu_seqlens_k, np.zeros(0, np.int64))
+    do = _as_f32(dout)
+    if do.shape != q.shape:
+        raise ValueError("dout must have the shape of q")
+    dq = np.zeros(q.shape, dtype=np.float64)
+    dk = np.zeros(k.shape, dtype=np.float64)
+    dv = np.zeros(v.shape, dtype=np.float64)
+    i32n = ctypes.POINTER(ctypes.c_int32)()
+    rc = lib.oracle_attention_bwd(
+        _ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float), _ptr(v, ctypes.c_float),
+        _ptr(do, ctypes.c_float), _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
+        _ptr(dv, ctypes.c_double), B, Hq, Hkv, Sq, Sk, D, float(scale), int(bool(causal)),
+        _ptr(cu_q, ctypes.c_int32) if cu_q is not None else i32n,
+        _ptr(cu_k, ctypes.c_int32) if cu_k is not None else i32n, int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd failed with status {rc}")
+    return dq, dk, dv
 
 
 def row_index_dense(b, h, i, Hq, Sq):

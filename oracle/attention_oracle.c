@@ -47,6 +47,19 @@
  *                             oracle_attention() is this function with every
  *                             variant switched off.
  *
+ *  oracle_attention_bwd()     the gradients of the plain definition (the
+ *                             backward pass the fork's v1.7 release notes
+ *                             validate in section 4.4): for a loss with
+ *                             dL/dO = dO, per query row with its visible keys
+ *                             P = softmax(S), S = scale * Q K^T,
+ *                               dV_j += P_j dO,        dP_j = <dO, V_j>,
+ *                               dS_j  = P_j (dP_j - sum_k P_k dP_k),
+ *                               dQ    = scale * sum_j dS_j K_j,
+ *                               dK_j += scale * dS_j Q,
+ *                             the derivative of softmax written out (no
+ *                             blocking, no recomputation tricks); K/V
+ *                             gradients sum over the query heads of a group.
+ *
  * Readings of points the pages leave open: LSE is the natural log over the
  * scaled scores; causal masking with Sq != Sk is aligned bottom-right (key j
  * visible iff j <= i + Lk - Lq); a row with no visible key gets O = 0 and
@@ -308,6 +321,97 @@ int oracle_attention_online(const float *q, const float *k, const float *v,
     if (n_rescale) *n_rescale = rescales;
     if (max_p) *max_p = pmax;
     return bad ? -2 : 0;
+}
+
+/* Gradients of the plain definition (oracle_attention) with respect to q, k
+ * and v for the upstream gradient dout (same layout as the output): dq has
+ * q's layout, dk / dv have k's.  Parallel over (sequence, K/V head) groups,
+ * each of which owns its dk / dv rows.  Rows without visible keys get dq = 0
+ * and add nothing. */
+int oracle_attention_bwd(const float *q, const float *k, const float *v, const float *dout,
+                         double *dq, double *dk, double *dv,
+                         int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                         double scale, int causal,
+                         const int32_t *cu_q, const int32_t *cu_k, int nthreads) {
+    if (check_args(B, Hq, Hkv, Sq, Sk, D, cu_q, cu_k)) return -1;
+    const int group = Hq / Hkv;
+    const int64_t total_q = cu_q ? (int64_t)cu_q[B] : (int64_t)B * Sq;
+    const int64_t total_k = cu_k ? (int64_t)cu_k[B] : (int64_t)B * Sk;
+    memset(dq, 0, (size_t)(total_q * Hq * D) * sizeof(double));
+    memset(dk, 0, (size_t)(total_k * Hkv * D) * sizeof(double));
+    memset(dv, 0, (size_t)(total_k * Hkv * D) * sizeof(double));
+    int64_t max_lk = Sk;
+    if (cu_k) {
+        max_lk = 0;
+        for (int b = 0; b < B; b++)
+            if (cu_k[b + 1] - cu_k[b] > max_lk) max_lk = cu_k[b + 1] - cu_k[b];
+    }
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel
+    {
+        double *p = (double *)malloc((size_t)(max_lk > 0 ? max_lk : 1) * sizeof(double));
+        double *dp = (double *)malloc((size_t)(max_lk > 0 ? max_lk : 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t gid = 0; gid < (int64_t)B * Hkv; gid++) {
+            const int b = (int)(gid / Hkv), g = (int)(gid % Hkv);
+            const int64_t lq = cu_q ? cu_q[b + 1] - cu_q[b] : Sq;
+            const int64_t lk = cu_k ? cu_k[b + 1] - cu_k[b] : Sk;
+            const int64_t q_tok0 = cu_q ? cu_q[b] : (int64_t)b * Sq;
+            const int64_t k_tok0 = cu_k ? cu_k[b] : (int64_t)b * Sk;
+            for (int h = g * group; h < (g + 1) * group; h++) {
+                for (int64_t i = 0; i < lq; i++) {
+                    int64_t n = lk;
+                    if (causal && i + lk - lq + 1 < n) n = i + lk - lq + 1;
+                    if (n <= 0) continue;
+                    const float *qr = q + ((q_tok0 + i) * Hq + h) * (int64_t)D;
+                    const float *dor = dout + ((q_tok0 + i) * Hq + h) * (int64_t)D;
+                    double *dqr = dq + ((q_tok0 + i) * Hq + h) * (int64_t)D;
+                    /* P = softmax of the scaled scores over the visible keys */
+                    double m = -INFINITY;
+                    for (int64_t j = 0; j < n; j++) {
+                        const float *kr = k + ((k_tok0 + j) * Hkv + g) * (int64_t)D;
+                        double acc = 0.0;
+                        for (int d = 0; d < D; d++) acc += (double)qr[d] * (double)kr[d];
+                        p[j] = scale * acc;
+                        if (p[j] > m) m = p[j];
+                    }
+                    double l = 0.0;
+                    for (int64_t j = 0; j < n; j++) {
+                        p[j] = exp(p[j] - m);
+                        l += p[j];
+                    }
+                    /* dP_j = <dO, V_j> and the row's sum_k P_k dP_k */
+                    double delta = 0.0;
+                    for (int64_t j = 0; j < n; j++) {
+                        p[j] /= l;
+                        const float *vr = v + ((k_tok0 + j) * Hkv + g) * (int64_t)D;
+                        double acc = 0.0;
+                        for (int d = 0; d < D; d++) acc += (double)dor[d] * (double)vr[d];
+                        dp[j] = acc;
+                        delta += p[j] * acc;
+                    }
+                    for (int64_t j = 0; j < n; j++) {
+                        const double ds = p[j] * (dp[j] - delta);
+                        const float *kr = k + ((k_tok0 + j) * Hkv + g) * (int64_t)D;
+                        double *dkr = dk + ((k_tok0 + j) * Hkv + g) * (int64_t)D;
+                        double *dvr = dv + ((k_tok0 + j) * Hkv + g) * (int64_t)D;
+                        for (int d = 0; d < D; d++) {
+                            dqr[d] += scale * ds * (double)kr[d];
+                            dkr[d] += scale * ds * (double)qr[d];
+                            dvr[d] += p[j] * (double)dor[d];
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    return 0;
 }
 
 /* Threads the oracle would use by default (for reporting). */
