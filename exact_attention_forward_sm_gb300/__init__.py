@@ -23,8 +23,9 @@ __all__ = [
     "library_path", "load_library", "fa_fwd", "fa_fwd_ex", "fa_fwd_split", "fa_split_plan",
     "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes", "fa_fwd_kvcache", "attention_kvcache", "fa_kvcache_plan",
     "fa_get_device_error", "fa_debug_wait_timeout",
-    "fa_debug_trace_read", "fa_shutdown",
-    "fa_status_string", "fa_version", "attention_forward", "EXPORTED_SYMBOLS",
+    "fa_debug_trace_read", "fa_shutdown", "fa_bwd", "fa_bwd_workspace_bytes",
+    "fa_status_string", "fa_version", "attention_forward", "attention_backward",
+    "EXPORTED_SYMBOLS",
 ]
 
 FA_OK = 0
@@ -41,7 +42,8 @@ EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_split", "fa_split_plan",
                     "fa_fwd_split_noalloc", "fa_noalloc_scratch_bytes", "fa_fwd_kvcache",
                     "fa_kvcache_plan",
                     "fa_get_device_error", "fa_debug_wait_timeout",
-                    "fa_debug_trace_read", "fa_shutdown", "fa_status_string", "fa_version")
+                    "fa_debug_trace_read", "fa_shutdown", "fa_bwd", "fa_bwd_workspace_bytes",
+                    "fa_status_string", "fa_version")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -103,6 +105,11 @@ def load_library():
         lib.fa_debug_wait_timeout.restype = i32
         lib.fa_debug_trace_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i32]
         lib.fa_debug_trace_read.restype = i32
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                               f32, i32, vp, vp, vp, ctypes.c_longlong, vp, i32]
+        lib.fa_bwd.restype = i32
+        lib.fa_bwd_workspace_bytes.argtypes = [i32, i32, i32]
+        lib.fa_bwd_workspace_bytes.restype = ctypes.c_longlong
         lib.fa_shutdown.argtypes = []
         lib.fa_shutdown.restype = i32
         lib.fa_status_string.argtypes = [i32]
@@ -229,6 +236,54 @@ def fa_shutdown() -> int:
     """Drop the library's cached per-device state (status-word and scratch
     addresses, SM counts, shared-memory opt-ins); later calls set it up again."""
     return load_library().fa_shutdown()
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, D, scale, causal,
+           cu_seqlens_q, cu_seqlens_k, workspace, workspace_bytes, stream, dtype) -> int:
+    """Call the C ``fa_bwd`` (gradients dq, dk, dv); returns its status code."""
+    lib = load_library()
+    return lib.fa_bwd(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dout), _addr(dq),
+                      _addr(dk), _addr(dv), int(B), int(Hq), int(Hkv), int(Sq), int(Sk), int(D),
+                      float(scale), int(causal), _addr(cu_seqlens_q), _addr(cu_seqlens_k),
+                      _addr(workspace), int(workspace_bytes), _stream(stream), int(dtype))
+
+
+def fa_bwd_workspace_bytes(B, Hq, Sq) -> int:
+    """Device workspace bytes ``fa_bwd`` needs (or minus a status code)."""
+    return int(load_library().fa_bwd_workspace_bytes(int(B), int(Hq), int(Sq)))
+
+
+def attention_backward(q, k, v, out, lse, dout, causal=False, scale=None, stream=None):
+    """Gradients of exact attention on dense CUDA tensors; returns ``(dq, dk, dv)``.
+
+    q / out / dout [B, Sq, Hq, D], k / v [B, Sk, Hkv, D], lse [B, Hq, Sq] as
+    :func:`attention_forward` returned them.  The workspace is a PyTorch
+    allocation; everything else runs in ``fa_bwd``'s kernels.
+    """
+    import torch
+
+    dtype = {torch.float16: FA_DTYPE_FP16, torch.bfloat16: FA_DTYPE_BF16}.get(q.dtype)
+    if dtype is None:
+        raise FaError(FA_ERR_UNSUPPORTED, "attention_backward (dtype)")
+    for t in (q, k, v, out, lse, dout):
+        if not t.is_contiguous():
+            raise FaError(FA_ERR_INVALID_ARG, "attention_backward (contiguity)")
+    B, Sq, Hq, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = fa_bwd_workspace_bytes(B, Hq, Sq)
+    if nbytes < 0:
+        raise FaError(-nbytes, "fa_bwd_workspace_bytes")
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = fa_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, D, scale,
+                int(bool(causal)), None, None, ws, nbytes, stream, dtype)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")
+    return dq, dk, dv
 
 
 def fa_status_string(status) -> str:

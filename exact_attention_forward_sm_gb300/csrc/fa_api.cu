@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_bwd.cuh"
 #include "fa_combine.cuh"
 #include "fa_launch.cuh"
 
@@ -623,6 +624,84 @@ int fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache, void
 }
 
 long long fa_noalloc_scratch_bytes(void) { return (long long)kFixedScratchBytes; }
+
+long long fa_bwd_workspace_bytes(int B, int Hq, int Sq) {
+  if (B < 0 || Hq <= 0 || Sq < 0) return -FA_ERR_INVALID_ARG;
+  const long long rows = (long long)B * Hq * Sq;
+  return 4 * ((rows + 3) / 4 * 4) + 4 * rows;  // lse in log2 units, then delta
+}
+
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Sq,
+           int Sk, int D, float scale, int causal, const int32_t *cu_seqlens_q,
+           const int32_t *cu_seqlens_k, void *workspace, long long workspace_bytes,
+           fa_stream_t stream, int dtype) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (cu_seqlens_q || cu_seqlens_k) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (B == 0) return FA_OK;
+  const bool rows_q = Sq > 0, rows_k = Sk > 0;
+  if (rows_q && (!q || !o || !dout || !dq || !lse || !workspace)) return FA_ERR_INVALID_ARG;
+  if (rows_k && (!k || !v || !dk || !dv)) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_INVALID_ARG;
+  const long long need = fa_bwd_workspace_bytes(B, Hq, Sq);
+  if (rows_q && workspace_bytes < need) return FA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t elem = 2;
+  // no keys: dq = 0; no queries: dk = dv = 0
+  if (!rows_k) {
+    if (rows_q && cudaMemsetAsync(dq, 0, (size_t)B * Sq * Hq * D * elem, st) != cudaSuccess)
+      return FA_ERR_CUDA;
+    return FA_OK;
+  }
+  if (!rows_q) {
+    if (cudaMemsetAsync(dk, 0, (size_t)B * Sk * Hkv * D * elem, st) != cudaSuccess ||
+        cudaMemsetAsync(dv, 0, (size_t)B * Sk * Hkv * D * elem, st) != cudaSuccess)
+      return FA_ERR_CUDA;
+    return FA_OK;
+  }
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
+  int *status = status_ptr(device);
+  if (!status) return FA_ERR_CUDA;
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  fa::BwdLaunch a;
+  if (!make_map(&a.tm_q, q, bf16, D, Hq, Sq, B) || !make_map(&a.tm_do, dout, bf16, D, Hq, Sq, B) ||
+      !make_map(&a.tm_k, k, bf16, D, Hkv, Sk, B) || !make_map(&a.tm_v, v, bf16, D, Hkv, Sk, B))
+    return FA_ERR_CUDA;
+  const long long rows = (long long)B * Hq * Sq;
+  fa::BwdParams &p = a.p;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.lse_l2 = static_cast<float *>(workspace);
+  p.delta = static_cast<float *>(workspace) + (rows + 3) / 4 * 4;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.group = Hq / Hkv;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.q_tiles = (Sq + fa::kBlockM - 1) / fa::kBlockM;
+  p.k_tiles = (Sk + fa::kBlockN - 1) / fa::kBlockN;
+  p.wait_limit = kDefaultWaitLimit;
+  p.status = status;
+  a.stream = st;
+  a.device = device;
+  return fa::launch_bwd(a, D, bf16, causal != 0) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 int fa_shutdown(void) {
   reset_device_caches();

@@ -1,0 +1,617 @@
+// Backward pass of exact attention on sm_103a (see fa_bwd.cuh for the math).
+//
+// Both tile passes use the same two tcgen05 patterns as the forward kernel:
+//   SS, both operands K-major, M128 N128 K=D:  S^T = K Q^T, dP^T = V dO^T
+//                                              (key pass), S = Q K^T,
+//                                              dP = dO V^T (query pass);
+//   TS, A = 16-bit P / dS in tensor memory, B MN-major, M128 N=D K=128:
+//                                              dV += P^T dO, dK += dS^T Q
+//                                              (key pass), dQ += dS K
+//                                              (query pass).
+// A CTA has six warps: warps 0-3 do the elementwise work (warp w owns tensor
+// memory lanes 32w..32w+31, one key row per thread in the key pass, one query
+// row in the query pass), warp 4 issues the TMA loads, warp 5 owns the tensor
+// memory and issues the MMAs (one elected lane).  Per tile step the MMA pair
+// that produces the scores and dP runs, the elementwise warps turn them into
+// P / dS (16-bit, written over the scores in tensor memory), and the MMAs
+// that consume them run; the tensor pipe executes one thread's MMAs in issue
+// order, so the next step's score MMA cannot overwrite P before it is read.
+// Every wait is bounded (timeout -> FA_ERR_TIMEOUT in the status word); after
+// a failed wait a role keeps walking its loop without waiting, so every named
+// barrier still completes, and in-flight copies and MMAs are drained before
+// shared and tensor memory are released.
+#include "fa_bwd.cuh"
+#include "fa_launch.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBwdThreads = 192;
+constexpr int kBwdProducer = 4;
+constexpr int kBwdMma = 5;
+
+template <int D>
+struct SmemBwd {
+  static constexpr uint32_t kTile = (D / 64) * kChunkBytes;  // 128 rows x D, 16-bit
+  // resident pair (key pass: K, V; query pass: Q, dO) and two stages of the
+  // streamed pair (key pass: Q, dO; query pass: K, V)
+  static constexpr uint32_t kResOff = 0;
+  static constexpr uint32_t kStOff = 2 * kTile;
+  static constexpr uint32_t kVecOff = kStOff + 4 * kTile;  // [2][2][128] floats (key pass)
+  static constexpr uint32_t kBarOff = kVecOff + 2048;
+  static constexpr int kNumBars = 9;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kBytes = kMiscOff + 16;
+  // at least 120 KB, so that two CTAs never share an SM: each allocates all
+  // 512 tensor-memory columns
+  static constexpr uint32_t kAlloc = kBytes + 1024 > 120u * 1024 ? kBytes + 1024 : 120u * 1024;
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+// Dynamic shared memory opt-in, once per device and library epoch.
+struct BwdOptIn {
+  std::atomic<unsigned long long> bits{0};
+  std::atomic<unsigned> epoch{0};
+  template <class Kernel>
+  cudaError_t ensure(Kernel kern, int bytes, int device) {
+    const unsigned ep = launch_epoch().load(std::memory_order_acquire);
+    if (epoch.load(std::memory_order_acquire) != ep) {
+      bits.store(0, std::memory_order_release);
+      epoch.store(ep, std::memory_order_release);
+    }
+    const unsigned long long bit = 1ull << (device & 63);
+    if (bits.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) bits.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+  }
+};
+
+// ---------------------------------------------------------------- row pass
+// Delta = rowsum(dO * O) in fp32 and the LSE in log2 units; one warp per row
+// (b, h, i), rows in LSE order.  A row without visible keys (LSE = -inf) gets
+// +inf, so exp2(s - lse) = 0 for it.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_rows_kernel(const BwdParams p) {
+  using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  const int64_t rows = (int64_t)p.B * p.Hq * p.Sq;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const int64_t i = r % p.Sq;
+  const int64_t bh = r / p.Sq;
+  const int64_t h = bh % p.Hq, b = bh / p.Hq;
+  const int64_t off = ((b * p.Sq + i) * p.Hq + h) * D;
+  const elem_t *o = reinterpret_cast<const elem_t *>(p.o) + off;
+  const elem_t *g = reinterpret_cast<const elem_t *>(p.dout) + off;
+  float acc = 0.f;
+#pragma unroll
+  for (int e = lane; e < D; e += 32) acc += (float)o[e] * (float)g[e];
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) {
+    p.delta[r] = acc;
+    const float l = p.lse[r];
+    p.lse_l2[r] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+  }
+}
+
+// 32 fp32 values -> 16-bit, stored as four 16-byte chunks.
+template <bool BF16>
+__device__ __forceinline__ void store_row32(void *dst, const float *x, float mul) {
+  uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    d[k] = make_uint4(pack_p<BF16>(x[8 * k] * mul, x[8 * k + 1] * mul),
+                      pack_p<BF16>(x[8 * k + 2] * mul, x[8 * k + 3] * mul),
+                      pack_p<BF16>(x[8 * k + 4] * mul, x[8 * k + 5] * mul),
+                      pack_p<BF16>(x[8 * k + 6] * mul, x[8 * k + 7] * mul));
+}
+
+// SS MMA group: D[tmem] = A B^T over K = D, both operands K-major tiles.
+template <int D>
+__device__ __forceinline__ void issue_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+  mma_ss(d, a, b, idesc, 0u);
+#pragma unroll
+  for (int kk = 1; kk < D / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+    mma_ss_acc(d, a + off, b + off, idesc);
+  }
+}
+
+// TS MMA group: D[tmem] (+)= A[tmem] B over K = 128 rows of the B tile; A is
+// 16-bit pairs in 64 tensor-memory columns, B an MN-major 128 x D tile.
+__device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                         bool accumulate) {
+  mma_ts(d, a, b, idesc, accumulate ? 1u : 0u);
+#pragma unroll
+  for (int t = 1; t < 8; ++t) mma_ts_acc(d, a + t * 8, b + ((t * 2048) >> 4), idesc);
+}
+
+// ---------------------------------------------------------------- key pass
+// One CTA per (key tile, batch, K/V head), heaviest key tiles first under
+// causal masking.  dV and dK of the tile's 128 keys accumulate in tensor
+// memory over every query tile that sees a key of the tile, for every query
+// head of the group.
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using L = SmemBwd<D>;
+  using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::kBarOff;
+  const uint32_t kv_full = bar0, s_full = bar0 + 40, p_ready = bar0 + 48,
+                 acc_ready = bar0 + 56, drain = bar0 + 64;
+  auto st_full = [&](int s) { return bar0 + 8u + 8u * s; };
+  auto st_empty = [&](int s) { return bar0 + 24u + 8u * s; };
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+  float *vec = reinterpret_cast<float *>(smem + L::kVecOff);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // heavy-first: the key tile is the slowest-varying part of the CTA index
+  const int bg = blockIdx.x % (p.B * p.Hkv);
+  const int kt = blockIdx.x / (p.B * p.Hkv);
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int k0 = kt * kBlockN;
+  const int off = p.Sk - p.Sq;  // bottom-right aligned causal diagonal
+  int qt_begin = 0;
+  if (CAUSAL) qt_begin = max(0, k0 - off) / kBlockM;
+  const int nq = max(0, p.q_tiles - qt_begin);
+  const int n_it = nq * p.group;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(st_full(s), 1);
+      mbar_init(st_empty(s), 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, 4);
+    mbar_init(acc_ready, 1);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == kBwdMma) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kBwdProducer && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const long long limit = p.wait_limit;
+  auto wait = [&](uint32_t bar, uint32_t par) {
+    return wait_bar(bar, par, abort_flag, limit, p.status);
+  };
+  auto it_head = [&](int it) { return g * p.group + it / nq; };
+  auto it_tile = [&](int it) { return qt_begin + it % nq; };
+
+  if (warp == kBwdProducer) {
+    if (lane == 0 && n_it > 0) {
+      const uint64_t pol_res = policy_evict_first();
+      const uint64_t pol_st = policy_evict_last();
+      bool ok = true;
+      mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_4d(sbase + L::kResOff + c * kChunkBytes, &tm_k, kv_full, c * 64, g, k0, b,
+                    pol_res);
+        tma_load_4d(sbase + L::kResOff + L::kTile + c * kChunkBytes, &tm_v, kv_full, c * 64, g,
+                    k0, b, pol_res);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int s = it & 1;
+        if (it >= 2 && !wait(st_empty(s), ((it >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const int h = it_head(it), q0 = it_tile(it) * kBlockM;
+        const uint32_t dst = sbase + L::kStOff + s * 2 * L::kTile;
+        mbar_arrive_expect_tx(st_full(s), 2 * L::kTile);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(dst + c * kChunkBytes, &tm_q, st_full(s), c * 64, h, q0, b, pol_st);
+          tma_load_4d(dst + L::kTile + c * kChunkBytes, &tm_do, st_full(s), c * 64, h, q0, b,
+                      pol_st);
+        }
+        issued = it + 1;
+      }
+      // drain the copies still in flight before the CTA exits
+      wait_bar(kv_full, 0, abort_flag, limit, p.status, false);
+      for (int it = max(0, issued - 2); it < issued; ++it)
+        wait_bar(st_full(it & 1), (it >> 1) & 1, abort_flag, limit, p.status, false);
+    }
+  } else if (warp == kBwdMma) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_ss = make_idesc_f16(BF16, kBlockM, kBlockN, false);
+      constexpr uint32_t idesc_ts = make_idesc_f16(BF16, kBlockM, D, true);
+      const uint64_t k_desc = make_sdesc_sw128(sbase + L::kResOff, 16, 1024);
+      const uint64_t v_desc = make_sdesc_sw128(sbase + L::kResOff + L::kTile, 16, 1024);
+      bool ok = n_it == 0 || wait(kv_full, 0);
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int s = it & 1;
+        const uint32_t st = sbase + L::kStOff + s * 2 * L::kTile;
+        ok = wait(st_full(s), (it >> 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_ss<D>(tmem, k_desc, make_sdesc_sw128(st, 16, 1024), idesc_ss);  // S^T = K Q^T
+        issue_ss<D>(tmem + 128, v_desc, make_sdesc_sw128(st + L::kTile, 16, 1024),
+                    idesc_ss);  // dP^T = V dO^T
+        tc_commit(s_full);
+        ok = wait_bar_spin(p_ready, it & 1, abort_flag, limit, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        // dV += P^T dO, dK += dS^T Q (B tiles MN-major: rows = queries)
+        issue_ts(tmem + 256, tmem, make_sdesc_sw128(st + L::kTile, kChunkBytes, 1024), idesc_ts,
+                 it > 0);
+        issue_ts(tmem + 256 + D, tmem + 128, make_sdesc_sw128(st, kChunkBytes, 1024), idesc_ts,
+                 it > 0);
+        tc_commit(st_empty(s));
+      }
+      tc_commit(acc_ready);
+      // no MMA may still run when tensor memory is released
+      tc_commit(drain);
+      wait_bar(drain, 0, abort_flag, limit, p.status, false);
+    }
+  } else {
+    // -------------------------------------------- elementwise: one key per thread
+    const int row = warp * 32 + lane;
+    const int j = k0 + row;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it & 1;
+      const int h = it_head(it), q0 = it_tile(it) * kBlockM;
+      float *v_lse = vec + s * 256, *v_delta = v_lse + 128;
+      {
+        const int qi = q0 + row;
+        const int64_t r = ((int64_t)b * p.Hq + h) * p.Sq + qi;
+        v_lse[row] = qi < p.Sq ? p.lse_l2[r] : INFINITY;
+        v_delta[row] = qi < p.Sq ? p.delta[r] : 0.f;
+      }
+      named_barrier_sync(1, 128);
+      if (ok) ok = __all_sync(0xffffffffu, wait(s_full, it & 1));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(lane_base + c * 32, sr);
+          tmem_ld32(lane_base + 128 + c * 32, dr);
+          tmem_wait_ld32(sr);
+          tmem_wait_ld32(dr);
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float pe[2], de[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int qc = c * 32 + e + u;
+              const int qi = q0 + qc;
+              const bool vis = j < p.Sk && qi < p.Sq && (!CAUSAL || j <= qi + off);
+              const float pr = vis ? ex2(__uint_as_float(sr[e + u]) * sl2 - v_lse[qc]) : 0.f;
+              pe[u] = pr;
+              de[u] = pr * (__uint_as_float(dr[e + u]) - v_delta[qc]);
+            }
+            pk[e / 2] = pack_p<BF16>(pe[0], pe[1]);
+            dk[e / 2] = pack_p<BF16>(de[0], de[1]);
+          }
+          // P^T over S^T columns [16c, 16c + 16), dS^T over dP^T's: both
+          // already read (chunk c / 2 <= c)
+          tmem_st16(lane_base + c * 16, pk);
+          tmem_st16(lane_base + 128 + c * 16, dk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(p_ready);
+    }
+    // ------------------------------------------------------------- epilogue
+    bool have = n_it > 0 && ok;
+    if (have) have = __all_sync(0xffffffffu, wait(acc_ready, 0));
+    if (n_it > 0 && !have) ok = false;
+    if (have) tc_fence_after();
+    // the tensor-memory loads are warp-wide (have, ok are warp-uniform); only
+    // the stores of keys inside the sequence are per lane
+    const bool store = j < p.Sk && (ok || n_it == 0);
+    const int64_t rbase = (((int64_t)b * p.Sk + (store ? j : 0)) * p.Hkv + g) * D;
+    elem_t *dv = reinterpret_cast<elem_t *>(p.dv) + rbase;
+    elem_t *dk = reinterpret_cast<elem_t *>(p.dk) + rbase;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      float xv[32], xk[32];
+      if (have) {
+        uint32_t rv[32], rk[32];
+        tmem_ld32(lane_base + 256 + c * 32, rv);
+        tmem_ld32(lane_base + 256 + D + c * 32, rk);
+        tmem_wait_ld32(rv);
+        tmem_wait_ld32(rk);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          xv[e] = __uint_as_float(rv[e]);
+          xk[e] = __uint_as_float(rk[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) xv[e] = xk[e] = 0.f;  // no query sees these keys
+      }
+      if (store) {
+        store_row32<BF16>(dv + c * 32, xv, 1.f);
+        store_row32<BF16>(dk + c * 32, xk, p.scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdMma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// -------------------------------------------------------------- query pass
+// One CTA per (query tile, batch, query head), heaviest (latest) query tiles
+// first under causal masking.  dQ of the tile's 128 rows accumulates in
+// tensor memory over the key tiles the rows see.
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using L = SmemBwd<D>;
+  using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::kBarOff;
+  const uint32_t q_full = bar0, s_full = bar0 + 40, ds_ready = bar0 + 48,
+                 acc_ready = bar0 + 56, drain = bar0 + 64;
+  auto st_full = [&](int s) { return bar0 + 8u + 8u * s; };
+  auto st_empty = [&](int s) { return bar0 + 24u + 8u * s; };
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x % (p.B * p.Hq);
+  const int qt = p.q_tiles - 1 - (int)(blockIdx.x / (p.B * p.Hq));
+  const int b = bh / p.Hq, h = bh % p.Hq, g = h / p.group;
+  const int q0 = qt * kBlockM;
+  const int off = p.Sk - p.Sq;
+  int n_kt = p.k_tiles;
+  if (CAUSAL) {
+    const int last = min(q0 + kBlockM, p.Sq) - 1 + off;  // last key any row sees
+    n_kt = last < 0 ? 0 : min(p.k_tiles, last / kBlockN + 1);
+  }
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(st_full(s), 1);
+      mbar_init(st_empty(s), 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(ds_ready, 4);
+    mbar_init(acc_ready, 1);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == kBwdMma) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kBwdProducer && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const long long limit = p.wait_limit;
+  auto wait = [&](uint32_t bar, uint32_t par) {
+    return wait_bar(bar, par, abort_flag, limit, p.status);
+  };
+
+  if (warp == kBwdProducer) {
+    if (lane == 0 && n_kt > 0) {
+      const uint64_t pol_res = policy_evict_first();
+      const uint64_t pol_st = policy_evict_last();
+      bool ok = true;
+      mbar_arrive_expect_tx(q_full, 2 * L::kTile);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_4d(sbase + L::kResOff + c * kChunkBytes, &tm_q, q_full, c * 64, h, q0, b,
+                    pol_res);
+        tma_load_4d(sbase + L::kResOff + L::kTile + c * kChunkBytes, &tm_do, q_full, c * 64, h,
+                    q0, b, pol_res);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_kt && ok; ++it) {
+        const int s = it & 1;
+        if (it >= 2 && !wait(st_empty(s), ((it >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = sbase + L::kStOff + s * 2 * L::kTile;
+        mbar_arrive_expect_tx(st_full(s), 2 * L::kTile);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(dst + c * kChunkBytes, &tm_k, st_full(s), c * 64, g, it * kBlockN, b,
+                      pol_st);
+          tma_load_4d(dst + L::kTile + c * kChunkBytes, &tm_v, st_full(s), c * 64, g,
+                      it * kBlockN, b, pol_st);
+        }
+        issued = it + 1;
+      }
+      wait_bar(q_full, 0, abort_flag, limit, p.status, false);
+      for (int it = max(0, issued - 2); it < issued; ++it)
+        wait_bar(st_full(it & 1), (it >> 1) & 1, abort_flag, limit, p.status, false);
+    }
+  } else if (warp == kBwdMma) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_ss = make_idesc_f16(BF16, kBlockM, kBlockN, false);
+      constexpr uint32_t idesc_ts = make_idesc_f16(BF16, kBlockM, D, true);
+      const uint64_t q_desc = make_sdesc_sw128(sbase + L::kResOff, 16, 1024);
+      const uint64_t do_desc = make_sdesc_sw128(sbase + L::kResOff + L::kTile, 16, 1024);
+      bool ok = n_kt == 0 || wait(q_full, 0);
+      for (int it = 0; it < n_kt && ok; ++it) {
+        const int s = it & 1;
+        const uint32_t st = sbase + L::kStOff + s * 2 * L::kTile;
+        ok = wait(st_full(s), (it >> 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_ss<D>(tmem, q_desc, make_sdesc_sw128(st, 16, 1024), idesc_ss);  // S = Q K^T
+        issue_ss<D>(tmem + 128, do_desc, make_sdesc_sw128(st + L::kTile, 16, 1024),
+                    idesc_ss);  // dP = dO V^T
+        tc_commit(s_full);
+        ok = wait_bar_spin(ds_ready, it & 1, abort_flag, limit, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        // dQ += dS K (K tile MN-major: rows = keys)
+        issue_ts(tmem + 256, tmem, make_sdesc_sw128(st, kChunkBytes, 1024), idesc_ts, it > 0);
+        tc_commit(st_empty(s));
+      }
+      tc_commit(acc_ready);
+      tc_commit(drain);
+      wait_bar(drain, 0, abort_flag, limit, p.status, false);
+    }
+  } else {
+    // ------------------------------------------ elementwise: one query row per thread
+    const int row = warp * 32 + lane;
+    const int qi = q0 + row;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = p.scale_log2;
+    const int64_t r = ((int64_t)b * p.Hq + h) * p.Sq + qi;
+    const float lse2 = qi < p.Sq ? p.lse_l2[r] : INFINITY;
+    const float dlt = qi < p.Sq ? p.delta[r] : 0.f;
+    bool ok = true;
+    for (int it = 0; it < n_kt; ++it) {
+      if (ok) ok = __all_sync(0xffffffffu, wait(s_full, it & 1));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(lane_base + c * 32, sr);
+          tmem_ld32(lane_base + 128 + c * 32, dr);
+          tmem_wait_ld32(sr);
+          tmem_wait_ld32(dr);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float de[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int j = it * kBlockN + c * 32 + e + u;
+              const bool vis = j < p.Sk && qi < p.Sq && (!CAUSAL || j <= qi + off);
+              const float pr = vis ? ex2(__uint_as_float(sr[e + u]) * sl2 - lse2) : 0.f;
+              de[u] = pr * (__uint_as_float(dr[e + u]) - dlt);
+            }
+            pk[e / 2] = pack_p<BF16>(de[0], de[1]);
+          }
+          tmem_st16(lane_base + c * 16, pk);  // dS over S columns already read
+        }
+        tmem_st_wait();
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(ds_ready);
+    }
+    bool have = n_kt > 0 && ok;
+    if (have) have = __all_sync(0xffffffffu, wait(acc_ready, 0));
+    if (n_kt > 0 && !have) ok = false;
+    if (have) tc_fence_after();
+    const bool store = qi < p.Sq && (ok || n_kt == 0);
+    elem_t *dq = reinterpret_cast<elem_t *>(p.dq) +
+                 (((int64_t)b * p.Sq + (store ? qi : 0)) * p.Hq + h) * D;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      float x[32];
+      if (have) {
+        uint32_t rq[32];
+        tmem_ld32_wait(lane_base + 256 + c * 32, rq);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(rq[e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = 0.f;  // the row sees no key
+      }
+      if (store) store_row32<BF16>(dq + c * 32, x, p.scale);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdMma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_bwd_t(const BwdLaunch &a) {
+  const BwdParams &p = a.p;
+  const int64_t rows = (int64_t)p.B * p.Hq * p.Sq;
+  if (rows > 0) {
+    fa_bwd_rows_kernel<D, BF16><<<(unsigned)((rows + 7) / 8), 256, 0, a.stream>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  using L = SmemBwd<D>;
+  auto kv = fa_bwd_kv_kernel<D, BF16, CAUSAL>;
+  auto qk = fa_bwd_q_kernel<D, BF16, CAUSAL>;
+  static BwdOptIn opt_kv, opt_q;
+  cudaError_t e = opt_kv.ensure(kv, (int)L::kAlloc, a.device);
+  if (e != cudaSuccess) return e;
+  e = opt_q.ensure(qk, (int)L::kAlloc, a.device);
+  if (e != cudaSuccess) return e;
+  const int64_t kv_ctas = (int64_t)p.k_tiles * p.B * p.Hkv;
+  const int64_t q_ctas = (int64_t)p.q_tiles * p.B * p.Hq;
+  if (kv_ctas > 0) {
+    kv<<<(unsigned)kv_ctas, kBwdThreads, L::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do,
+                                                               p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (q_ctas > 0) {
+    qk<<<(unsigned)q_ctas, kBwdThreads, L::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do,
+                                                              p);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdLaunch &a, int D, bool bf16, bool causal) {
+  if (D == 64) {
+    if (bf16) return causal ? launch_bwd_t<64, true, true>(a) : launch_bwd_t<64, true, false>(a);
+    return causal ? launch_bwd_t<64, false, true>(a) : launch_bwd_t<64, false, false>(a);
+  }
+  if (bf16) return causal ? launch_bwd_t<128, true, true>(a) : launch_bwd_t<128, true, false>(a);
+  return causal ? launch_bwd_t<128, false, true>(a) : launch_bwd_t<128, false, false>(a);
+}
+
+}  // namespace fa

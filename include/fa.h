@@ -266,6 +266,49 @@ int fa_split_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int varlen,
                   int num_splits, long long *scratch_bytes);
 
 /*
+ * fa_bwd — gradients of exact attention: the backward pass that the fork's
+ * v1.7 release notes validate next to the forward (section 4.4).  Dense
+ * problems (no cu_seqlens), head dim 64 or 128, fp16 or bf16.
+ *
+ * Inputs, all DEVICE memory in the layouts of fa_fwd:
+ *   q [B, Sq, Hq, D], k / v [B, Sk, Hkv, D]  the forward's inputs
+ *   o [B, Sq, Hq, D], lse [B, Hq, Sq] fp32    the forward's outputs (as fa_fwd
+ *                                             with the same arguments wrote
+ *                                             them)
+ *   dout [B, Sq, Hq, D]                       dL/dO, the upstream gradient
+ * Outputs (written in full, never accumulated into):
+ *   dq [B, Sq, Hq, D], dk / dv [B, Sk, Hkv, D], the inputs' dtype.
+ * With P = softmax(scale q k^T) over each row's visible keys (causal masking
+ * bottom-right aligned, as fa_fwd), dP = dout v^T and
+ * dS = P * (dP - rowsum(dout * o)):
+ *   dq = scale dS k,   dk = scale dS^T q,   dv = P^T dout,
+ * dk and dv summed over the query heads of each K/V head's group.  Keys that
+ * no query sees get zero gradients, rows without a visible key dq = 0.  The
+ * result does not depend on scheduling (no atomics): repeated calls agree
+ * bit for bit.
+ *
+ * workspace: DEVICE memory owned by the caller, 16-byte aligned, at least
+ * fa_bwd_workspace_bytes(B, Hq, Sq) bytes; used by this call's kernels on
+ * `stream` only (two fp32 values per query row and head); contents on entry
+ * do not matter.
+ *
+ * Returns FA_OK once queued; FA_ERR_INVALID_ARG (nothing queued) for invalid
+ * sizes, flags or scale, a NULL or misaligned pointer (16 bytes; lse 4) or a
+ * workspace smaller than needed; FA_ERR_UNSUPPORTED for another head dim or
+ * non-NULL cu_seqlens; FA_ERR_CUDA.  A device-side pipeline timeout is
+ * recorded for fa_get_device_error (FA_ERR_TIMEOUT).
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Sq,
+           int Sk, int D, float scale, int causal, const int32_t *cu_seqlens_q,
+           const int32_t *cu_seqlens_k, void *workspace, long long workspace_bytes,
+           fa_stream_t stream, int dtype);
+
+/* Device workspace fa_bwd needs for these sizes, in bytes (two fp32 values
+ * per query row and head, 16-byte aligned halves), or minus a status code. */
+long long fa_bwd_workspace_bytes(int B, int Hq, int Sq);
+
+/*
  * fa_get_device_error — synchronize `stream`, then return and clear the status
  * word that kernels on the current device set on a device-side error
  * (FA_OK if none).  Returns FA_ERR_CUDA if the synchronization itself fails.

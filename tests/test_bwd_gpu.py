@@ -1,0 +1,141 @@
+"""GPU parity of the backward pass (``fa_bwd``) against the fp64 backward oracle.
+
+The fork's v1.7 release notes validate a backward pass next to the forward
+(section 4.4): finite dQ / dK / dV at S = 2048 causal in fp16 and bf16, and
+gradient errors against an fp32 reference.  Here the library's gradients,
+computed from its own forward output and LSE, are compared element by element
+with ``oracle.attention_bwd`` (fp64, plain definition) on the same 16-bit
+inputs and upstream gradient.
+
+Gates per gradient tensor: cosine >= 0.9995 and max |g - ref| <= TOL *
+max(max |ref|, 1e-3) with TOL = 2e-2 (bf16) / 1e-2 (fp16).  The kernels round P and dS
+to the input type for the tensor-core products and the outputs to it (bf16
+keeps 8 significant bits: 2^-9 relative per rounding, 2^-8 per output
+element at worst); the row term rowsum(dO * O) reads the 16-bit O, and dS =
+P (dP - rowsum) cancels, so the gates sit a few output roundings above that.
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines too
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import exact_attention_forward_sm_gb300 as fa  # noqa: E402
+import oracle  # noqa: E402
+
+TOL = {"bf16": 2e-2, "fp16": 1e-2}
+COS_MIN = 0.9995
+ABS_FLOOR = 1e-3
+TORCH_DT = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from exact_attention_forward_sm_gb300 import _build
+    _build.build()
+    fa.load_library()
+
+
+def _draw(B, Hq, Hkv, Sq, Sk, D, dtype, seed, sigma=1.0):
+    g = torch.Generator().manual_seed(seed)
+    dt = TORCH_DT[dtype]
+    q = (torch.randn(B, Sq, Hq, D, generator=g) * sigma).to(dt)
+    k = (torch.randn(B, Sk, Hkv, D, generator=g) * sigma).to(dt)
+    v = torch.randn(B, Sk, Hkv, D, generator=g).to(dt)
+    do = torch.randn(B, Sq, Hq, D, generator=g).to(dt)
+    return q, k, v, do
+
+
+def _run(q, k, v, do, causal, scale=None):
+    dev = "cuda:0"
+    qd, kd, vd, dod = (t.to(dev).contiguous() for t in (q, k, v, do))
+    out, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, out, lse, dod, causal=causal, scale=scale)
+    st = fa.fa_get_device_error(torch.cuda.current_stream())
+    assert st == fa.FA_OK, fa.fa_status_string(st)
+    return dq, dk, dv
+
+
+def _compare(name, got, ref, dtype):
+    g = got.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(g).all(), f"{name}: non-finite gradient"
+    # a reference that vanishes (one key: dS = 0 exactly) is held to an
+    # absolute floor: the rounding noise of dP - rowsum(dO * O) stays far below
+    scale = max(np.max(np.abs(ref)), ABS_FLOOR)
+    err = np.max(np.abs(g - ref)) / scale
+    cos = float(np.sum(g * ref) / max(np.linalg.norm(g) * np.linalg.norm(ref), 1e-300))
+    assert err <= TOL[dtype], f"{name}: max error {err:.3e} of max |ref|"
+    if np.max(np.abs(ref)) > 0:
+        assert cos >= COS_MIN, f"{name}: cosine {cos:.6f}"
+    return err, cos
+
+
+def _check(B, Hq, Hkv, Sq, Sk, D, dtype, causal, seed, sigma=1.0):
+    q, k, v, do = _draw(B, Hq, Hkv, Sq, Sk, D, dtype, seed, sigma)
+    dq, dk, dv = _run(q, k, v, do, causal)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, B, Hq, Hkv, Sq, Sk, D, D ** -0.5, causal)
+    return {n: _compare(n, g, r, dtype) for n, g, r in
+            (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv))}
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "fp16"), (128, "fp16"), (64, "bf16")])
+def test_gradients_several_tiles_ragged(causal, D, dtype):
+    """Three query and key tiles with a ragged tail, GQA 2:1."""
+    _check(2, 4, 2, 300, 300, D, dtype, causal, seed=D + 7 * causal + (dtype == "bf16"))
+
+
+@pytest.mark.parametrize("Sq,Sk", [(200, 333), (333, 200), (1, 129), (129, 1)])
+def test_gradients_unequal_lengths(Sq, Sk):
+    """Bottom-right aligned causal masking with Sq != Sk; Sq > Sk leaves the
+    first Sq - Sk rows without keys (dq = 0) and Sk = 1 / Sq = 1 edge tiles."""
+    _check(1, 2, 2, Sq, Sk, 64, "fp16", True, seed=Sq * 1000 + Sk)
+    _check(1, 2, 1, Sq, Sk, 128, "bf16", False, seed=Sq * 1000 + Sk + 1)
+
+
+def test_gradients_gqa_4_to_1_wide_scores():
+    _check(1, 8, 2, 257, 384, 128, "bf16", True, seed=41, sigma=1.6)
+
+
+def test_repeatable_bit_for_bit():
+    q, k, v, do = _draw(2, 4, 2, 256, 384, 128, "bf16", 5)
+    a = _run(q, k, v, do, True)
+    b = _run(q, k, v, do, True)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_no_queries_or_no_keys_give_zero_gradients():
+    dev = "cuda:0"
+    q = torch.randn(2, 0, 4, 64, device=dev, dtype=torch.bfloat16)
+    k = torch.randn(2, 50, 2, 64, device=dev, dtype=torch.bfloat16)
+    v = torch.randn_like(k)
+    o = torch.empty_like(q)
+    lse = torch.empty(2, 4, 0, device=dev)
+    dk = torch.full_like(k, float("nan"))
+    dv = torch.full_like(v, float("nan"))
+    st = fa.fa_bwd(q, k, v, o, lse, o, o, dk, dv, 2, 4, 2, 0, 50, 64, 0.125, 1, None, None,
+                   None, 0, torch.cuda.current_stream(), fa.FA_DTYPE_BF16)
+    assert st == fa.FA_OK
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
+    q = torch.randn(2, 30, 4, 64, device=dev, dtype=torch.bfloat16)
+    k = torch.empty(2, 0, 2, 64, device=dev, dtype=torch.bfloat16)
+    dq = torch.full_like(q, float("nan"))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(2, 4, 30), dtype=torch.uint8, device=dev)
+    lse = torch.full((2, 4, 30), float("-inf"), device=dev)
+    st = fa.fa_bwd(q, k, k, q, lse, q, dq, k, k, 2, 4, 2, 30, 0, 64, 0.125, 0, None, None,
+                   ws, ws.numel(), torch.cuda.current_stream(), fa.FA_DTYPE_BF16)
+    assert st == fa.FA_OK
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dq) == 0
+
+
+def test_full_size_causal_benchmark_shape():
+    """B4 H16 S2048 D128 bf16 causal (the forward benchmark's shape; the
+    release notes' backward finiteness check runs S = 2048 causal): every
+    element of dq, dk, dv against the oracle."""
+    _check(4, 16, 16, 2048, 2048, 128, "bf16", True, seed=2048)
