@@ -46,6 +46,7 @@ KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd_kernel.cuh", "fa_ptx.cuh", "fa_launch.cuh"],
     "fa_fwd_wide_kernel": ["fa_fwd_wide.cuh", "fa_fwd_kernel.cuh", "fa_ptx.cuh",
                            "fa_launch.cuh"],
+    "fa_bwd": ["fa_bwd.cu", "fa_bwd.cuh", "fa_fwd_kernel.cuh", "fa_ptx.cuh", "fa_launch.cuh"],
 }
 
 
@@ -226,6 +227,31 @@ def oracle_sample_kvcache(case, seconds, seed=0):
             "rows_total": int(n_rows), "flops": fl, "threads": threads}
 
 
+def oracle_sample_bwd(case, dout, seconds):
+    """Time the fp64 backward oracle on a sub-problem of the workload: batch
+    0, every head, the first S' query and key positions, with S' sized from a
+    256-position calibration run to about `seconds` of work (causal work grows
+    as S'^2).  TFLOP/s counts 2.5x the forward FLOPs of the sub-problem."""
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+    q, k, v, do = (t[:1].float().numpy() for t in (case.q, case.k, case.v, dout))
+
+    def run(sp):
+        sub = [np.ascontiguousarray(x[:, :sp]) for x in (q, k, v, do)]
+        t0 = time.perf_counter()
+        oracle.attention_bwd(*sub, 1, case.Hq, case.Hkv, sp, sp, case.D, case.scale,
+                             case.causal, nthreads=threads)
+        pairs = sp * (sp + 1) / 2 if case.causal else sp * sp
+        return time.perf_counter() - t0, 2.5 * 4.0 * case.D * case.Hq * pairs
+
+    s0 = min(case.Sq, case.Sk, 256)
+    dt, _ = run(s0)
+    sp = int(min(case.Sq, case.Sk, max(s0, s0 * (seconds / max(dt, 1e-6)) ** 0.5)))
+    dt, fl = run(sp)
+    return {"tflops": fl / dt / 1e12, "seconds": dt, "rows": case.Hq * sp,
+            "rows_total": case.B * case.Hq * case.Sq, "flops": fl, "threads": threads}
+
+
 def _visible_per_row(case):
     """Visible keys of every row in LSE-index order."""
     out = []
@@ -326,6 +352,57 @@ def attention_problem(args, fa, rank, dev, stream):
                    kernel="fa_fwd_wide_kernel" if case.D == 256 else "fa_fwd_kernel")
 
 
+# backward workloads: "bwd_" + a dense forward workload without score variants
+BWD_PREFIX = "bwd_"
+BWD_WORKLOADS = sorted(BWD_PREFIX + w.name for w in wl.WORKLOADS
+                       if w.D in (64, 128) and not w.varlen_count)
+
+
+def backward_problem(args, fa, rank, dev, stream):
+    """fa_bwd (dq, dk, dv) after one untimed fa_fwd of the same workload."""
+    w = wl.BY_NAME[args.workload[len(BWD_PREFIX):]]
+    w_rank = wl.Workload(**{**w.__dict__, "seed": rank_seed(w.seed, rank)})
+    case = wl.make_workload(w_rank)
+    dtype_code = wl.DTYPE_CODE[case.dtype]
+    q, k, v = (t.to(dev) for t in (case.q, case.k, case.v))
+    o = torch.empty_like(q)
+    lse = torch.empty((case.B, case.Hq, case.Sq), dtype=torch.float32, device=dev)
+    st = fa.fa_fwd(q, k, v, o, lse, case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D,
+                   case.scale, int(case.causal), None, None, stream, dtype_code)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"fa_fwd: {fa.fa_status_string(st)}")
+    g = torch.Generator().manual_seed(w_rank.seed + 17)
+    dout_h = torch.randn(tuple(case.q.shape), generator=g).to(case.q.dtype)
+    dout = dout_h.to(dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = fa.fa_bwd_workspace_bytes(case.B, case.Hq, case.Sq)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+
+    def launch():
+        rc = fa.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, case.B, case.Hq, case.Hkv, case.Sq,
+                       case.Sk, case.D, case.scale, int(case.causal), None, None, ws, nbytes,
+                       stream, dtype_code)
+        if rc != fa.FA_OK:
+            raise RuntimeError(f"fa_bwd: {fa.fa_status_string(rc)}")
+
+    torch.cuda.synchronize()
+    o_h, lse_h = o.cpu(), lse.cpu()
+    elem = 2
+    rows = case.B * case.Hq * case.Sq
+    n_q, n_k = case.q.numel(), case.k.numel()
+    # read q, k, v, o, dout, lse; write dq, dk, dv; the row pass's two fp32
+    # values per row written once and read by both tile passes
+    alg_bytes = elem * (3 * n_q + 2 * n_k) + 4 * rows + elem * (n_q + 2 * n_k) + 8 * rows * 3
+    config = {"workload": args.workload, "pass": "backward (dq, dk, dv)", "B": case.B,
+              "Hq": case.Hq, "Hkv": case.Hkv, "Sq": case.Sq, "Sk": case.Sk, "D": case.D,
+              "causal": case.causal, "flops": "2.5 x forward (dS, dP recomputed: the kernels "
+              "run 3.5 x forward on the tensor cores)"}
+    return Problem(args.workload, case.dtype, 2.5 * wl.attention_flops(case), alg_bytes,
+                   [case.q, case.k, case.v, o_h, lse_h, dout_h], [q, k, v, o, lse, dout],
+                   [dq, dk, dv], launch, 3, config,
+                   lambda secs: oracle_sample_bwd(case, dout_h, secs), kernel="fa_bwd")
+
+
 def kvcache_problem(args, fa, rank, dev, stream):
     """fa_fwd_kvcache over one of the KV-cache (decoding) workloads."""
     w = wl.CACHE_BY_NAME[args.workload]
@@ -374,7 +451,8 @@ def run_gpu_arm(args, rank, local_rank, world):
         _build.build(variant=args.variant)
     fa.load_library()
     stream = torch.cuda.current_stream(dev)
-    make = kvcache_problem if args.workload in wl.CACHE_BY_NAME else attention_problem
+    make = (kvcache_problem if args.workload in wl.CACHE_BY_NAME else
+            backward_problem if args.workload.startswith(BWD_PREFIX) else attention_problem)
     prob = make(args, fa, rank, dev, stream)
     flops = prob.flops
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -588,7 +666,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(wl.BY_NAME) + sorted(wl.CACHE_BY_NAME))
+                    choices=sorted(wl.BY_NAME) + sorted(wl.CACHE_BY_NAME) + BWD_WORKLOADS)
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--reference-budget-s", type=float, default=90.0,

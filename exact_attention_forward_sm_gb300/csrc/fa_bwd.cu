@@ -8,10 +8,12 @@
 //                                              dV += P^T dO, dK += dS^T Q
 //                                              (key pass), dQ += dS K
 //                                              (query pass).
-// A CTA has six warps: warps 0-3 do the elementwise work (warp w owns tensor
-// memory lanes 32w..32w+31, one key row per thread in the key pass, one query
-// row in the query pass), warp 4 issues the TMA loads, warp 5 owns the tensor
-// memory and issues the MMAs (one elected lane).  Per tile step the MMA pair
+// A CTA has ten warps: warps 0-7 do the elementwise work (warp w owns tensor
+// memory lanes 32 (w % 4) .. 32 (w % 4) + 31 -- one key row per thread in the
+// key pass, one query row in the query pass -- and warpgroup w / 4 the column
+// half 64 (w / 4) .. 64 (w / 4) + 63, so two warps share each sub-partition),
+// warp 8 issues the TMA loads, warp 9 owns the tensor memory and issues the
+// MMAs (one elected lane).  Per tile step the MMA pair
 // that produces the scores and dP runs, the elementwise warps turn them into
 // P / dS (16-bit, written over the scores in tensor memory), and the MMAs
 // that consume them run; the tensor pipe executes one thread's MMAs in issue
@@ -26,9 +28,9 @@
 namespace fa {
 namespace {
 
-constexpr int kBwdThreads = 192;
-constexpr int kBwdProducer = 4;
-constexpr int kBwdMma = 5;
+constexpr int kBwdThreads = 320;
+constexpr int kBwdProducer = 8;
+constexpr int kBwdMma = 9;
 
 template <int D>
 struct SmemBwd {
@@ -39,7 +41,7 @@ struct SmemBwd {
   static constexpr uint32_t kStOff = 2 * kTile;
   static constexpr uint32_t kVecOff = kStOff + 4 * kTile;  // [2][2][128] floats (key pass)
   static constexpr uint32_t kBarOff = kVecOff + 2048;
-  static constexpr int kNumBars = 9;
+  static constexpr int kNumBars = 10;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   // at least 120 KB, so that two CTAs never share an SM: each allocates all
@@ -85,9 +87,16 @@ __global__ void __launch_bounds__(256) fa_bwd_rows_kernel(const BwdParams p) {
   const int64_t off = ((b * p.Sq + i) * p.Hq + h) * D;
   const elem_t *o = reinterpret_cast<const elem_t *>(p.o) + off;
   const elem_t *g = reinterpret_cast<const elem_t *>(p.dout) + off;
+  // each lane reads D / 32 consecutive elements of both rows in one load
+  constexpr int kPer = D / 32;
+  using vec_t = typename std::conditional<kPer == 4, uint2, uint32_t>::type;
+  const vec_t vo = *reinterpret_cast<const vec_t *>(o + lane * kPer);
+  const vec_t vg = *reinterpret_cast<const vec_t *>(g + lane * kPer);
+  const elem_t *eo = reinterpret_cast<const elem_t *>(&vo);
+  const elem_t *eg = reinterpret_cast<const elem_t *>(&vg);
   float acc = 0.f;
 #pragma unroll
-  for (int e = lane; e < D; e += 32) acc += (float)o[e] * (float)g[e];
+  for (int e = 0; e < kPer; ++e) acc += (float)eo[e] * (float)eg[e];
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (lane == 0) {
@@ -120,13 +129,109 @@ __device__ __forceinline__ void issue_ss(uint32_t d, uint64_t a, uint64_t b, uin
   }
 }
 
-// TS MMA group: D[tmem] (+)= A[tmem] B over K = 128 rows of the B tile; A is
-// 16-bit pairs in 64 tensor-memory columns, B an MN-major 128 x D tile.
-__device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
-                                         bool accumulate) {
-  mma_ts(d, a, b, idesc, accumulate ? 1u : 0u);
+// Half h of a TS MMA group: D[tmem] (+)= A[tmem] B over rows 64h .. 64h + 63
+// of the B tile (four K = 16 steps); A is the half's 16-bit pairs in tensor-
+// memory columns 64h .. 64h + 31 (the first half of the half's own 64 score
+// columns, which only its own warpgroup reads), B an MN-major 128 x D tile.
+// `accumulate` applies to the first step of half 0 (the group's first
+// product).
+__device__ __forceinline__ void issue_ts_half(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                              int h, bool accumulate) {
+  const uint32_t ah = a + 64 * h;
+  const uint64_t bh = b + ((h * 4 * 2048) >> 4);
+  if (h == 0)
+    mma_ts(d, ah, bh, idesc, accumulate ? 1u : 0u);
+  else
+    mma_ts_acc(d, ah, bh, idesc);
 #pragma unroll
-  for (int t = 1; t < 8; ++t) mma_ts_acc(d, a + t * 8, b + ((t * 2048) >> 4), idesc);
+  for (int t = 1; t < 4; ++t) mma_ts_acc(d, ah + t * 8, bh + ((t * 2048) >> 4), idesc);
+}
+
+// Tensor-memory column (relative to a score tile) of the 16-bit pairs of
+// score chunk c (32 columns): half c / 2 packs into the first 32 of its own
+// 64 columns, so a warpgroup only overwrites columns it has read itself.
+__device__ __forceinline__ uint32_t packed_col(int c) { return 64 * (c >> 1) + 16 * (c & 1); }
+
+__device__ __forceinline__ void mul2(float &d0, float &d1, float a0, float a1, float b0,
+                                     float b1) {
+  const float2 d = __fmul2_rn(make_float2(a0, a1), make_float2(b0, b1));
+  d0 = d.x;
+  d1 = d.y;
+}
+
+// Key pass, 32 query columns 32c .. 32c + 31 of one key row: P^T = exp2(S^T
+// scale log2e - lse) and dS^T = P^T (dP^T - Delta), written as 16-bit pairs
+// over the columns already read.  MASKED: per-element visibility (a tile at
+// a sequence end or crossing the causal diagonal); otherwise every element
+// is visible.
+template <bool BF16, bool MASKED, bool CAUSAL>
+__device__ __forceinline__ void kv_chunk(uint32_t lane_base, int c, float sl2, const float *v_lse,
+                                         const float *v_delta, int j, int q0, int Sq, int Sk,
+                                         int off) {
+  uint32_t sr[32], dr[32];
+  tmem_ld32(lane_base + c * 32, sr);
+  tmem_ld32(lane_base + 128 + c * 32, dr);
+  tmem_wait_ld32(sr);
+  tmem_wait_ld32(dr);
+  const float2 *l2 = reinterpret_cast<const float2 *>(v_lse + c * 32);
+  const float2 *dl = reinterpret_cast<const float2 *>(v_delta + c * 32);
+  uint32_t pk[16], dk[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float2 lv = l2[e], dv = dl[e];
+    float x0, x1;
+    fma_f32x2(x0, x1, __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]), sl2, sl2,
+              -lv.x, -lv.y);
+    float p0 = ex2(x0), p1 = ex2(x1);
+    if (MASKED) {
+      const int qi = q0 + c * 32 + 2 * e;
+      const bool ok_j = j < Sk;
+      p0 = (ok_j && qi < Sq && (!CAUSAL || j <= qi + off)) ? p0 : 0.f;
+      p1 = (ok_j && qi + 1 < Sq && (!CAUSAL || j <= qi + 1 + off)) ? p1 : 0.f;
+    }
+    float t0 = __uint_as_float(dr[2 * e]), t1 = __uint_as_float(dr[2 * e + 1]);
+    add_f32x2(t0, t1, -dv.x, -dv.y);
+    float d0, d1;
+    mul2(d0, d1, p0, p1, t0, t1);
+    pk[e] = pack_p<BF16>(p0, p1);
+    dk[e] = pack_p<BF16>(d0, d1);
+  }
+  // P^T over S^T columns, dS^T over dP^T's, both in this chunk's half and
+  // already read by this warp (chunk 2h + 1 packs over columns chunk 2h read)
+  tmem_st16(lane_base + packed_col(c), pk);
+  tmem_st16(lane_base + 128 + packed_col(c), dk);
+}
+
+// Query pass, 32 key columns 32c .. 32c + 31 of key tile kt for one query
+// row: dS = exp2(S scale log2e - lse) (dP - Delta) as 16-bit pairs over S.
+template <bool BF16, bool MASKED, bool CAUSAL>
+__device__ __forceinline__ void q_chunk(uint32_t lane_base, int c, float sl2, float lse2,
+                                        float dlt, int qi, int kt, int Sq, int Sk, int off) {
+  uint32_t sr[32], dr[32];
+  tmem_ld32(lane_base + c * 32, sr);
+  tmem_ld32(lane_base + 128 + c * 32, dr);
+  tmem_wait_ld32(sr);
+  tmem_wait_ld32(dr);
+  uint32_t pk[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    float x0, x1;
+    fma_f32x2(x0, x1, __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]), sl2, sl2,
+              -lse2, -lse2);
+    float p0 = ex2(x0), p1 = ex2(x1);
+    if (MASKED) {
+      const int j = kt * kBlockN + c * 32 + 2 * e;
+      const bool ok_q = qi < Sq;
+      p0 = (ok_q && j < Sk && (!CAUSAL || j <= qi + off)) ? p0 : 0.f;
+      p1 = (ok_q && j + 1 < Sk && (!CAUSAL || j + 1 <= qi + off)) ? p1 : 0.f;
+    }
+    float t0 = __uint_as_float(dr[2 * e]), t1 = __uint_as_float(dr[2 * e + 1]);
+    add_f32x2(t0, t1, -dlt, -dlt);
+    float d0, d1;
+    mul2(d0, d1, p0, p1, t0, t1);
+    pk[e] = pack_p<BF16>(d0, d1);
+  }
+  tmem_st16(lane_base + packed_col(c), pk);  // dS over S columns this warp read
 }
 
 // ---------------------------------------------------------------- key pass
@@ -147,10 +252,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::kBarOff;
-  const uint32_t kv_full = bar0, s_full = bar0 + 40, p_ready = bar0 + 48,
-                 acc_ready = bar0 + 56, drain = bar0 + 64;
+  const uint32_t kv_full = bar0, s_full = bar0 + 40, acc_ready = bar0 + 56,
+                 drain = bar0 + 64;
   auto st_full = [&](int s) { return bar0 + 8u + 8u * s; };
   auto st_empty = [&](int s) { return bar0 + 24u + 8u * s; };
+  // P^T / dS^T of queries 64h .. 64h + 63 written (h = 0, 1)
+  auto p_half = [&](int h) { return h ? bar0 + 72u : bar0 + 48u; };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
   float *vec = reinterpret_cast<float *>(smem + L::kVecOff);
@@ -175,7 +282,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(st_empty(s), 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_ready, 4);
+    mbar_init(p_half(0), 4);
+    mbar_init(p_half(1), 4);
     mbar_init(acc_ready, 1);
     mbar_init(drain, 1);
     fence_barrier_init();
@@ -252,14 +360,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         issue_ss<D>(tmem + 128, v_desc, make_sdesc_sw128(st + L::kTile, 16, 1024),
                     idesc_ss);  // dP^T = V dO^T
         tc_commit(s_full);
-        ok = wait_bar_spin(p_ready, it & 1, abort_flag, limit, p.status);
+        // dV += P^T dO, dK += dS^T Q (B tiles MN-major: rows = queries), each
+        // half of the queries as soon as the elementwise warps have written it
+        const uint64_t do_mn = make_sdesc_sw128(st + L::kTile, kChunkBytes, 1024);
+        const uint64_t q_mn = make_sdesc_sw128(st, kChunkBytes, 1024);
+        for (int hh = 0; hh < 2 && ok; ++hh) {
+          ok = wait_bar_spin(p_half(hh), it & 1, abort_flag, limit, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_ts_half(tmem + 256, tmem, do_mn, idesc_ts, hh, it > 0);
+          issue_ts_half(tmem + 256 + D, tmem + 128, q_mn, idesc_ts, hh, it > 0);
+        }
         if (!ok) break;
-        tc_fence_after();
-        // dV += P^T dO, dK += dS^T Q (B tiles MN-major: rows = queries)
-        issue_ts(tmem + 256, tmem, make_sdesc_sw128(st + L::kTile, kChunkBytes, 1024), idesc_ts,
-                 it > 0);
-        issue_ts(tmem + 256 + D, tmem + 128, make_sdesc_sw128(st, kChunkBytes, 1024), idesc_ts,
-                 it > 0);
         tc_commit(st_empty(s));
       }
       tc_commit(acc_ready);
@@ -269,58 +381,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // -------------------------------------------- elementwise: one key per thread
-    const int row = warp * 32 + lane;
+    const int quarter = warp & 3, wg = warp >> 2;  // TMEM lane quarter, column half
+    const int row = quarter * 32 + lane;
     const int j = k0 + row;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
       const int h = it_head(it), q0 = it_tile(it) * kBlockM;
       float *v_lse = vec + s * 256, *v_delta = v_lse + 128;
-      {
+      if (wg == 0) {
         const int qi = q0 + row;
         const int64_t r = ((int64_t)b * p.Hq + h) * p.Sq + qi;
         v_lse[row] = qi < p.Sq ? p.lse_l2[r] : INFINITY;
         v_delta[row] = qi < p.Sq ? p.delta[r] : 0.f;
       }
-      named_barrier_sync(1, 128);
+      named_barrier_sync(1, 256);
       if (ok) ok = __all_sync(0xffffffffu, wait(s_full, it & 1));
       if (ok) {
         tc_fence_after();
+        const bool interior = k0 + kBlockN <= p.Sk && q0 + kBlockM <= p.Sq &&
+                              (!CAUSAL || k0 + kBlockN - 1 <= q0 + off);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32], dr[32];
-          tmem_ld32(lane_base + c * 32, sr);
-          tmem_ld32(lane_base + 128 + c * 32, dr);
-          tmem_wait_ld32(sr);
-          tmem_wait_ld32(dr);
-          uint32_t pk[16], dk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float pe[2], de[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int qc = c * 32 + e + u;
-              const int qi = q0 + qc;
-              const bool vis = j < p.Sk && qi < p.Sq && (!CAUSAL || j <= qi + off);
-              const float pr = vis ? ex2(__uint_as_float(sr[e + u]) * sl2 - v_lse[qc]) : 0.f;
-              pe[u] = pr;
-              de[u] = pr * (__uint_as_float(dr[e + u]) - v_delta[qc]);
-            }
-            pk[e / 2] = pack_p<BF16>(pe[0], pe[1]);
-            dk[e / 2] = pack_p<BF16>(de[0], de[1]);
-          }
-          // P^T over S^T columns [16c, 16c + 16), dS^T over dP^T's: both
-          // already read (chunk c / 2 <= c)
-          tmem_st16(lane_base + c * 16, pk);
-          tmem_st16(lane_base + 128 + c * 16, dk);
+        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
+          if (interior)
+            kv_chunk<BF16, false, CAUSAL>(lane_base, c, sl2, v_lse, v_delta, j, q0, p.Sq, p.Sk,
+                                          off);
+          else
+            kv_chunk<BF16, true, CAUSAL>(lane_base, c, sl2, v_lse, v_delta, j, q0, p.Sq, p.Sk,
+                                         off);
         }
         tmem_st_wait();
         tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_half(wg));  // this half of the queries is written
       }
       __syncwarp();
-      if (ok && lane == 0) mbar_arrive(p_ready);
     }
     // ------------------------------------------------------------- epilogue
     bool have = n_it > 0 && ok;
@@ -328,13 +425,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (n_it > 0 && !have) ok = false;
     if (have) tc_fence_after();
     // the tensor-memory loads are warp-wide (have, ok are warp-uniform); only
-    // the stores of keys inside the sequence are per lane
+    // the stores of keys inside the sequence are per lane.  Warpgroup wg
+    // writes columns wg D / 2 .. (wg + 1) D / 2 - 1 of dV and dK.
     const bool store = j < p.Sk && (ok || n_it == 0);
     const int64_t rbase = (((int64_t)b * p.Sk + (store ? j : 0)) * p.Hkv + g) * D;
     elem_t *dv = reinterpret_cast<elem_t *>(p.dv) + rbase;
     elem_t *dk = reinterpret_cast<elem_t *>(p.dk) + rbase;
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = wg * D / 64; c < (wg + 1) * D / 64; ++c) {
       float xv[32], xk[32];
       if (have) {
         uint32_t rv[32], rk[32];
@@ -384,8 +482,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::kBarOff;
-  const uint32_t q_full = bar0, s_full = bar0 + 40, ds_ready = bar0 + 48,
-                 acc_ready = bar0 + 56, drain = bar0 + 64;
+  const uint32_t q_full = bar0, s_full = bar0 + 40, acc_ready = bar0 + 56, drain = bar0 + 64;
+  // dS of keys 64h .. 64h + 63 written (h = 0, 1)
+  auto ds_half = [&](int hh) { return hh ? bar0 + 72u : bar0 + 48u; };
   auto st_full = [&](int s) { return bar0 + 8u + 8u * s; };
   auto st_empty = [&](int s) { return bar0 + 24u + 8u * s; };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
@@ -411,7 +510,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(st_empty(s), 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(ds_ready, 4);
+    mbar_init(ds_half(0), 4);
+    mbar_init(ds_half(1), 4);
     mbar_init(acc_ready, 1);
     mbar_init(drain, 1);
     fence_barrier_init();
@@ -485,11 +585,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         issue_ss<D>(tmem + 128, do_desc, make_sdesc_sw128(st + L::kTile, 16, 1024),
                     idesc_ss);  // dP = dO V^T
         tc_commit(s_full);
-        ok = wait_bar_spin(ds_ready, it & 1, abort_flag, limit, p.status);
+        // dQ += dS K (K tile MN-major: rows = keys), half by half
+        const uint64_t k_mn = make_sdesc_sw128(st, kChunkBytes, 1024);
+        for (int hh = 0; hh < 2 && ok; ++hh) {
+          ok = wait_bar_spin(ds_half(hh), it & 1, abort_flag, limit, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_ts_half(tmem + 256, tmem, k_mn, idesc_ts, hh, it > 0);
+        }
         if (!ok) break;
-        tc_fence_after();
-        // dQ += dS K (K tile MN-major: rows = keys)
-        issue_ts(tmem + 256, tmem, make_sdesc_sw128(st, kChunkBytes, 1024), idesc_ts, it > 0);
         tc_commit(st_empty(s));
       }
       tc_commit(acc_ready);
@@ -498,9 +602,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------ elementwise: one query row per thread
-    const int row = warp * 32 + lane;
+    const int quarter = warp & 3, wg = warp >> 2;  // TMEM lane quarter, column half
+    const int row = quarter * 32 + lane;
     const int qi = q0 + row;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
     const int64_t r = ((int64_t)b * p.Hq + h) * p.Sq + qi;
     const float lse2 = qi < p.Sq ? p.lse_l2[r] : INFINITY;
@@ -510,33 +615,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) ok = __all_sync(0xffffffffu, wait(s_full, it & 1));
       if (ok) {
         tc_fence_after();
+        const bool interior = (it + 1) * kBlockN <= p.Sk && q0 + kBlockM <= p.Sq &&
+                              (!CAUSAL || it * kBlockN + kBlockN - 1 <= q0 + off);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32], dr[32];
-          tmem_ld32(lane_base + c * 32, sr);
-          tmem_ld32(lane_base + 128 + c * 32, dr);
-          tmem_wait_ld32(sr);
-          tmem_wait_ld32(dr);
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float de[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int j = it * kBlockN + c * 32 + e + u;
-              const bool vis = j < p.Sk && qi < p.Sq && (!CAUSAL || j <= qi + off);
-              const float pr = vis ? ex2(__uint_as_float(sr[e + u]) * sl2 - lse2) : 0.f;
-              de[u] = pr * (__uint_as_float(dr[e + u]) - dlt);
-            }
-            pk[e / 2] = pack_p<BF16>(de[0], de[1]);
-          }
-          tmem_st16(lane_base + c * 16, pk);  // dS over S columns already read
+        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
+          if (interior)
+            q_chunk<BF16, false, CAUSAL>(lane_base, c, sl2, lse2, dlt, qi, it, p.Sq, p.Sk, off);
+          else
+            q_chunk<BF16, true, CAUSAL>(lane_base, c, sl2, lse2, dlt, qi, it, p.Sq, p.Sk, off);
         }
         tmem_st_wait();
         tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_half(wg));  // this half of the keys is written
       }
       __syncwarp();
-      if (ok && lane == 0) mbar_arrive(ds_ready);
     }
     bool have = n_kt > 0 && ok;
     if (have) have = __all_sync(0xffffffffu, wait(acc_ready, 0));
@@ -546,7 +639,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     elem_t *dq = reinterpret_cast<elem_t *>(p.dq) +
                  (((int64_t)b * p.Sq + (store ? qi : 0)) * p.Hq + h) * D;
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = wg * D / 64; c < (wg + 1) * D / 64; ++c) {
       float x[32];
       if (have) {
         uint32_t rq[32];
