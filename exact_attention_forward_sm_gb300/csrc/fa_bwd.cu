@@ -205,11 +205,12 @@ __device__ __forceinline__ void kv_chunk(uint32_t lane_base, int c, float sl2, c
 // Query pass, 32 key columns 32c .. 32c + 31 of key tile kt for one query
 // row: dS = exp2(S scale log2e - lse) (dP - Delta) as 16-bit pairs over S.
 template <bool BF16, bool MASKED, bool CAUSAL>
-__device__ __forceinline__ void q_chunk(uint32_t lane_base, int c, float sl2, float lse2,
-                                        float dlt, int qi, int kt, int Sq, int Sk, int off) {
+__device__ __forceinline__ void q_chunk(uint32_t lane_base, uint32_t dp_off, int c, float sl2,
+                                        float lse2, float dlt, int qi, int kt, int Sq, int Sk,
+                                        int off) {
   uint32_t sr[32], dr[32];
   tmem_ld32(lane_base + c * 32, sr);
-  tmem_ld32(lane_base + 128 + c * 32, dr);
+  tmem_ld32(lane_base + dp_off + c * 32, dr);
   tmem_wait_ld32(sr);
   tmem_wait_ld32(dr);
   uint32_t pk[16];
@@ -466,27 +467,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // -------------------------------------------------------------- query pass
+// Shared memory of the query pass: Q and dO resident, a three-slot K ring
+// (S of key tile it + 2 is computed while dQ += dS K of tile it may still
+// read K(it)) and a two-slot V ring.
+template <int D>
+struct SmemBwdQ {
+  static constexpr uint32_t kTile = (D / 64) * kChunkBytes;
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kDoOff = kTile;
+  static constexpr uint32_t kKOff = 2 * kTile;  // 3 slots
+  static constexpr uint32_t kVOff = 5 * kTile;  // 2 slots
+  static constexpr uint32_t kBarOff = 7 * kTile;
+  // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], sdp_full,
+  // ds_half[2], acc_ready, drain
+  static constexpr int kNumBars = 16;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kBytes = kMiscOff + 16;
+  static constexpr uint32_t kAlloc = kBytes + 1024 > 120u * 1024 ? kBytes + 1024 : 120u * 1024;
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
 // One CTA per (query tile, batch, query head), heaviest (latest) query tiles
 // first under causal masking.  dQ of the tile's 128 rows accumulates in
-// tensor memory over the key tiles the rows see.
+// tensor memory over the key tiles the rows see.  The scores alternate
+// between two tensor-memory buffers (columns 0-127 and 384-511; dP at
+// 128-255, dQ at 256-383): per key tile the MMA issuer runs dP(it + 1),
+// dQ += dS(it) K(it) and S(it + 2), so the elementwise work of tile it + 1
+// overlaps the last two.
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
-  using L = SmemBwd<D>;
+  using L = SmemBwdQ<D>;
   using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::kBarOff;
-  const uint32_t q_full = bar0, s_full = bar0 + 40, acc_ready = bar0 + 56, drain = bar0 + 64;
-  // dS of keys 64h .. 64h + 63 written (h = 0, 1)
-  auto ds_half = [&](int hh) { return hh ? bar0 + 72u : bar0 + 48u; };
-  auto st_full = [&](int s) { return bar0 + 8u + 8u * s; };
-  auto st_empty = [&](int s) { return bar0 + 24u + 8u * s; };
+  const uint32_t q_full = bar0, sdp_full = bar0 + 88, acc_ready = bar0 + 112,
+                 drain = bar0 + 120;
+  auto k_full = [&](int s) { return bar0 + 8u + 8u * s; };
+  auto k_empty = [&](int s) { return bar0 + 32u + 8u * s; };
+  auto v_full = [&](int s) { return bar0 + 56u + 8u * s; };
+  auto v_empty = [&](int s) { return bar0 + 72u + 8u * s; };
+  auto ds_half = [&](int hh) { return bar0 + 96u + 8u * hh; };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
@@ -505,13 +532,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(st_full(s), 1);
-      mbar_init(st_empty(s), 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(ds_half(0), 4);
-    mbar_init(ds_half(1), 4);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
+      mbar_init(ds_half(s), 4);
+    }
+    mbar_init(sdp_full, 1);
     mbar_init(acc_ready, 1);
     mbar_init(drain, 1);
     fence_barrier_init();
@@ -534,6 +564,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto wait = [&](uint32_t bar, uint32_t par) {
     return wait_bar(bar, par, abort_flag, limit, p.status);
   };
+  // score buffer of key tile it
+  auto s_buf = [&](int it) { return (it & 1) ? 384u : 0u; };
 
   if (warp == kBwdProducer) {
     if (lane == 0 && n_kt > 0) {
@@ -542,59 +574,87 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = true;
       mbar_arrive_expect_tx(q_full, 2 * L::kTile);
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_4d(sbase + L::kResOff + c * kChunkBytes, &tm_q, q_full, c * 64, h, q0, b,
+        tma_load_4d(sbase + L::kQOff + c * kChunkBytes, &tm_q, q_full, c * 64, h, q0, b,
                     pol_res);
-        tma_load_4d(sbase + L::kResOff + L::kTile + c * kChunkBytes, &tm_do, q_full, c * 64, h,
-                    q0, b, pol_res);
+        tma_load_4d(sbase + L::kDoOff + c * kChunkBytes, &tm_do, q_full, c * 64, h, q0, b,
+                    pol_res);
       }
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int it = 0; it < n_kt && ok; ++it) {
-        const int s = it & 1;
-        if (it >= 2 && !wait(st_empty(s), ((it >> 1) - 1) & 1)) {
+        const int ks = it % 3, vs = it & 1;
+        if (it >= 3 && !wait(k_empty(ks), ((it / 3) - 1) & 1)) {
           ok = false;
           break;
         }
-        const uint32_t dst = sbase + L::kStOff + s * 2 * L::kTile;
-        mbar_arrive_expect_tx(st_full(s), 2 * L::kTile);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(dst + c * kChunkBytes, &tm_k, st_full(s), c * 64, g, it * kBlockN, b,
-                      pol_st);
-          tma_load_4d(dst + L::kTile + c * kChunkBytes, &tm_v, st_full(s), c * 64, g,
-                      it * kBlockN, b, pol_st);
+        mbar_arrive_expect_tx(k_full(ks), L::kTile);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sbase + L::kKOff + ks * L::kTile + c * kChunkBytes, &tm_k, k_full(ks),
+                      c * 64, g, it * kBlockN, b, pol_st);
+        k_issued = it + 1;
+        if (it >= 2 && !wait(v_empty(vs), ((it >> 1) - 1) & 1)) {
+          ok = false;
+          break;
         }
-        issued = it + 1;
+        mbar_arrive_expect_tx(v_full(vs), L::kTile);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sbase + L::kVOff + vs * L::kTile + c * kChunkBytes, &tm_v, v_full(vs),
+                      c * 64, g, it * kBlockN, b, pol_st);
+        v_issued = it + 1;
       }
+      // drain the copies still in flight before the CTA exits
       wait_bar(q_full, 0, abort_flag, limit, p.status, false);
-      for (int it = max(0, issued - 2); it < issued; ++it)
-        wait_bar(st_full(it & 1), (it >> 1) & 1, abort_flag, limit, p.status, false);
+      for (int it = max(0, k_issued - 3); it < k_issued; ++it)
+        wait_bar(k_full(it % 3), (it / 3) & 1, abort_flag, limit, p.status, false);
+      for (int it = max(0, v_issued - 2); it < v_issued; ++it)
+        wait_bar(v_full(it & 1), (it >> 1) & 1, abort_flag, limit, p.status, false);
     }
   } else if (warp == kBwdMma) {
     if (lane == 0) {
       constexpr uint32_t idesc_ss = make_idesc_f16(BF16, kBlockM, kBlockN, false);
       constexpr uint32_t idesc_ts = make_idesc_f16(BF16, kBlockM, D, true);
-      const uint64_t q_desc = make_sdesc_sw128(sbase + L::kResOff, 16, 1024);
-      const uint64_t do_desc = make_sdesc_sw128(sbase + L::kResOff + L::kTile, 16, 1024);
+      const uint64_t q_desc = make_sdesc_sw128(sbase + L::kQOff, 16, 1024);
+      const uint64_t do_desc = make_sdesc_sw128(sbase + L::kDoOff, 16, 1024);
+      auto k_addr = [&](int it) { return sbase + L::kKOff + (it % 3) * L::kTile; };
+      auto v_addr = [&](int it) { return sbase + L::kVOff + (it & 1) * L::kTile; };
+      // S(it) = Q K(it)^T into its score buffer
+      auto issue_s = [&](int it) {
+        if (!wait(k_full(it % 3), (it / 3) & 1)) return false;
+        tc_fence_after();
+        issue_ss<D>(tmem + s_buf(it), q_desc, make_sdesc_sw128(k_addr(it), 16, 1024), idesc_ss);
+        return true;
+      };
+      // dP(it) = dO V(it)^T, then the V slot is released once it completes
+      auto issue_dp = [&](int it) {
+        if (!wait(v_full(it & 1), (it >> 1) & 1)) return false;
+        tc_fence_after();
+        issue_ss<D>(tmem + 128, do_desc, make_sdesc_sw128(v_addr(it), 16, 1024), idesc_ss);
+        tc_commit(v_empty(it & 1));
+        return true;
+      };
       bool ok = n_kt == 0 || wait(q_full, 0);
+      if (ok && n_kt > 0) {
+        ok = issue_s(0) && issue_dp(0);
+        if (ok) tc_commit(sdp_full);
+        if (ok && n_kt > 1) ok = issue_s(1);
+      }
       for (int it = 0; it < n_kt && ok; ++it) {
-        const int s = it & 1;
-        const uint32_t st = sbase + L::kStOff + s * 2 * L::kTile;
-        ok = wait(st_full(s), (it >> 1) & 1);
+        // dS(it) written by both warpgroups (and S(it), dP(it) read)
+        ok = wait_bar_spin(ds_half(0), it & 1, abort_flag, limit, p.status) &&
+             wait_bar_spin(ds_half(1), it & 1, abort_flag, limit, p.status);
         if (!ok) break;
         tc_fence_after();
-        issue_ss<D>(tmem, q_desc, make_sdesc_sw128(st, 16, 1024), idesc_ss);  // S = Q K^T
-        issue_ss<D>(tmem + 128, do_desc, make_sdesc_sw128(st + L::kTile, 16, 1024),
-                    idesc_ss);  // dP = dO V^T
-        tc_commit(s_full);
-        // dQ += dS K (K tile MN-major: rows = keys), half by half
-        const uint64_t k_mn = make_sdesc_sw128(st, kChunkBytes, 1024);
-        for (int hh = 0; hh < 2 && ok; ++hh) {
-          ok = wait_bar_spin(ds_half(hh), it & 1, abort_flag, limit, p.status);
+        if (it + 1 < n_kt) {  // the next tile's dP first: its elementwise waits on it
+          ok = issue_dp(it + 1);
           if (!ok) break;
-          tc_fence_after();
-          issue_ts_half(tmem + 256, tmem, k_mn, idesc_ts, hh, it > 0);
+          tc_commit(sdp_full);
         }
-        if (!ok) break;
-        tc_commit(st_empty(s));
+        // dQ += dS(it) K(it) (K tile MN-major: rows = keys)
+        const uint64_t k_mn = make_sdesc_sw128(k_addr(it), kChunkBytes, 1024);
+        issue_ts_half(tmem + 256, tmem + s_buf(it), k_mn, idesc_ts, 0, it > 0);
+        issue_ts_half(tmem + 256, tmem + s_buf(it), k_mn, idesc_ts, 1, it > 0);
+        tc_commit(k_empty(it % 3));
+        // S(it + 2) into the buffer dQ(it) reads (the pipe keeps issue order)
+        if (it + 2 < n_kt) ok = issue_s(it + 2);
       }
       tc_commit(acc_ready);
       tc_commit(drain);
@@ -612,17 +672,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float dlt = qi < p.Sq ? p.delta[r] : 0.f;
     bool ok = true;
     for (int it = 0; it < n_kt; ++it) {
-      if (ok) ok = __all_sync(0xffffffffu, wait(s_full, it & 1));
+      if (ok) ok = __all_sync(0xffffffffu, wait(sdp_full, it & 1));
       if (ok) {
         tc_fence_after();
         const bool interior = (it + 1) * kBlockN <= p.Sk && q0 + kBlockM <= p.Sq &&
                               (!CAUSAL || it * kBlockN + kBlockN - 1 <= q0 + off);
+        const uint32_t base = lane_base + s_buf(it);
+        const uint32_t dp_minus_s = 128u - s_buf(it);  // dP columns relative to base
 #pragma unroll 1
         for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
           if (interior)
-            q_chunk<BF16, false, CAUSAL>(lane_base, c, sl2, lse2, dlt, qi, it, p.Sq, p.Sk, off);
+            q_chunk<BF16, false, CAUSAL>(base, dp_minus_s, c, sl2, lse2, dlt, qi, it, p.Sq,
+                                         p.Sk, off);
           else
-            q_chunk<BF16, true, CAUSAL>(lane_base, c, sl2, lse2, dlt, qi, it, p.Sq, p.Sk, off);
+            q_chunk<BF16, true, CAUSAL>(base, dp_minus_s, c, sl2, lse2, dlt, qi, it, p.Sq,
+                                        p.Sk, off);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -673,12 +737,13 @@ cudaError_t launch_bwd_t(const BwdLaunch &a) {
     if (e != cudaSuccess) return e;
   }
   using L = SmemBwd<D>;
+  using LQ = SmemBwdQ<D>;
   auto kv = fa_bwd_kv_kernel<D, BF16, CAUSAL>;
   auto qk = fa_bwd_q_kernel<D, BF16, CAUSAL>;
   static BwdOptIn opt_kv, opt_q;
   cudaError_t e = opt_kv.ensure(kv, (int)L::kAlloc, a.device);
   if (e != cudaSuccess) return e;
-  e = opt_q.ensure(qk, (int)L::kAlloc, a.device);
+  e = opt_q.ensure(qk, (int)LQ::kAlloc, a.device);
   if (e != cudaSuccess) return e;
   const int64_t kv_ctas = (int64_t)p.k_tiles * p.B * p.Hkv;
   const int64_t q_ctas = (int64_t)p.q_tiles * p.B * p.Hq;
@@ -689,8 +754,8 @@ cudaError_t launch_bwd_t(const BwdLaunch &a) {
     if (e != cudaSuccess) return e;
   }
   if (q_ctas > 0) {
-    qk<<<(unsigned)q_ctas, kBwdThreads, L::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do,
-                                                              p);
+    qk<<<(unsigned)q_ctas, kBwdThreads, LQ::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v,
+                                                               a.tm_do, p);
     e = cudaGetLastError();
   }
   return e;
