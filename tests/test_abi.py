@@ -186,3 +186,33 @@ def test_no_alloc_checks_arguments_before_any_cuda_call(lib, bad):
 def test_no_alloc_empty_problem_is_a_no_op(lib):
     assert _call_noalloc(B=0) == fa.FA_OK
     assert _call_noalloc(Sq=0) == fa.FA_OK
+
+
+def _call_bwd(**kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=16, dout=16, dq=16, dk=16, dv=16, B=1, Hq=2, Hkv=2,
+                Sq=8, Sk=8, D=64, scale=0.125, causal=0, cu_seqlens_q=None, cu_seqlens_k=None,
+                workspace=16, workspace_bytes=1 << 20, stream=None, dtype=fa.FA_DTYPE_BF16)
+    args.update(kw)
+    return fa.fa_bwd(**args)
+
+
+@pytest.mark.parametrize("bad", [dict(B=-1), dict(Hq=3, Hkv=2), dict(Sq=-1), dict(causal=2),
+                                 dict(dtype=7), dict(scale=0.0), dict(scale=float("nan")),
+                                 dict(q=8), dict(dq=None), dict(workspace=None),
+                                 dict(workspace_bytes=8), dict(lse=18)])
+def test_backward_invalid_arguments_rejected_without_launch(lib, bad):
+    assert _call_bwd(**bad) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bad", [dict(D=256), dict(D=96), dict(cu_seqlens_q=64, cu_seqlens_k=64)])
+def test_backward_unsupported(lib, bad):
+    assert _call_bwd(**bad) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_backward_workspace_bytes(lib):
+    # lse in log2 units (rows rounded up to 4 floats), then delta
+    assert fa.fa_bwd_workspace_bytes(2, 4, 10) == 4 * 80 + 4 * 80
+    assert fa.fa_bwd_workspace_bytes(1, 1, 3) == 4 * 4 + 4 * 3
+    assert fa.fa_bwd_workspace_bytes(0, 4, 10) == 0
+    assert fa.fa_bwd_workspace_bytes(-1, 4, 10) == -fa.FA_ERR_INVALID_ARG
+    assert _call_bwd(B=0) == fa.FA_OK
