@@ -47,6 +47,10 @@ KERNEL_SOURCES = {
     "fa_fwd_wide_kernel": ["fa_fwd_wide.cuh", "fa_fwd_kernel.cuh", "fa_ptx.cuh",
                            "fa_launch.cuh"],
     "fa_bwd": ["fa_bwd.cu", "fa_bwd.cuh", "fa_fwd_kernel.cuh", "fa_ptx.cuh", "fa_launch.cuh"],
+    "fa_bwd_kv_kernel": ["fa_bwd.cu", "fa_bwd.cuh", "fa_fwd_kernel.cuh", "fa_ptx.cuh",
+                         "fa_launch.cuh"],
+    "fa_bwd_q_kernel": ["fa_bwd.cu", "fa_bwd.cuh", "fa_fwd_kernel.cuh", "fa_ptx.cuh",
+                        "fa_launch.cuh"],
 }
 
 

@@ -71,38 +71,57 @@ struct BwdOptIn {
 };
 
 // ---------------------------------------------------------------- row pass
-// Delta = rowsum(dO * O) in fp32 and the LSE in log2 units; one warp per row
-// (b, h, i), rows in LSE order.  A row without visible keys (LSE = -inf) gets
-// +inf, so exp2(s - lse) = 0 for it.
+// Delta = rowsum(dO * O) in fp32 and the LSE in log2 units, rows in LSE order
+// (b, h, i).  A row of D 16-bit values is D / 8 sixteen-byte chunks; each
+// thread reads one chunk of O and dO for each of two rows (all four loads in
+// flight together), and the D / 8 lanes of a row sum with shuffles.  A row
+// without visible keys (LSE = -inf) gets +inf, so exp2(s - lse) = 0 for it.
+constexpr int kRowsPerThread = 2;
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_rows_kernel(const BwdParams p) {
   using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  const int64_t rows = (int64_t)p.B * p.Hq * p.Sq;
-  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
-  const int64_t i = r % p.Sq;
-  const int64_t bh = r / p.Sq;
-  const int64_t h = bh % p.Hq, b = bh / p.Hq;
-  const int64_t off = ((b * p.Sq + i) * p.Hq + h) * D;
-  const elem_t *o = reinterpret_cast<const elem_t *>(p.o) + off;
-  const elem_t *g = reinterpret_cast<const elem_t *>(p.dout) + off;
-  // each lane reads D / 32 consecutive elements of both rows in one load
-  constexpr int kPer = D / 32;
-  using vec_t = typename std::conditional<kPer == 4, uint2, uint32_t>::type;
-  const vec_t vo = *reinterpret_cast<const vec_t *>(o + lane * kPer);
-  const vec_t vg = *reinterpret_cast<const vec_t *>(g + lane * kPer);
-  const elem_t *eo = reinterpret_cast<const elem_t *>(&vo);
-  const elem_t *eg = reinterpret_cast<const elem_t *>(&vg);
-  float acc = 0.f;
+  constexpr int kLanes = D / 8;               // threads per row
+  constexpr int kRowsPerBlock = 256 / kLanes;  // rows per pass of the block
+  // block -> (batch * head, chunk of the head's rows): one 32-bit division
+  const unsigned chunks = (unsigned)((p.Sq + kRowsPerThread * kRowsPerBlock - 1) /
+                                     (kRowsPerThread * kRowsPerBlock));
+  const unsigned bh = blockIdx.x / chunks, chunk = blockIdx.x - bh * chunks;
+  const int b = (int)(bh / (unsigned)p.Hq), h = (int)(bh - (unsigned)b * p.Hq);
+  const int sub = threadIdx.x % kLanes;
+  float acc[kRowsPerThread];
+  int64_t rid[kRowsPerThread];
+  bool valid[kRowsPerThread];
+  uint4 vo[kRowsPerThread], vg[kRowsPerThread];
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) acc += (float)eo[e] * (float)eg[e];
+  for (int u = 0; u < kRowsPerThread; ++u) {
+    const int i = (int)(chunk * kRowsPerThread + u) * kRowsPerBlock + threadIdx.x / kLanes;
+    valid[u] = i < p.Sq;
+    rid[u] = (int64_t)bh * p.Sq + i;
+    vo[u] = vg[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (valid[u]) {
+      const int64_t off = (((int64_t)b * p.Sq + i) * p.Hq + h) * D + sub * 8;
+      vo[u] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const elem_t *>(p.o) + off);
+      vg[u] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const elem_t *>(p.dout) + off);
+    }
+  }
 #pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
-    p.delta[r] = acc;
-    const float l = p.lse[r];
-    p.lse_l2[r] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+  for (int u = 0; u < kRowsPerThread; ++u) {
+    const elem_t *eo = reinterpret_cast<const elem_t *>(&vo[u]);
+    const elem_t *eg = reinterpret_cast<const elem_t *>(&vg[u]);
+    float a = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a += (float)eo[e] * (float)eg[e];
+#pragma unroll
+    for (int w = kLanes / 2; w > 0; w >>= 1) a += __shfl_xor_sync(0xffffffffu, a, w);
+    acc[u] = a;
+  }
+#pragma unroll
+  for (int u = 0; u < kRowsPerThread; ++u) {
+    if (sub == 0 && valid[u]) {
+      p.delta[rid[u]] = acc[u];
+      const float l = p.lse[rid[u]];
+      p.lse_l2[rid[u]] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+    }
   }
 }
 
@@ -387,16 +406,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int j = k0 + row;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
+    // warpgroup 0 loads a query tile's lse / Delta one step ahead, so the
+    // global-memory latency overlaps the previous step's work
+    float n_lse = INFINITY, n_delta = 0.f;
+    auto fetch = [&](int it) {
+      const int qi = it_tile(it) * kBlockM + row;
+      const int64_t r = ((int64_t)b * p.Hq + it_head(it)) * p.Sq + qi;
+      n_lse = qi < p.Sq ? p.lse_l2[r] : INFINITY;
+      n_delta = qi < p.Sq ? p.delta[r] : 0.f;
+    };
+    if (wg == 0 && n_it > 0) fetch(0);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
-      const int h = it_head(it), q0 = it_tile(it) * kBlockM;
+      const int q0 = it_tile(it) * kBlockM;
       float *v_lse = vec + s * 256, *v_delta = v_lse + 128;
       if (wg == 0) {
-        const int qi = q0 + row;
-        const int64_t r = ((int64_t)b * p.Hq + h) * p.Sq + qi;
-        v_lse[row] = qi < p.Sq ? p.lse_l2[r] : INFINITY;
-        v_delta[row] = qi < p.Sq ? p.delta[r] : 0.f;
+        v_lse[row] = n_lse;
+        v_delta[row] = n_delta;
+        if (it + 1 < n_it) fetch(it + 1);
       }
       named_barrier_sync(1, 256);
       if (ok) ok = __all_sync(0xffffffffu, wait(s_full, it & 1));
@@ -732,7 +760,10 @@ cudaError_t launch_bwd_t(const BwdLaunch &a) {
   const BwdParams &p = a.p;
   const int64_t rows = (int64_t)p.B * p.Hq * p.Sq;
   if (rows > 0) {
-    fa_bwd_rows_kernel<D, BF16><<<(unsigned)((rows + 7) / 8), 256, 0, a.stream>>>(p);
+    constexpr int64_t per_block = (int64_t)kRowsPerThread * 256 / (D / 8);
+    const int64_t blocks = (int64_t)p.B * p.Hq * ((p.Sq + per_block - 1) / per_block);
+    if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+    fa_bwd_rows_kernel<D, BF16><<<(unsigned)blocks, 256, 0, a.stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

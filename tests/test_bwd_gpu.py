@@ -139,3 +139,32 @@ def test_full_size_causal_benchmark_shape():
     release notes' backward finiteness check runs S = 2048 causal): every
     element of dq, dk, dv against the oracle."""
     _check(4, 16, 16, 2048, 2048, 128, "bf16", True, seed=2048)
+
+
+def test_full_size_gqa_rising_bias_workload():
+    """The GQA 4:1 workload with the rising per-key bias (B2 Hq32 Hkv8 S4096
+    D128 bf16 causal), its own seeded inputs, every gradient element against
+    the oracle.
+
+    The workload carries its bias in channel D-1: q[..., D-1] = 1 and
+    k[j, D-1] = b(j) ln2 / scale, up to |k| = 1256.  The row term
+    Delta = rowsum(dO * O) is read from the 16-bit O (as the standard
+    formulation does), so its rounding delta_i enters dq_i as
+    scale * delta_i * sum_j P_ij k_j, and in channel D-1 that product is as
+    large as dq itself (an fp64 emulation of the rounding alone moves that
+    channel by up to its own size).  dk, dv and dq's other channels are held
+    to the gates; channel D-1 of dq only to finiteness and to half of
+    max |dq|."""
+    from exact_attention_forward_sm_gb300 import workloads as wl
+    case = wl.make_workload(wl.BY_NAME["b2_hq32_hkv8_s4096_d128_bf16_causal_risingbias"])
+    g = torch.Generator().manual_seed(4096)
+    do = torch.randn(tuple(case.q.shape), generator=g).to(case.q.dtype)
+    dq, dk, dv = _run(case.q, case.k, case.v, do, True, scale=case.scale)
+    rq, rk, rv = oracle.attention_bwd(case.q, case.k, case.v, do, case.B, case.Hq, case.Hkv,
+                                      case.Sq, case.Sk, case.D, case.scale, True)
+    _compare("dk", dk, rk, "bf16")
+    _compare("dv", dv, rv, "bf16")
+    _compare("dq[..., :D-1]", dq[..., :-1].contiguous(), rq[..., :-1], "bf16")
+    carrier = dq[..., -1].float().cpu().numpy()
+    assert np.isfinite(carrier).all()
+    assert np.max(np.abs(carrier - rq[..., -1])) <= 0.5 * np.max(np.abs(rq))
