@@ -358,8 +358,7 @@ def attention_problem(args, fa, rank, dev, stream):
 
 # backward workloads: "bwd_" + a dense forward workload without score variants
 BWD_PREFIX = "bwd_"
-BWD_WORKLOADS = sorted(BWD_PREFIX + w.name for w in wl.WORKLOADS
-                       if w.D in (64, 128) and not w.varlen_count)
+BWD_WORKLOADS = sorted(BWD_PREFIX + w.name for w in wl.WORKLOADS if w.D in (64, 128))
 
 
 def backward_problem(args, fa, rank, dev, stream):
@@ -369,22 +368,25 @@ def backward_problem(args, fa, rank, dev, stream):
     case = wl.make_workload(w_rank)
     dtype_code = wl.DTYPE_CODE[case.dtype]
     q, k, v = (t.to(dev) for t in (case.q, case.k, case.v))
+    cu_q = case.cu_seqlens_q.to(dev) if case.varlen else None
+    cu_k = case.cu_seqlens_k.to(dev) if case.varlen else None
     o = torch.empty_like(q)
-    lse = torch.empty((case.B, case.Hq, case.Sq), dtype=torch.float32, device=dev)
+    lse_shape = (case.Hq, case.Sq) if case.varlen else (case.B, case.Hq, case.Sq)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
     st = fa.fa_fwd(q, k, v, o, lse, case.B, case.Hq, case.Hkv, case.Sq, case.Sk, case.D,
-                   case.scale, int(case.causal), None, None, stream, dtype_code)
+                   case.scale, int(case.causal), cu_q, cu_k, stream, dtype_code)
     if st != fa.FA_OK:
         raise RuntimeError(f"fa_fwd: {fa.fa_status_string(st)}")
     g = torch.Generator().manual_seed(w_rank.seed + 17)
     dout_h = torch.randn(tuple(case.q.shape), generator=g).to(case.q.dtype)
     dout = dout_h.to(dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    nbytes = fa.fa_bwd_workspace_bytes(case.B, case.Hq, case.Sq)
+    nbytes = fa.fa_bwd_workspace_bytes(1 if case.varlen else case.B, case.Hq, case.Sq)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
 
     def launch():
         rc = fa.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, case.B, case.Hq, case.Hkv, case.Sq,
-                       case.Sk, case.D, case.scale, int(case.causal), None, None, ws, nbytes,
+                       case.Sk, case.D, case.scale, int(case.causal), cu_q, cu_k, ws, nbytes,
                        stream, dtype_code)
         if rc != fa.FA_OK:
             raise RuntimeError(f"fa_bwd: {fa.fa_status_string(rc)}")
@@ -392,19 +394,24 @@ def backward_problem(args, fa, rank, dev, stream):
     torch.cuda.synchronize()
     o_h, lse_h = o.cpu(), lse.cpu()
     elem = 2
-    rows = case.B * case.Hq * case.Sq
+    rows = case.lse_rows()
     n_q, n_k = case.q.numel(), case.k.numel()
     # read q, k, v, o, dout, lse; write dq, dk, dv; the row pass's two fp32
     # values per row written once and read by both tile passes
     alg_bytes = elem * (3 * n_q + 2 * n_k) + 4 * rows + elem * (n_q + 2 * n_k) + 8 * rows * 3
     config = {"workload": args.workload, "pass": "backward (dq, dk, dv)", "B": case.B,
               "Hq": case.Hq, "Hkv": case.Hkv, "Sq": case.Sq, "Sk": case.Sk, "D": case.D,
-              "causal": case.causal, "flops": "2.5 x forward (dS, dP recomputed: the kernels "
-              "run 3.5 x forward on the tensor cores)"}
+              "causal": case.causal, "varlen": case.varlen,
+              "flops": "2.5 x forward (S and dP recomputed: the kernels run 3.5 x forward "
+              "on the tensor cores)"}
+    host_in = [case.q, case.k, case.v, o_h, lse_h, dout_h]
+    dev_in = [q, k, v, o, lse, dout]
+    if case.varlen:
+        host_in += [case.cu_seqlens_q, case.cu_seqlens_k]
+        dev_in += [cu_q, cu_k]
+    sample = (None if case.varlen else lambda secs: oracle_sample_bwd(case, dout_h, secs))
     return Problem(args.workload, case.dtype, 2.5 * wl.attention_flops(case), alg_bytes,
-                   [case.q, case.k, case.v, o_h, lse_h, dout_h], [q, k, v, o, lse, dout],
-                   [dq, dk, dv], launch, 3, config,
-                   lambda secs: oracle_sample_bwd(case, dout_h, secs), kernel="fa_bwd")
+                   host_in, dev_in, [dq, dk, dv], launch, 3, config, sample, kernel="fa_bwd")
 
 
 def kvcache_problem(args, fa, rank, dev, stream):
@@ -698,7 +705,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     line, prob = run_gpu_arm(args, rank, local_rank, world)
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and prob.oracle_sample is not None:
         cb = prob.oracle_sample(args.cpu_baseline_s)
         line["cpu_baseline"] = {
             "value": cb["tflops"], "unit": UNIT, "cores": cb["threads"], "kind": "oracle",

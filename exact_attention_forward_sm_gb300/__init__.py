@@ -253,12 +253,15 @@ def fa_bwd_workspace_bytes(B, Hq, Sq) -> int:
     return int(load_library().fa_bwd_workspace_bytes(int(B), int(Hq), int(Sq)))
 
 
-def attention_backward(q, k, v, out, lse, dout, causal=False, scale=None, stream=None):
-    """Gradients of exact attention on dense CUDA tensors; returns ``(dq, dk, dv)``.
+def attention_backward(q, k, v, out, lse, dout, causal=False, scale=None, stream=None,
+                       cu_seqlens_q=None, cu_seqlens_k=None):
+    """Gradients of exact attention on CUDA tensors; returns ``(dq, dk, dv)``.
 
-    q / out / dout [B, Sq, Hq, D], k / v [B, Sk, Hkv, D], lse [B, Hq, Sq] as
-    :func:`attention_forward` returned them.  The workspace is a PyTorch
-    allocation; everything else runs in ``fa_bwd``'s kernels.
+    Dense: q / out / dout [B, Sq, Hq, D], k / v [B, Sk, Hkv, D], lse
+    [B, Hq, Sq]; packed: q / out / dout [total_q, Hq, D], k / v [total_k, Hkv,
+    D], lse [Hq, total_q] with int32 cu_seqlens, as :func:`attention_forward`
+    returned them.  The workspace is a PyTorch allocation; everything else
+    runs in ``fa_bwd``'s kernels.
     """
     import torch
 
@@ -268,19 +271,25 @@ def attention_backward(q, k, v, out, lse, dout, causal=False, scale=None, stream
     for t in (q, k, v, out, lse, dout):
         if not t.is_contiguous():
             raise FaError(FA_ERR_INVALID_ARG, "attention_backward (contiguity)")
-    B, Sq, Hq, D = q.shape
-    Sk, Hkv = k.shape[1], k.shape[2]
+    if cu_seqlens_q is None:
+        B, Sq, Hq, D = q.shape
+        Sk, Hkv = k.shape[1], k.shape[2]
+        rows_b = B
+    else:
+        Sq, Hq, D = q.shape
+        Sk, Hkv = k.shape[0], k.shape[1]
+        B, rows_b = cu_seqlens_q.numel() - 1, 1
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    nbytes = fa_bwd_workspace_bytes(B, Hq, Sq)
+    nbytes = fa_bwd_workspace_bytes(rows_b, Hq, Sq)
     if nbytes < 0:
         raise FaError(-nbytes, "fa_bwd_workspace_bytes")
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     st = fa_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, D, scale,
-                int(bool(causal)), None, None, ws, nbytes, stream, dtype)
+                int(bool(causal)), cu_seqlens_q, cu_seqlens_k, ws, nbytes, stream, dtype)
     if st != FA_OK:
         raise FaError(st, "fa_bwd")
     return dq, dk, dv

@@ -641,7 +641,11 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (cu_seqlens_q || cu_seqlens_k) return FA_ERR_UNSUPPORTED;
+  const bool varlen = cu_seqlens_q != nullptr;
+  if (varlen != (cu_seqlens_k != nullptr)) return FA_ERR_INVALID_ARG;
+  if (varlen && ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) ||
+                 (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u)))
+    return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
   if (B == 0) return FA_OK;
   const bool rows_q = Sq > 0, rows_k = Sk > 0;
@@ -651,19 +655,23 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
     return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_INVALID_ARG;
-  const long long need = fa_bwd_workspace_bytes(B, Hq, Sq);
+  // packed: Sq / Sk are the token totals and the workspace is sized as for
+  // one batch of Sq rows
+  const int rows_b = varlen ? 1 : B;
+  const long long need = fa_bwd_workspace_bytes(rows_b, Hq, Sq);
   if (rows_q && workspace_bytes < need) return FA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t elem = 2;
   // no keys: dq = 0; no queries: dk = dv = 0
   if (!rows_k) {
-    if (rows_q && cudaMemsetAsync(dq, 0, (size_t)B * Sq * Hq * D * elem, st) != cudaSuccess)
+    if (rows_q &&
+        cudaMemsetAsync(dq, 0, (size_t)rows_b * Sq * Hq * D * elem, st) != cudaSuccess)
       return FA_ERR_CUDA;
     return FA_OK;
   }
   if (!rows_q) {
-    if (cudaMemsetAsync(dk, 0, (size_t)B * Sk * Hkv * D * elem, st) != cudaSuccess ||
-        cudaMemsetAsync(dv, 0, (size_t)B * Sk * Hkv * D * elem, st) != cudaSuccess)
+    if (cudaMemsetAsync(dk, 0, (size_t)rows_b * Sk * Hkv * D * elem, st) != cudaSuccess ||
+        cudaMemsetAsync(dv, 0, (size_t)rows_b * Sk * Hkv * D * elem, st) != cudaSuccess)
       return FA_ERR_CUDA;
     return FA_OK;
   }
@@ -673,10 +681,12 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
   if (!status) return FA_ERR_CUDA;
   const bool bf16 = dtype == FA_DTYPE_BF16;
   fa::BwdLaunch a;
-  if (!make_map(&a.tm_q, q, bf16, D, Hq, Sq, B) || !make_map(&a.tm_do, dout, bf16, D, Hq, Sq, B) ||
-      !make_map(&a.tm_k, k, bf16, D, Hkv, Sk, B) || !make_map(&a.tm_v, v, bf16, D, Hkv, Sk, B))
+  if (!make_map(&a.tm_q, q, bf16, D, Hq, Sq, rows_b) ||
+      !make_map(&a.tm_do, dout, bf16, D, Hq, Sq, rows_b) ||
+      !make_map(&a.tm_k, k, bf16, D, Hkv, Sk, rows_b) ||
+      !make_map(&a.tm_v, v, bf16, D, Hkv, Sk, rows_b))
     return FA_ERR_CUDA;
-  const long long rows = (long long)B * Hq * Sq;
+  const long long rows = (long long)rows_b * Hq * Sq;
   fa::BwdParams &p = a.p;
   p.o = o;
   p.dout = dout;
@@ -686,6 +696,8 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -700,7 +712,7 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
   p.status = status;
   a.stream = st;
   a.device = device;
-  return fa::launch_bwd(a, D, bf16, causal != 0) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return fa::launch_bwd(a, D, bf16, causal != 0, varlen) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_shutdown(void) {

@@ -41,7 +41,7 @@ struct SmemBwd {
   static constexpr uint32_t kStOff = 2 * kTile;
   static constexpr uint32_t kVecOff = kStOff + 4 * kTile;  // [2][2][128] floats (key pass)
   static constexpr uint32_t kBarOff = kVecOff + 2048;
-  static constexpr int kNumBars = 10;
+  static constexpr int kNumBars = 12;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   // at least 120 KB, so that two CTAs never share an SM: each allocates all
@@ -202,16 +202,20 @@ __device__ __forceinline__ void kv_chunk(uint32_t lane_base, int c, float sl2, c
     fma_f32x2(x0, x1, __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]), sl2, sl2,
               -lv.x, -lv.y);
     float p0 = ex2(x0), p1 = ex2(x1);
-    if (MASKED) {
-      const int qi = q0 + c * 32 + 2 * e;
-      const bool ok_j = j < Sk;
-      p0 = (ok_j && qi < Sq && (!CAUSAL || j <= qi + off)) ? p0 : 0.f;
-      p1 = (ok_j && qi + 1 < Sq && (!CAUSAL || j <= qi + 1 + off)) ? p1 : 0.f;
-    }
     float t0 = __uint_as_float(dr[2 * e]), t1 = __uint_as_float(dr[2 * e + 1]);
     add_f32x2(t0, t1, -dv.x, -dv.y);
     float d0, d1;
     mul2(d0, d1, p0, p1, t0, t1);
+    if (MASKED) {  // selects, not products: a masked score may be inf or NaN
+      const int qi = q0 + c * 32 + 2 * e;
+      const bool ok_j = j < Sk;
+      const bool v0 = ok_j && qi < Sq && (!CAUSAL || j <= qi + off);
+      const bool v1 = ok_j && qi + 1 < Sq && (!CAUSAL || j <= qi + 1 + off);
+      p0 = v0 ? p0 : 0.f;
+      p1 = v1 ? p1 : 0.f;
+      d0 = v0 ? d0 : 0.f;
+      d1 = v1 ? d1 : 0.f;
+    }
     pk[e] = pack_p<BF16>(p0, p1);
     dk[e] = pack_p<BF16>(d0, d1);
   }
@@ -239,19 +243,82 @@ __device__ __forceinline__ void q_chunk(uint32_t lane_base, uint32_t dp_off, int
     fma_f32x2(x0, x1, __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]), sl2, sl2,
               -lse2, -lse2);
     float p0 = ex2(x0), p1 = ex2(x1);
-    if (MASKED) {
-      const int j = kt * kBlockN + c * 32 + 2 * e;
-      const bool ok_q = qi < Sq;
-      p0 = (ok_q && j < Sk && (!CAUSAL || j <= qi + off)) ? p0 : 0.f;
-      p1 = (ok_q && j + 1 < Sk && (!CAUSAL || j + 1 <= qi + off)) ? p1 : 0.f;
-    }
     float t0 = __uint_as_float(dr[2 * e]), t1 = __uint_as_float(dr[2 * e + 1]);
     add_f32x2(t0, t1, -dlt, -dlt);
     float d0, d1;
     mul2(d0, d1, p0, p1, t0, t1);
+    if (MASKED) {  // selects, not products: a masked score may be inf or NaN
+      const int j = kt * kBlockN + c * 32 + 2 * e;
+      const bool ok_q = qi < Sq;
+      d0 = (ok_q && j < Sk && (!CAUSAL || j <= qi + off)) ? d0 : 0.f;
+      d1 = (ok_q && j + 1 < Sk && (!CAUSAL || j + 1 <= qi + off)) ? d1 : 0.f;
+    }
     pk[e] = pack_p<BF16>(d0, d1);
   }
   tmem_st16(lane_base + packed_col(c), pk);  // dS over S columns this warp read
+}
+
+// The sequence and 128-row tile of tile `idx` of a packed problem, counting
+// every sequence's ceil(len / 128) tiles in order (lengths from the offsets
+// cu[0 .. B]); {-1, 0} past the last tile.  Warp-collective: every lane of
+// the calling warp gets the same result.
+__device__ __forceinline__ int2 packed_tile(const int32_t *cu, int B, int idx, int lane) {
+  int base = 0;
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const int bb = b0 + lane;
+    int cnt = 0;
+    if (bb < B) {
+      const int len = cu[bb + 1] - cu[bb];
+      cnt = len > 0 ? (len + kBlockM - 1) / kBlockM : 0;
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    const int excl = incl - cnt;
+    const unsigned m = __ballot_sync(0xffffffffu, bb < B && idx >= base + excl && idx < base + incl);
+    if (m) {
+      const int src = __ffs(m) - 1;
+      return make_int2(b0 + src, idx - base - __shfl_sync(0xffffffffu, excl, src));
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return make_int2(-1, 0);
+}
+
+// Where a CTA's sequence lives: lengths, first token of its queries and keys
+// in the tensors, and the batch coordinate of the tensor maps (dense: b;
+// packed: 0, rows addressed by token).
+struct SeqRef {
+  int lq, lk, q_tok0, k_tok0, map_b;
+};
+
+__device__ __forceinline__ bool packed_seq(const BwdParams &p, int b, SeqRef *r) {
+  const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+  if (q0 < 0 || q1 < q0 || q1 > p.Sq || k0 < 0 || k1 < k0 || k1 > p.Sk) return false;
+  r->lq = q1 - q0;
+  r->lk = k1 - k0;
+  r->q_tok0 = q0;
+  r->k_tok0 = k0;
+  r->map_b = 0;
+  return true;
+}
+
+// Zero rows [valid, 128) of a 128-row tile of D 16-bit columns in shared
+// memory (whole 128-byte rows of each 64-column chunk, so the swizzle does
+// not matter) and make the writes visible to the tensor core's proxy; the
+// whole warp takes part.  A packed tile reaching past its sequence would
+// otherwise feed the next sequence's rows (finite or not) into a product
+// where 0 * inf = NaN.
+template <int D>
+__device__ __forceinline__ void zero_tail_rows(uint32_t tile, int valid, int lane) {
+#pragma unroll 1
+  for (int c = 0; c < D / 64; ++c)
+#pragma unroll 1
+    for (uint32_t o = (uint32_t)valid * 128u + lane * 16u; o < kChunkBytes; o += 512u)
+      st_shared_v4(tile + c * kChunkBytes + o, 0u, 0u, 0u, 0u);
 }
 
 // ---------------------------------------------------------------- key pass
@@ -259,7 +326,7 @@ __device__ __forceinline__ void q_chunk(uint32_t lane_base, uint32_t dp_off, int
 // causal masking.  dV and dK of the tile's 128 keys accumulate in tensor
 // memory over every query tile that sees a key of the tile, for every query
 // head of the group.
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -278,21 +345,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto st_empty = [&](int s) { return bar0 + 24u + 8u * s; };
   // P^T / dS^T of queries 64h .. 64h + 63 written (h = 0, 1)
   auto p_half = [&](int h) { return h ? bar0 + 72u : bar0 + 48u; };
+  // packed: stage s's query rows past the sequence zeroed
+  auto st_fixed = [&](int s) { return bar0 + 80u + 8u * s; };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
   float *vec = reinterpret_cast<float *>(smem + L::kVecOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heavy-first: the key tile is the slowest-varying part of the CTA index
-  const int bg = blockIdx.x % (p.B * p.Hkv);
-  const int kt = blockIdx.x / (p.B * p.Hkv);
-  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  int b, g, kt;
+  SeqRef sq{p.Sq, p.Sk, 0, 0, 0};
+  if (VARLEN) {
+    // key tiles of all sequences in order, K/V head fastest; CTAs past the
+    // last tile have nothing to do
+    g = blockIdx.x % p.Hkv;
+    const int2 bt = packed_tile(p.cu_k, p.B, blockIdx.x / p.Hkv, lane);
+    b = bt.x;
+    kt = bt.y;
+    if (b < 0) return;
+    if (!packed_seq(p, b, &sq)) {
+      if (threadIdx.x == 0) record_status(p.status, 5);
+      return;
+    }
+  } else {
+    // heavy-first: the key tile is the slowest-varying part of the CTA index
+    const int bg = blockIdx.x % (p.B * p.Hkv);
+    kt = blockIdx.x / (p.B * p.Hkv);
+    b = bg / p.Hkv;
+    g = bg % p.Hkv;
+    sq.map_b = b;
+  }
+  const int lq = sq.lq, lk = sq.lk;
   const int k0 = kt * kBlockN;
-  const int off = p.Sk - p.Sq;  // bottom-right aligned causal diagonal
+  const int off = lk - lq;  // bottom-right aligned causal diagonal
   int qt_begin = 0;
   if (CAUSAL) qt_begin = max(0, k0 - off) / kBlockM;
-  const int nq = max(0, p.q_tiles - qt_begin);
+  const int nq = max(0, (lq + kBlockM - 1) / kBlockM - qt_begin);
   const int n_it = nq * p.group;
+  // rows of this sequence in the LSE / workspace order and in the outputs
+  const int64_t lse_row0 = VARLEN ? (int64_t)sq.q_tok0 : 0;
+  const int64_t lse_b = VARLEN ? 0 : (int64_t)b;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -306,6 +397,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(p_half(1), 4);
     mbar_init(acc_ready, 1);
     mbar_init(drain, 1);
+    mbar_init(st_fixed(0), 1);
+    mbar_init(st_fixed(1), 1);
     fence_barrier_init();
   }
   if (warp == kBwdMma) {
@@ -328,40 +421,61 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   };
   auto it_head = [&](int it) { return g * p.group + it / nq; };
   auto it_tile = [&](int it) { return qt_begin + it % nq; };
+  // packed: the query tile of step it reaches past the sequence's rows
+  auto it_partial = [&](int it) { return VARLEN && it_tile(it) * kBlockM + kBlockM > lq; };
 
   if (warp == kBwdProducer) {
-    if (lane == 0 && n_it > 0) {
+    if (n_it > 0) {
       const uint64_t pol_res = policy_evict_first();
       const uint64_t pol_st = policy_evict_last();
       bool ok = true;
-      mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_4d(sbase + L::kResOff + c * kChunkBytes, &tm_k, kv_full, c * 64, g, k0, b,
-                    pol_res);
-        tma_load_4d(sbase + L::kResOff + L::kTile + c * kChunkBytes, &tm_v, kv_full, c * 64, g,
-                    k0, b, pol_res);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(sbase + L::kResOff + c * kChunkBytes, &tm_k, kv_full, c * 64, g,
+                      sq.k_tok0 + k0, sq.map_b, pol_res);
+          tma_load_4d(sbase + L::kResOff + L::kTile + c * kChunkBytes, &tm_v, kv_full, c * 64,
+                      g, sq.k_tok0 + k0, sq.map_b, pol_res);
+        }
       }
       int issued = 0;
+      uint32_t fixpar = 0;  // bit s: phase of st_fixed(s)
       for (int it = 0; it < n_it && ok; ++it) {
         const int s = it & 1;
-        if (it >= 2 && !wait(st_empty(s), ((it >> 1) - 1) & 1)) {
-          ok = false;
-          break;
-        }
+        if (lane == 0 && it >= 2 && !wait(st_empty(s), ((it >> 1) - 1) & 1)) ok = false;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
         const int h = it_head(it), q0 = it_tile(it) * kBlockM;
         const uint32_t dst = sbase + L::kStOff + s * 2 * L::kTile;
-        mbar_arrive_expect_tx(st_full(s), 2 * L::kTile);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(dst + c * kChunkBytes, &tm_q, st_full(s), c * 64, h, q0, b, pol_st);
-          tma_load_4d(dst + L::kTile + c * kChunkBytes, &tm_do, st_full(s), c * 64, h, q0, b,
-                      pol_st);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(st_full(s), 2 * L::kTile);
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d(dst + c * kChunkBytes, &tm_q, st_full(s), c * 64, h, sq.q_tok0 + q0,
+                        sq.map_b, pol_st);
+            tma_load_4d(dst + L::kTile + c * kChunkBytes, &tm_do, st_full(s), c * 64, h,
+                        sq.q_tok0 + q0, sq.map_b, pol_st);
+          }
         }
         issued = it + 1;
+        if (it_partial(it)) {
+          // rows past the sequence belong to the next one: zero them in Q and
+          // dO (the B operands of dV += P^T dO and dK += dS^T Q) once landed
+          ok = __all_sync(0xffffffffu, wait(st_full(s), (it >> 1) & 1));
+          if (!ok) break;
+          zero_tail_rows<D>(dst, lq - q0, lane);
+          zero_tail_rows<D>(dst + L::kTile, lq - q0, lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(st_fixed(s));
+          fixpar ^= 1u << s;
+        }
       }
       // drain the copies still in flight before the CTA exits
-      wait_bar(kv_full, 0, abort_flag, limit, p.status, false);
-      for (int it = max(0, issued - 2); it < issued; ++it)
-        wait_bar(st_full(it & 1), (it >> 1) & 1, abort_flag, limit, p.status, false);
+      if (lane == 0) {
+        wait_bar(kv_full, 0, abort_flag, limit, p.status, false);
+        for (int it = max(0, issued - 2); it < issued; ++it)
+          wait_bar(st_full(it & 1), (it >> 1) & 1, abort_flag, limit, p.status, false);
+      }
     }
   } else if (warp == kBwdMma) {
     if (lane == 0) {
@@ -370,10 +484,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t k_desc = make_sdesc_sw128(sbase + L::kResOff, 16, 1024);
       const uint64_t v_desc = make_sdesc_sw128(sbase + L::kResOff + L::kTile, 16, 1024);
       bool ok = n_it == 0 || wait(kv_full, 0);
+      uint32_t fixpar = 0;  // bit s: phase of st_fixed(s), as the producer counts it
       for (int it = 0; it < n_it && ok; ++it) {
         const int s = it & 1;
         const uint32_t st = sbase + L::kStOff + s * 2 * L::kTile;
-        ok = wait(st_full(s), (it >> 1) & 1);
+        if (it_partial(it)) {
+          ok = wait(st_fixed(s), (fixpar >> s) & 1u);
+          fixpar ^= 1u << s;
+        } else {
+          ok = wait(st_full(s), (it >> 1) & 1);
+        }
         if (!ok) break;
         tc_fence_after();
         issue_ss<D>(tmem, k_desc, make_sdesc_sw128(st, 16, 1024), idesc_ss);  // S^T = K Q^T
@@ -411,9 +531,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float n_lse = INFINITY, n_delta = 0.f;
     auto fetch = [&](int it) {
       const int qi = it_tile(it) * kBlockM + row;
-      const int64_t r = ((int64_t)b * p.Hq + it_head(it)) * p.Sq + qi;
-      n_lse = qi < p.Sq ? p.lse_l2[r] : INFINITY;
-      n_delta = qi < p.Sq ? p.delta[r] : 0.f;
+      const int64_t r = (lse_b * p.Hq + it_head(it)) * p.Sq + lse_row0 + qi;
+      n_lse = qi < lq ? p.lse_l2[r] : INFINITY;
+      n_delta = qi < lq ? p.delta[r] : 0.f;
     };
     if (wg == 0 && n_it > 0) fetch(0);
     bool ok = true;
@@ -430,16 +550,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) ok = __all_sync(0xffffffffu, wait(s_full, it & 1));
       if (ok) {
         tc_fence_after();
-        const bool interior = k0 + kBlockN <= p.Sk && q0 + kBlockM <= p.Sq &&
+        const bool interior = k0 + kBlockN <= lk && q0 + kBlockM <= lq &&
                               (!CAUSAL || k0 + kBlockN - 1 <= q0 + off);
 #pragma unroll 1
         for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
           if (interior)
-            kv_chunk<BF16, false, CAUSAL>(lane_base, c, sl2, v_lse, v_delta, j, q0, p.Sq, p.Sk,
+            kv_chunk<BF16, false, CAUSAL>(lane_base, c, sl2, v_lse, v_delta, j, q0, lq, lk,
                                           off);
           else
-            kv_chunk<BF16, true, CAUSAL>(lane_base, c, sl2, v_lse, v_delta, j, q0, p.Sq, p.Sk,
-                                         off);
+            kv_chunk<BF16, true, CAUSAL>(lane_base, c, sl2, v_lse, v_delta, j, q0, lq, lk, off);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -456,8 +575,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // the tensor-memory loads are warp-wide (have, ok are warp-uniform); only
     // the stores of keys inside the sequence are per lane.  Warpgroup wg
     // writes columns wg D / 2 .. (wg + 1) D / 2 - 1 of dV and dK.
-    const bool store = j < p.Sk && (ok || n_it == 0);
-    const int64_t rbase = (((int64_t)b * p.Sk + (store ? j : 0)) * p.Hkv + g) * D;
+    const bool store = j < lk && (ok || n_it == 0);
+    const int64_t rbase = ((lse_b * p.Sk + sq.k_tok0 + (store ? j : 0)) * p.Hkv + g) * D;
     elem_t *dv = reinterpret_cast<elem_t *>(p.dv) + rbase;
     elem_t *dk = reinterpret_cast<elem_t *>(p.dk) + rbase;
 #pragma unroll 1
@@ -507,8 +626,8 @@ struct SmemBwdQ {
   static constexpr uint32_t kVOff = 5 * kTile;  // 2 slots
   static constexpr uint32_t kBarOff = 7 * kTile;
   // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], sdp_full,
-  // ds_half[2], acc_ready, drain
-  static constexpr int kNumBars = 16;
+  // ds_half[2], acc_ready, drain, k_fixed[3]
+  static constexpr int kNumBars = 19;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024 > 120u * 1024 ? kBytes + 1024 : 120u * 1024;
@@ -522,7 +641,7 @@ struct SmemBwdQ {
 // 128-255, dQ at 256-383): per key tile the MMA issuer runs dP(it + 1),
 // dQ += dS(it) K(it) and S(it + 2), so the elementwise work of tile it + 1
 // overlaps the last two.
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -542,20 +661,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto v_full = [&](int s) { return bar0 + 56u + 8u * s; };
   auto v_empty = [&](int s) { return bar0 + 72u + 8u * s; };
   auto ds_half = [&](int hh) { return bar0 + 96u + 8u * hh; };
+  // packed: K slot s's rows past the sequence's keys zeroed
+  auto k_fixed = [&](int s) { return bar0 + 128u + 8u * s; };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x % (p.B * p.Hq);
-  const int qt = p.q_tiles - 1 - (int)(blockIdx.x / (p.B * p.Hq));
-  const int b = bh / p.Hq, h = bh % p.Hq, g = h / p.group;
-  const int q0 = qt * kBlockM;
-  const int off = p.Sk - p.Sq;
-  int n_kt = p.k_tiles;
-  if (CAUSAL) {
-    const int last = min(q0 + kBlockM, p.Sq) - 1 + off;  // last key any row sees
-    n_kt = last < 0 ? 0 : min(p.k_tiles, last / kBlockN + 1);
+  int b, h, qt;
+  SeqRef sq{p.Sq, p.Sk, 0, 0, 0};
+  if (VARLEN) {
+    // query tiles of all sequences in order, query head fastest
+    h = blockIdx.x % p.Hq;
+    const int2 bt = packed_tile(p.cu_q, p.B, blockIdx.x / p.Hq, lane);
+    b = bt.x;
+    qt = bt.y;
+    if (b < 0) return;
+    if (!packed_seq(p, b, &sq)) {
+      if (threadIdx.x == 0) record_status(p.status, 5);
+      return;
+    }
+  } else {
+    const int bh = blockIdx.x % (p.B * p.Hq);
+    qt = p.q_tiles - 1 - (int)(blockIdx.x / (p.B * p.Hq));  // latest (heaviest) first
+    b = bh / p.Hq;
+    h = bh % p.Hq;
+    sq.map_b = b;
   }
+  const int g = h / p.group;
+  const int lq = sq.lq, lk = sq.lk;
+  const int q0 = qt * kBlockM;
+  const int off = lk - lq;
+  const int k_tiles = (lk + kBlockN - 1) / kBlockN;
+  int n_kt = k_tiles;
+  if (CAUSAL) {
+    const int last = min(q0 + kBlockM, lq) - 1 + off;  // last key any row sees
+    n_kt = last < 0 ? 0 : min(k_tiles, last / kBlockN + 1);
+  }
+  const int64_t lse_b = VARLEN ? 0 : (int64_t)b;
+  const int64_t lse_row0 = VARLEN ? (int64_t)sq.q_tok0 : 0;
+  // packed: key tile it reaches past the sequence's keys
+  auto k_partial = [&](int it) { return VARLEN && it * kBlockN + kBlockN > lk; };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -572,6 +717,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(sdp_full, 1);
     mbar_init(acc_ready, 1);
     mbar_init(drain, 1);
+    for (int s = 0; s < 3; ++s) mbar_init(k_fixed(s), 1);
     fence_barrier_init();
   }
   if (warp == kBwdMma) {
@@ -596,45 +742,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto s_buf = [&](int it) { return (it & 1) ? 384u : 0u; };
 
   if (warp == kBwdProducer) {
-    if (lane == 0 && n_kt > 0) {
+    if (n_kt > 0) {
       const uint64_t pol_res = policy_evict_first();
       const uint64_t pol_st = policy_evict_last();
       bool ok = true;
-      mbar_arrive_expect_tx(q_full, 2 * L::kTile);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_4d(sbase + L::kQOff + c * kChunkBytes, &tm_q, q_full, c * 64, h, q0, b,
-                    pol_res);
-        tma_load_4d(sbase + L::kDoOff + c * kChunkBytes, &tm_do, q_full, c * 64, h, q0, b,
-                    pol_res);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(q_full, 2 * L::kTile);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(sbase + L::kQOff + c * kChunkBytes, &tm_q, q_full, c * 64, h,
+                      sq.q_tok0 + q0, sq.map_b, pol_res);
+          tma_load_4d(sbase + L::kDoOff + c * kChunkBytes, &tm_do, q_full, c * 64, h,
+                      sq.q_tok0 + q0, sq.map_b, pol_res);
+        }
       }
       int k_issued = 0, v_issued = 0;
       for (int it = 0; it < n_kt && ok; ++it) {
         const int ks = it % 3, vs = it & 1;
-        if (it >= 3 && !wait(k_empty(ks), ((it / 3) - 1) & 1)) {
-          ok = false;
-          break;
+        if (lane == 0 && it >= 3 && !wait(k_empty(ks), ((it / 3) - 1) & 1)) ok = false;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const uint32_t kdst = sbase + L::kKOff + ks * L::kTile;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(k_full(ks), L::kTile);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(kdst + c * kChunkBytes, &tm_k, k_full(ks), c * 64, g,
+                        sq.k_tok0 + it * kBlockN, sq.map_b, pol_st);
         }
-        mbar_arrive_expect_tx(k_full(ks), L::kTile);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sbase + L::kKOff + ks * L::kTile + c * kChunkBytes, &tm_k, k_full(ks),
-                      c * 64, g, it * kBlockN, b, pol_st);
         k_issued = it + 1;
-        if (it >= 2 && !wait(v_empty(vs), ((it >> 1) - 1) & 1)) {
-          ok = false;
-          break;
+        if (k_partial(it)) {
+          // rows past the sequence's keys belong to the next one: zero them
+          // in K (the B operand of dQ += dS K) once the tile has landed
+          ok = __all_sync(0xffffffffu, wait(k_full(ks), (it / 3) & 1));
+          if (!ok) break;
+          zero_tail_rows<D>(kdst, lk - it * kBlockN, lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(k_fixed(ks));
         }
-        mbar_arrive_expect_tx(v_full(vs), L::kTile);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sbase + L::kVOff + vs * L::kTile + c * kChunkBytes, &tm_v, v_full(vs),
-                      c * 64, g, it * kBlockN, b, pol_st);
+        if (lane == 0 && it >= 2 && !wait(v_empty(vs), ((it >> 1) - 1) & 1)) ok = false;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(v_full(vs), L::kTile);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sbase + L::kVOff + vs * L::kTile + c * kChunkBytes, &tm_v, v_full(vs),
+                        c * 64, g, sq.k_tok0 + it * kBlockN, sq.map_b, pol_st);
+        }
         v_issued = it + 1;
       }
       // drain the copies still in flight before the CTA exits
-      wait_bar(q_full, 0, abort_flag, limit, p.status, false);
-      for (int it = max(0, k_issued - 3); it < k_issued; ++it)
-        wait_bar(k_full(it % 3), (it / 3) & 1, abort_flag, limit, p.status, false);
-      for (int it = max(0, v_issued - 2); it < v_issued; ++it)
-        wait_bar(v_full(it & 1), (it >> 1) & 1, abort_flag, limit, p.status, false);
+      if (lane == 0) {
+        wait_bar(q_full, 0, abort_flag, limit, p.status, false);
+        for (int it = max(0, k_issued - 3); it < k_issued; ++it)
+          wait_bar(k_full(it % 3), (it / 3) & 1, abort_flag, limit, p.status, false);
+        for (int it = max(0, v_issued - 2); it < v_issued; ++it)
+          wait_bar(v_full(it & 1), (it >> 1) & 1, abort_flag, limit, p.status, false);
+      }
     }
   } else if (warp == kBwdMma) {
     if (lane == 0) {
@@ -644,9 +807,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t do_desc = make_sdesc_sw128(sbase + L::kDoOff, 16, 1024);
       auto k_addr = [&](int it) { return sbase + L::kKOff + (it % 3) * L::kTile; };
       auto v_addr = [&](int it) { return sbase + L::kVOff + (it & 1) * L::kTile; };
-      // S(it) = Q K(it)^T into its score buffer
+      // S(it) = Q K(it)^T into its score buffer (tiles in increasing order);
+      // a partial packed tile is used once its tail rows are zeroed
+      uint32_t kfix = 0;  // bit s: phase of k_fixed(s), as the producer counts it
       auto issue_s = [&](int it) {
-        if (!wait(k_full(it % 3), (it / 3) & 1)) return false;
+        const int ks = it % 3;
+        if (k_partial(it)) {
+          if (!wait(k_fixed(ks), (kfix >> ks) & 1u)) return false;
+          kfix ^= 1u << ks;
+        } else if (!wait(k_full(ks), (it / 3) & 1)) {
+          return false;
+        }
         tc_fence_after();
         issue_ss<D>(tmem + s_buf(it), q_desc, make_sdesc_sw128(k_addr(it), 16, 1024), idesc_ss);
         return true;
@@ -695,26 +866,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int qi = q0 + row;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
-    const int64_t r = ((int64_t)b * p.Hq + h) * p.Sq + qi;
-    const float lse2 = qi < p.Sq ? p.lse_l2[r] : INFINITY;
-    const float dlt = qi < p.Sq ? p.delta[r] : 0.f;
+    const int64_t r = (lse_b * p.Hq + h) * p.Sq + lse_row0 + qi;
+    const float lse2 = qi < lq ? p.lse_l2[r] : INFINITY;
+    const float dlt = qi < lq ? p.delta[r] : 0.f;
     bool ok = true;
     for (int it = 0; it < n_kt; ++it) {
       if (ok) ok = __all_sync(0xffffffffu, wait(sdp_full, it & 1));
       if (ok) {
         tc_fence_after();
-        const bool interior = (it + 1) * kBlockN <= p.Sk && q0 + kBlockM <= p.Sq &&
+        const bool interior = (it + 1) * kBlockN <= lk && q0 + kBlockM <= lq &&
                               (!CAUSAL || it * kBlockN + kBlockN - 1 <= q0 + off);
         const uint32_t base = lane_base + s_buf(it);
         const uint32_t dp_minus_s = 128u - s_buf(it);  // dP columns relative to base
 #pragma unroll 1
         for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
           if (interior)
-            q_chunk<BF16, false, CAUSAL>(base, dp_minus_s, c, sl2, lse2, dlt, qi, it, p.Sq,
-                                         p.Sk, off);
+            q_chunk<BF16, false, CAUSAL>(base, dp_minus_s, c, sl2, lse2, dlt, qi, it, lq, lk,
+                                         off);
           else
-            q_chunk<BF16, true, CAUSAL>(base, dp_minus_s, c, sl2, lse2, dlt, qi, it, p.Sq,
-                                        p.Sk, off);
+            q_chunk<BF16, true, CAUSAL>(base, dp_minus_s, c, sl2, lse2, dlt, qi, it, lq, lk,
+                                        off);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -727,9 +898,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (have) have = __all_sync(0xffffffffu, wait(acc_ready, 0));
     if (n_kt > 0 && !have) ok = false;
     if (have) tc_fence_after();
-    const bool store = qi < p.Sq && (ok || n_kt == 0);
+    const bool store = qi < lq && (ok || n_kt == 0);
     elem_t *dq = reinterpret_cast<elem_t *>(p.dq) +
-                 (((int64_t)b * p.Sq + (store ? qi : 0)) * p.Hq + h) * D;
+                 ((lse_b * p.Sq + sq.q_tok0 + (store ? qi : 0)) * p.Hq + h) * D;
 #pragma unroll 1
     for (int c = wg * D / 64; c < (wg + 1) * D / 64; ++c) {
       float x[32];
@@ -755,29 +926,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 cudaError_t launch_bwd_t(const BwdLaunch &a) {
   const BwdParams &p = a.p;
-  const int64_t rows = (int64_t)p.B * p.Hq * p.Sq;
+  // the row pass sees a packed problem as one batch of Sq (= total) rows
+  BwdParams pr = p;
+  if (VARLEN) pr.B = 1;
+  const int64_t rows = (int64_t)pr.B * pr.Hq * pr.Sq;
   if (rows > 0) {
     constexpr int64_t per_block = (int64_t)kRowsPerThread * 256 / (D / 8);
-    const int64_t blocks = (int64_t)p.B * p.Hq * ((p.Sq + per_block - 1) / per_block);
+    const int64_t blocks = (int64_t)pr.B * pr.Hq * ((pr.Sq + per_block - 1) / per_block);
     if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-    fa_bwd_rows_kernel<D, BF16><<<(unsigned)blocks, 256, 0, a.stream>>>(p);
+    fa_bwd_rows_kernel<D, BF16><<<(unsigned)blocks, 256, 0, a.stream>>>(pr);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   using L = SmemBwd<D>;
   using LQ = SmemBwdQ<D>;
-  auto kv = fa_bwd_kv_kernel<D, BF16, CAUSAL>;
-  auto qk = fa_bwd_q_kernel<D, BF16, CAUSAL>;
+  auto kv = fa_bwd_kv_kernel<D, BF16, CAUSAL, VARLEN>;
+  auto qk = fa_bwd_q_kernel<D, BF16, CAUSAL, VARLEN>;
   static BwdOptIn opt_kv, opt_q;
   cudaError_t e = opt_kv.ensure(kv, (int)L::kAlloc, a.device);
   if (e != cudaSuccess) return e;
   e = opt_q.ensure(qk, (int)LQ::kAlloc, a.device);
   if (e != cudaSuccess) return e;
-  const int64_t kv_ctas = (int64_t)p.k_tiles * p.B * p.Hkv;
-  const int64_t q_ctas = (int64_t)p.q_tiles * p.B * p.Hq;
+  // packed: every sequence rounds its tiles up once, so total / 128 + B
+  // bounds the tiles; CTAs past the last one return at once
+  const int64_t kv_ctas = VARLEN ? ((int64_t)p.k_tiles + p.B) * p.Hkv
+                                 : (int64_t)p.k_tiles * p.B * p.Hkv;
+  const int64_t q_ctas = VARLEN ? ((int64_t)p.q_tiles + p.B) * p.Hq
+                                : (int64_t)p.q_tiles * p.B * p.Hq;
+  if (kv_ctas > 0x7fffffffll || q_ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
   if (kv_ctas > 0) {
     kv<<<(unsigned)kv_ctas, kBwdThreads, L::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do,
                                                                p);
@@ -792,15 +971,21 @@ cudaError_t launch_bwd_t(const BwdLaunch &a) {
   return e;
 }
 
+template <int D, bool BF16>
+cudaError_t launch_bwd_d(const BwdLaunch &a, bool causal, bool varlen) {
+  if (causal)
+    return varlen ? launch_bwd_t<D, BF16, true, true>(a) : launch_bwd_t<D, BF16, true, false>(a);
+  return varlen ? launch_bwd_t<D, BF16, false, true>(a) : launch_bwd_t<D, BF16, false, false>(a);
+}
+
 }  // namespace
 
-cudaError_t launch_bwd(const BwdLaunch &a, int D, bool bf16, bool causal) {
-  if (D == 64) {
-    if (bf16) return causal ? launch_bwd_t<64, true, true>(a) : launch_bwd_t<64, true, false>(a);
-    return causal ? launch_bwd_t<64, false, true>(a) : launch_bwd_t<64, false, false>(a);
-  }
-  if (bf16) return causal ? launch_bwd_t<128, true, true>(a) : launch_bwd_t<128, true, false>(a);
-  return causal ? launch_bwd_t<128, false, true>(a) : launch_bwd_t<128, false, false>(a);
+cudaError_t launch_bwd(const BwdLaunch &a, int D, bool bf16, bool causal, bool varlen) {
+  if (D == 64)
+    return bf16 ? launch_bwd_d<64, true>(a, causal, varlen)
+                : launch_bwd_d<64, false>(a, causal, varlen);
+  return bf16 ? launch_bwd_d<128, true>(a, causal, varlen)
+              : launch_bwd_d<128, false>(a, causal, varlen);
 }
 
 }  // namespace fa

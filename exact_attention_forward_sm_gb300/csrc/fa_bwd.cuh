@@ -26,7 +26,8 @@ struct BwdParams {
   float *lse_l2;       // workspace: LSE * log2(e), +inf for rows without keys
   float *delta;        // workspace: rowsum(dO * O) in fp32
   void *dq, *dk, *dv;  // outputs, layouts of q, k, v
-  int B, Hq, Hkv, Sq, Sk, group;
+  const int32_t *cu_q, *cu_k;  // packed sequences: B + 1 offsets each (else null)
+  int B, Hq, Hkv, Sq, Sk, group;  // packed: B sequences, Sq / Sk the packed totals
   float scale, scale_log2;
   int q_tiles, k_tiles;
   long long wait_limit;  // bounded-wait limit in cycles
@@ -40,7 +41,8 @@ struct BwdLaunch {
   int device;
 };
 
-// Launches the three passes for head dim 64 or 128 (bf16 or fp16).
-cudaError_t launch_bwd(const BwdLaunch &a, int D, bool bf16, bool causal);
+// Launches the three passes for head dim 64 or 128 (bf16 or fp16), dense or
+// packed (p.cu_q / p.cu_k set).
+cudaError_t launch_bwd(const BwdLaunch &a, int D, bool bf16, bool causal, bool varlen);
 
 }  // namespace fa

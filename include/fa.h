@@ -267,17 +267,21 @@ int fa_split_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int varlen,
 
 /*
  * fa_bwd — gradients of exact attention: the backward pass that the fork's
- * v1.7 release notes validate next to the forward (section 4.4).  Dense
- * problems (no cu_seqlens), head dim 64 or 128, fp16 or bf16.
+ * v1.7 release notes validate next to the forward (section 4.4), dense or
+ * packed, head dim 64 or 128, fp16 or bf16.
  *
  * Inputs, all DEVICE memory in the layouts of fa_fwd:
- *   q [B, Sq, Hq, D], k / v [B, Sk, Hkv, D]  the forward's inputs
- *   o [B, Sq, Hq, D], lse [B, Hq, Sq] fp32    the forward's outputs (as fa_fwd
- *                                             with the same arguments wrote
- *                                             them)
- *   dout [B, Sq, Hq, D]                       dL/dO, the upstream gradient
- * Outputs (written in full, never accumulated into):
- *   dq [B, Sq, Hq, D], dk / dv [B, Sk, Hkv, D], the inputs' dtype.
+ *   dense (cu_seqlens NULL):
+ *     q [B, Sq, Hq, D], k / v [B, Sk, Hkv, D]  the forward's inputs
+ *     o [B, Sq, Hq, D], lse [B, Hq, Sq] fp32    the forward's outputs (as
+ *                                               fa_fwd with the same
+ *                                               arguments wrote them)
+ *     dout [B, Sq, Hq, D]                       dL/dO, the upstream gradient
+ *   packed (cu_seqlens_q / cu_seqlens_k: B + 1 int32 offsets each, as in
+ *   fa_fwd; Sq / Sk the token totals):
+ *     q / o / dout [Sq, Hq, D], k / v [Sk, Hkv, D], lse [Hq, Sq]
+ * Outputs (written in full, never accumulated into), the inputs' dtype:
+ *   dq like q, dk / dv like k.
  * With P = softmax(scale q k^T) over each row's visible keys (causal masking
  * bottom-right aligned, as fa_fwd), dP = dout v^T and
  * dS = P * (dP - rowsum(dout * o)):
@@ -287,16 +291,22 @@ int fa_split_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int varlen,
  * result does not depend on scheduling (no atomics): repeated calls agree
  * bit for bit.
  *
+ * Packed sequences may sit next to each other in any order of lengths; a
+ * tile that reaches past its sequence reads the next one's rows, which may
+ * hold any values (Inf and NaN included): they are masked and, where they
+ * would feed a tensor-core product, zeroed in shared memory first.
+ *
  * workspace: DEVICE memory owned by the caller, 16-byte aligned, at least
- * fa_bwd_workspace_bytes(B, Hq, Sq) bytes; used by this call's kernels on
- * `stream` only (two fp32 values per query row and head); contents on entry
- * do not matter.
+ * fa_bwd_workspace_bytes(B, Hq, Sq) bytes (packed: fa_bwd_workspace_bytes(1,
+ * Hq, Sq) with Sq the total); used by this call's kernels on `stream` only
+ * (two fp32 values per query row and head); contents on entry do not matter.
  *
  * Returns FA_OK once queued; FA_ERR_INVALID_ARG (nothing queued) for invalid
- * sizes, flags or scale, a NULL or misaligned pointer (16 bytes; lse 4) or a
- * workspace smaller than needed; FA_ERR_UNSUPPORTED for another head dim or
- * non-NULL cu_seqlens; FA_ERR_CUDA.  A device-side pipeline timeout is
- * recorded for fa_get_device_error (FA_ERR_TIMEOUT).
+ * sizes, flags or scale, a NULL or misaligned pointer (16 bytes; lse and
+ * cu_seqlens 4), only one cu_seqlens pointer, or a workspace smaller than
+ * needed; FA_ERR_UNSUPPORTED for another head dim; FA_ERR_CUDA.  Recorded
+ * on the device for fa_get_device_error: FA_ERR_TIMEOUT (a pipeline wait
+ * timed out), FA_ERR_BAD_SEQLENS (offsets not monotone or past Sq / Sk).
  */
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
            const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Sq,

@@ -204,9 +204,16 @@ def test_backward_invalid_arguments_rejected_without_launch(lib, bad):
     assert _call_bwd(**bad) == fa.FA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("bad", [dict(D=256), dict(D=96), dict(cu_seqlens_q=64, cu_seqlens_k=64)])
+@pytest.mark.parametrize("bad", [dict(D=256), dict(D=96)])
 def test_backward_unsupported(lib, bad):
     assert _call_bwd(**bad) == fa.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("bad", [dict(cu_seqlens_q=64), dict(cu_seqlens_k=64),
+                                 dict(cu_seqlens_q=66, cu_seqlens_k=64)])
+def test_backward_packed_offsets_checked(lib, bad):
+    # both offset arrays or neither, each 4-byte aligned
+    assert _call_bwd(**bad) == fa.FA_ERR_INVALID_ARG
 
 
 def test_backward_workspace_bytes(lib):
