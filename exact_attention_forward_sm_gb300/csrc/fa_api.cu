@@ -712,6 +712,8 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
   p.status = status;
   a.stream = st;
   a.device = device;
+  a.sms = sm_count(device);
+  if (a.sms <= 0) return FA_ERR_CUDA;
   return fa::launch_bwd(a, D, bf16, causal != 0, varlen) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -41,7 +41,7 @@ struct SmemBwd {
   static constexpr uint32_t kStOff = 2 * kTile;
   static constexpr uint32_t kVecOff = kStOff + 4 * kTile;  // [2][2][128] floats (key pass)
   static constexpr uint32_t kBarOff = kVecOff + 2048;
-  static constexpr int kNumBars = 12;
+  static constexpr int kNumBars = 14;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   // at least 120 KB, so that two CTAs never share an SM: each allocates all
@@ -322,10 +322,52 @@ __device__ __forceinline__ void zero_tail_rows(uint32_t tile, int valid, int lan
 }
 
 // ---------------------------------------------------------------- key pass
-// One CTA per (key tile, batch, K/V head), heaviest key tiles first under
-// causal masking.  dV and dK of the tile's 128 keys accumulate in tensor
-// memory over every query tile that sees a key of the tile, for every query
-// head of the group.
+// Persistent: one CTA per SM walks a snake over the work items (key tile,
+// batch, K/V head; heaviest key tiles first under causal masking; packed:
+// every sequence's key tiles in order, K/V head fastest).  dV and dK of an
+// item's 128 keys accumulate in tensor memory over every query tile that
+// sees a key of the tile, for every query head of the group.  Across items
+// the phases continue: the next item's K / V load starts once the previous
+// item's last S^T / dP^T has read K / V, and its first dV / dK product waits
+// until the previous item's accumulators are read out (acc_free), so the
+// epilogue of one item overlaps the start of the next.
+struct KvItem {
+  int valid, b, g, k0, qt_begin, nq, n_it, off;
+  SeqRef sq;
+};
+
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ KvItem decode_kv_item(const BwdParams &p, int w, int lane) {
+  KvItem t;
+  t.valid = 0;
+  t.sq = SeqRef{p.Sq, p.Sk, 0, 0, 0};
+  int kt;
+  if (VARLEN) {
+    t.g = w % p.Hkv;
+    const int2 bt = packed_tile(p.cu_k, p.B, w / p.Hkv, lane);
+    if (bt.x < 0) return t;
+    if (!packed_seq(p, bt.x, &t.sq)) {
+      if (lane == 0) record_status(p.status, 5);
+      return t;
+    }
+    t.b = bt.x;
+    kt = bt.y;
+  } else {
+    const int bg = w % (p.B * p.Hkv);
+    kt = w / (p.B * p.Hkv);
+    t.b = bg / p.Hkv;
+    t.g = bg % p.Hkv;
+    t.sq.map_b = t.b;
+  }
+  t.k0 = kt * kBlockN;
+  t.off = t.sq.lk - t.sq.lq;  // bottom-right aligned causal diagonal
+  t.qt_begin = CAUSAL ? max(0, t.k0 - t.off) / kBlockM : 0;
+  t.nq = max(0, (t.sq.lq + kBlockM - 1) / kBlockM - t.qt_begin);
+  t.n_it = t.nq * p.group;
+  t.valid = 1;
+  return t;
+}
+
 template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -340,7 +382,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::kBarOff;
   const uint32_t kv_full = bar0, s_full = bar0 + 40, acc_ready = bar0 + 56,
-                 drain = bar0 + 64;
+                 drain = bar0 + 64, kv_empty = bar0 + 96, acc_free = bar0 + 104;
   auto st_full = [&](int s) { return bar0 + 8u + 8u * s; };
   auto st_empty = [&](int s) { return bar0 + 24u + 8u * s; };
   // P^T / dS^T of queries 64h .. 64h + 63 written (h = 0, 1)
@@ -352,53 +394,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float *vec = reinterpret_cast<float *>(smem + L::kVecOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int b, g, kt;
-  SeqRef sq{p.Sq, p.Sk, 0, 0, 0};
-  if (VARLEN) {
-    // key tiles of all sequences in order, K/V head fastest; CTAs past the
-    // last tile have nothing to do
-    g = blockIdx.x % p.Hkv;
-    const int2 bt = packed_tile(p.cu_k, p.B, blockIdx.x / p.Hkv, lane);
-    b = bt.x;
-    kt = bt.y;
-    if (b < 0) return;
-    if (!packed_seq(p, b, &sq)) {
-      if (threadIdx.x == 0) record_status(p.status, 5);
-      return;
-    }
-  } else {
-    // heavy-first: the key tile is the slowest-varying part of the CTA index
-    const int bg = blockIdx.x % (p.B * p.Hkv);
-    kt = blockIdx.x / (p.B * p.Hkv);
-    b = bg / p.Hkv;
-    g = bg % p.Hkv;
-    sq.map_b = b;
-  }
-  const int lq = sq.lq, lk = sq.lk;
-  const int k0 = kt * kBlockN;
-  const int off = lk - lq;  // bottom-right aligned causal diagonal
-  int qt_begin = 0;
-  if (CAUSAL) qt_begin = max(0, k0 - off) / kBlockM;
-  const int nq = max(0, (lq + kBlockM - 1) / kBlockM - qt_begin);
-  const int n_it = nq * p.group;
-  // rows of this sequence in the LSE / workspace order and in the outputs
-  const int64_t lse_row0 = VARLEN ? (int64_t)sq.q_tok0 : 0;
-  const int64_t lse_b = VARLEN ? 0 : (int64_t)b;
+  const int n_items = VARLEN ? (p.k_tiles + p.B) * p.Hkv : p.k_tiles * p.B * p.Hkv;
+  const int G = gridDim.x;
+  auto item_of = [&](int i) {  // snake over the heavy-first item order
+    return i * G + ((i & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+  };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(st_full(s), 1);
       mbar_init(st_empty(s), 1);
+      mbar_init(st_fixed(s), 1);
+      mbar_init(p_half(s), 4);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_half(0), 4);
-    mbar_init(p_half(1), 4);
     mbar_init(acc_ready, 1);
+    mbar_init(acc_free, 8);  // every elementwise warp, after reading dV / dK
     mbar_init(drain, 1);
-    mbar_init(st_fixed(0), 1);
-    mbar_init(st_fixed(1), 1);
     fence_barrier_init();
   }
   if (warp == kBwdMma) {
@@ -419,187 +434,239 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto wait = [&](uint32_t bar, uint32_t par) {
     return wait_bar(bar, par, abort_flag, limit, p.status);
   };
-  auto it_head = [&](int it) { return g * p.group + it / nq; };
-  auto it_tile = [&](int it) { return qt_begin + it % nq; };
-  // packed: the query tile of step it reaches past the sequence's rows
-  auto it_partial = [&](int it) { return VARLEN && it_tile(it) * kBlockM + kBlockM > lq; };
+  // step s_ of item t: query head, first query row, tail past the sequence
+  auto step_head = [&](const KvItem &t, int s_) { return t.g * p.group + s_ / t.nq; };
+  auto step_q0 = [&](const KvItem &t, int s_) { return (t.qt_begin + s_ % t.nq) * kBlockM; };
+  auto step_partial = [&](const KvItem &t, int s_) {
+    return VARLEN && step_q0(t, s_) + kBlockM > t.sq.lq;
+  };
 
   if (warp == kBwdProducer) {
-    if (n_it > 0) {
-      const uint64_t pol_res = policy_evict_first();
-      const uint64_t pol_st = policy_evict_last();
-      bool ok = true;
+    const uint64_t pol_res = policy_evict_first();
+    const uint64_t pol_st = policy_evict_last();
+    bool ok = true;
+    int g_it = 0, n_acc = 0, issued = 0;
+    for (int i = 0; ok; ++i) {
+      const int w = item_of(i);
+      if (w >= n_items) break;
+      const KvItem t = decode_kv_item<CAUSAL, VARLEN>(p, w, lane);
+      if (!t.valid || t.n_it == 0) continue;
+      // the previous item's last S^T / dP^T has read K and V
+      if (lane == 0 && n_acc > 0 && !wait(kv_empty, (n_acc - 1) & 1)) ok = false;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(sbase + L::kResOff + c * kChunkBytes, &tm_k, kv_full, c * 64, g,
-                      sq.k_tok0 + k0, sq.map_b, pol_res);
+          tma_load_4d(sbase + L::kResOff + c * kChunkBytes, &tm_k, kv_full, c * 64, t.g,
+                      t.sq.k_tok0 + t.k0, t.sq.map_b, pol_res);
           tma_load_4d(sbase + L::kResOff + L::kTile + c * kChunkBytes, &tm_v, kv_full, c * 64,
-                      g, sq.k_tok0 + k0, sq.map_b, pol_res);
+                      t.g, t.sq.k_tok0 + t.k0, t.sq.map_b, pol_res);
         }
       }
-      int issued = 0;
-      uint32_t fixpar = 0;  // bit s: phase of st_fixed(s)
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int s = it & 1;
-        if (lane == 0 && it >= 2 && !wait(st_empty(s), ((it >> 1) - 1) & 1)) ok = false;
+      ++n_acc;
+      for (int s_ = 0; s_ < t.n_it && ok; ++s_, ++g_it) {
+        const int s = g_it & 1;
+        if (lane == 0 && g_it >= 2 && !wait(st_empty(s), ((g_it >> 1) - 1) & 1)) ok = false;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        const int h = it_head(it), q0 = it_tile(it) * kBlockM;
+        const int h = step_head(t, s_), q0 = step_q0(t, s_);
         const uint32_t dst = sbase + L::kStOff + s * 2 * L::kTile;
         if (lane == 0) {
           mbar_arrive_expect_tx(st_full(s), 2 * L::kTile);
           for (int c = 0; c < D / 64; ++c) {
-            tma_load_4d(dst + c * kChunkBytes, &tm_q, st_full(s), c * 64, h, sq.q_tok0 + q0,
-                        sq.map_b, pol_st);
+            tma_load_4d(dst + c * kChunkBytes, &tm_q, st_full(s), c * 64, h, t.sq.q_tok0 + q0,
+                        t.sq.map_b, pol_st);
             tma_load_4d(dst + L::kTile + c * kChunkBytes, &tm_do, st_full(s), c * 64, h,
-                        sq.q_tok0 + q0, sq.map_b, pol_st);
+                        t.sq.q_tok0 + q0, t.sq.map_b, pol_st);
           }
         }
-        issued = it + 1;
-        if (it_partial(it)) {
+        issued = g_it + 1;
+        if (step_partial(t, s_)) {
           // rows past the sequence belong to the next one: zero them in Q and
           // dO (the B operands of dV += P^T dO and dK += dS^T Q) once landed
-          ok = __all_sync(0xffffffffu, wait(st_full(s), (it >> 1) & 1));
+          ok = __all_sync(0xffffffffu, wait(st_full(s), (g_it >> 1) & 1));
           if (!ok) break;
-          zero_tail_rows<D>(dst, lq - q0, lane);
-          zero_tail_rows<D>(dst + L::kTile, lq - q0, lane);
+          zero_tail_rows<D>(dst, t.sq.lq - q0, lane);
+          zero_tail_rows<D>(dst + L::kTile, t.sq.lq - q0, lane);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(st_fixed(s));
-          fixpar ^= 1u << s;
         }
       }
-      // drain the copies still in flight before the CTA exits
-      if (lane == 0) {
-        wait_bar(kv_full, 0, abort_flag, limit, p.status, false);
-        for (int it = max(0, issued - 2); it < issued; ++it)
-          wait_bar(st_full(it & 1), (it >> 1) & 1, abort_flag, limit, p.status, false);
-      }
+    }
+    // drain the copies still in flight before the CTA exits (K / V loads are
+    // serialised by kv_empty, so only the last can be outstanding)
+    if (lane == 0 && n_acc > 0) {
+      wait_bar(kv_full, (n_acc - 1) & 1, abort_flag, limit, p.status, false);
+      for (int it = max(0, issued - 2); it < issued; ++it)
+        wait_bar(st_full(it & 1), (it >> 1) & 1, abort_flag, limit, p.status, false);
     }
   } else if (warp == kBwdMma) {
-    if (lane == 0) {
+    // the whole warp walks the items (the packed decode is warp-collective);
+    // lane 0 issues every MMA and commit
+    {
       constexpr uint32_t idesc_ss = make_idesc_f16(BF16, kBlockM, kBlockN, false);
       constexpr uint32_t idesc_ts = make_idesc_f16(BF16, kBlockM, D, true);
       const uint64_t k_desc = make_sdesc_sw128(sbase + L::kResOff, 16, 1024);
       const uint64_t v_desc = make_sdesc_sw128(sbase + L::kResOff + L::kTile, 16, 1024);
-      bool ok = n_it == 0 || wait(kv_full, 0);
+      bool ok = true;
+      int g_it = 0, n_acc = 0;
       uint32_t fixpar = 0;  // bit s: phase of st_fixed(s), as the producer counts it
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int s = it & 1;
-        const uint32_t st = sbase + L::kStOff + s * 2 * L::kTile;
-        if (it_partial(it)) {
-          ok = wait(st_fixed(s), (fixpar >> s) & 1u);
-          fixpar ^= 1u << s;
-        } else {
-          ok = wait(st_full(s), (it >> 1) & 1);
-        }
-        if (!ok) break;
-        tc_fence_after();
-        issue_ss<D>(tmem, k_desc, make_sdesc_sw128(st, 16, 1024), idesc_ss);  // S^T = K Q^T
-        issue_ss<D>(tmem + 128, v_desc, make_sdesc_sw128(st + L::kTile, 16, 1024),
-                    idesc_ss);  // dP^T = V dO^T
-        tc_commit(s_full);
-        // dV += P^T dO, dK += dS^T Q (B tiles MN-major: rows = queries), each
-        // half of the queries as soon as the elementwise warps have written it
-        const uint64_t do_mn = make_sdesc_sw128(st + L::kTile, kChunkBytes, 1024);
-        const uint64_t q_mn = make_sdesc_sw128(st, kChunkBytes, 1024);
-        for (int hh = 0; hh < 2 && ok; ++hh) {
-          ok = wait_bar_spin(p_half(hh), it & 1, abort_flag, limit, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          issue_ts_half(tmem + 256, tmem, do_mn, idesc_ts, hh, it > 0);
-          issue_ts_half(tmem + 256 + D, tmem + 128, q_mn, idesc_ts, hh, it > 0);
-        }
-        if (!ok) break;
-        tc_commit(st_empty(s));
+      for (int i = 0; ok; ++i) {
+        const int w = item_of(i);
+        if (w >= n_items) break;
+        const KvItem t = decode_kv_item<CAUSAL, VARLEN>(p, w, lane);
+        if (!t.valid || t.n_it == 0) continue;
+        if (lane == 0) {  // lanes 1-31 only follow the item sequence
+          ok = wait(kv_full, n_acc & 1);
+          for (int s_ = 0; s_ < t.n_it && ok; ++s_, ++g_it) {
+            const int s = g_it & 1;
+            const uint32_t st = sbase + L::kStOff + s * 2 * L::kTile;
+            if (step_partial(t, s_)) {
+              ok = wait(st_fixed(s), (fixpar >> s) & 1u);
+              fixpar ^= 1u << s;
+            } else {
+              ok = wait(st_full(s), (g_it >> 1) & 1);
+            }
+            if (!ok) break;
+            tc_fence_after();
+            issue_ss<D>(tmem, k_desc, make_sdesc_sw128(st, 16, 1024), idesc_ss);  // S^T = K Q^T
+            issue_ss<D>(tmem + 128, v_desc, make_sdesc_sw128(st + L::kTile, 16, 1024),
+                        idesc_ss);  // dP^T = V dO^T
+            if (s_ == t.n_it - 1) tc_commit(kv_empty);  // K / V read for the last time
+            tc_commit(s_full);
+            // dV += P^T dO, dK += dS^T Q (B tiles MN-major: rows = queries), each
+            // half of the queries as soon as the elementwise warps have written it
+            const uint64_t do_mn = make_sdesc_sw128(st + L::kTile, kChunkBytes, 1024);
+            const uint64_t q_mn = make_sdesc_sw128(st, kChunkBytes, 1024);
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+              ok = wait_bar_spin(p_half(hh), g_it & 1, abort_flag, limit, p.status);
+              // the item's first product overwrites the accumulators: the
+              // previous item's epilogue must have read them
+              if (ok && s_ == 0 && hh == 0 && n_acc > 0) ok = wait(acc_free, (n_acc - 1) & 1);
+              if (!ok) break;
+              tc_fence_after();
+              issue_ts_half(tmem + 256, tmem, do_mn, idesc_ts, hh, s_ > 0);
+              issue_ts_half(tmem + 256 + D, tmem + 128, q_mn, idesc_ts, hh, s_ > 0);
+            }
+            if (!ok) break;
+            tc_commit(st_empty(s));
+          }
+          if (ok) {
+            tc_commit(acc_ready);
+            ++n_acc;
+          }
+        }  // lane 0
+        ok = __shfl_sync(0xffffffffu, ok, 0);  // every lane, once per item
       }
-      tc_commit(acc_ready);
-      // no MMA may still run when tensor memory is released
-      tc_commit(drain);
-      wait_bar(drain, 0, abort_flag, limit, p.status, false);
+      if (lane == 0) {
+        // no MMA may still run when tensor memory is released
+        tc_commit(drain);
+        wait_bar(drain, 0, abort_flag, limit, p.status, false);
+      }
     }
   } else {
     // -------------------------------------------- elementwise: one key per thread
     const int quarter = warp & 3, wg = warp >> 2;  // TMEM lane quarter, column half
     const int row = quarter * 32 + lane;
-    const int j = k0 + row;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
-    // warpgroup 0 loads a query tile's lse / Delta one step ahead, so the
-    // global-memory latency overlaps the previous step's work
-    float n_lse = INFINITY, n_delta = 0.f;
-    auto fetch = [&](int it) {
-      const int qi = it_tile(it) * kBlockM + row;
-      const int64_t r = (lse_b * p.Hq + it_head(it)) * p.Sq + lse_row0 + qi;
-      n_lse = qi < lq ? p.lse_l2[r] : INFINITY;
-      n_delta = qi < lq ? p.delta[r] : 0.f;
-    };
-    if (wg == 0 && n_it > 0) fetch(0);
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int s = it & 1;
-      const int q0 = it_tile(it) * kBlockM;
-      float *v_lse = vec + s * 256, *v_delta = v_lse + 128;
-      if (wg == 0) {
-        v_lse[row] = n_lse;
-        v_delta[row] = n_delta;
-        if (it + 1 < n_it) fetch(it + 1);
-      }
-      named_barrier_sync(1, 256);
-      if (ok) ok = __all_sync(0xffffffffu, wait(s_full, it & 1));
-      if (ok) {
-        tc_fence_after();
-        const bool interior = k0 + kBlockN <= lk && q0 + kBlockM <= lq &&
-                              (!CAUSAL || k0 + kBlockN - 1 <= q0 + off);
-#pragma unroll 1
-        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-          if (interior)
-            kv_chunk<BF16, false, CAUSAL>(lane_base, c, sl2, v_lse, v_delta, j, q0, lq, lk,
-                                          off);
-          else
-            kv_chunk<BF16, true, CAUSAL>(lane_base, c, sl2, v_lse, v_delta, j, q0, lq, lk, off);
+    int g_it = 0, n_acc = 0;
+    for (int i = 0;; ++i) {
+      const int w = item_of(i);
+      if (w >= n_items) break;
+      const KvItem t = decode_kv_item<CAUSAL, VARLEN>(p, w, lane);
+      if (!t.valid) continue;
+      const int lq = t.sq.lq, lk = t.sq.lk, k0 = t.k0, off = t.off;
+      const int j = k0 + row;
+      const int64_t lse_b = VARLEN ? 0 : (int64_t)t.b;
+      const int64_t lse_row0 = VARLEN ? (int64_t)t.sq.q_tok0 : 0;
+      // warpgroup 0 loads a query tile's lse / Delta one step ahead, so the
+      // global-memory latency overlaps the previous step's work
+      float n_lse = INFINITY, n_delta = 0.f;
+      auto fetch = [&](int s_) {
+        const int qi = step_q0(t, s_) + row;
+        const int64_t r = (lse_b * p.Hq + step_head(t, s_)) * p.Sq + lse_row0 + qi;
+        n_lse = qi < lq ? p.lse_l2[r] : INFINITY;
+        n_delta = qi < lq ? p.delta[r] : 0.f;
+      };
+      if (wg == 0 && t.n_it > 0) fetch(0);
+      for (int s_ = 0; s_ < t.n_it; ++s_, ++g_it) {
+        const int s = g_it & 1;
+        const int q0 = step_q0(t, s_);
+        float *v_lse = vec + s * 256, *v_delta = v_lse + 128;
+        if (wg == 0) {
+          v_lse[row] = n_lse;
+          v_delta[row] = n_delta;
+          if (s_ + 1 < t.n_it) fetch(s_ + 1);
         }
-        tmem_st_wait();
+        named_barrier_sync(1, 256);
+        if (ok) ok = __all_sync(0xffffffffu, wait(s_full, g_it & 1));
+        if (ok) {
+          tc_fence_after();
+          const bool interior = k0 + kBlockN <= lk && q0 + kBlockM <= lq &&
+                                (!CAUSAL || k0 + kBlockN - 1 <= q0 + off);
+#pragma unroll 1
+          for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
+            if (interior)
+              kv_chunk<BF16, false, CAUSAL>(lane_base, c, sl2, v_lse, v_delta, j, q0, lq, lk,
+                                            off);
+            else
+              kv_chunk<BF16, true, CAUSAL>(lane_base, c, sl2, v_lse, v_delta, j, q0, lq, lk,
+                                           off);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_half(wg));  // this half of the queries is written
+        }
+        __syncwarp();
+      }
+      // ----------------------------------------------------------- epilogue
+      // Warpgroup wg owns columns wg D / 2 .. (wg + 1) D / 2 - 1 of dV and dK:
+      // all of them are read out of tensor memory first and the accumulators
+      // released (acc_free), then converted and stored.  The loads are
+      // warp-wide (have, ok are warp-uniform); only the stores of keys inside
+      // the sequence are per lane.
+      bool have = t.n_it > 0 && ok;
+      if (have) have = __all_sync(0xffffffffu, wait(acc_ready, n_acc & 1));
+      if (t.n_it > 0 && !have) ok = false;
+      constexpr int kHalf = D / 2;
+      uint32_t rv[kHalf], rk[kHalf];
+      if (have) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kHalf / 32; ++c) {
+          tmem_ld32(lane_base + 256 + wg * kHalf + c * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(rv + 32 * c));
+          tmem_ld32(lane_base + 256 + D + wg * kHalf + c * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(rk + 32 * c));
+        }
+#pragma unroll
+        for (int c = 0; c < kHalf / 32; ++c) {
+          tmem_wait_ld32(*reinterpret_cast<uint32_t(*)[32]>(rv + 32 * c));
+          tmem_wait_ld32(*reinterpret_cast<uint32_t(*)[32]>(rk + 32 * c));
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_half(wg));  // this half of the queries is written
-      }
-      __syncwarp();
-    }
-    // ------------------------------------------------------------- epilogue
-    bool have = n_it > 0 && ok;
-    if (have) have = __all_sync(0xffffffffu, wait(acc_ready, 0));
-    if (n_it > 0 && !have) ok = false;
-    if (have) tc_fence_after();
-    // the tensor-memory loads are warp-wide (have, ok are warp-uniform); only
-    // the stores of keys inside the sequence are per lane.  Warpgroup wg
-    // writes columns wg D / 2 .. (wg + 1) D / 2 - 1 of dV and dK.
-    const bool store = j < lk && (ok || n_it == 0);
-    const int64_t rbase = ((lse_b * p.Sk + sq.k_tok0 + (store ? j : 0)) * p.Hkv + g) * D;
-    elem_t *dv = reinterpret_cast<elem_t *>(p.dv) + rbase;
-    elem_t *dk = reinterpret_cast<elem_t *>(p.dk) + rbase;
-#pragma unroll 1
-    for (int c = wg * D / 64; c < (wg + 1) * D / 64; ++c) {
-      float xv[32], xk[32];
-      if (have) {
-        uint32_t rv[32], rk[32];
-        tmem_ld32(lane_base + 256 + c * 32, rv);
-        tmem_ld32(lane_base + 256 + D + c * 32, rk);
-        tmem_wait_ld32(rv);
-        tmem_wait_ld32(rk);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          xv[e] = __uint_as_float(rv[e]);
-          xk[e] = __uint_as_float(rk[e]);
-        }
+        if (lane == 0) mbar_arrive(acc_free);
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) xv[e] = xk[e] = 0.f;  // no query sees these keys
+        for (int e = 0; e < kHalf; ++e) rv[e] = rk[e] = 0u;  // no query sees these keys
       }
+      if (t.n_it > 0) ++n_acc;
+      const bool store = j < lk && (ok || t.n_it == 0);
       if (store) {
-        store_row32<BF16>(dv + c * 32, xv, 1.f);
-        store_row32<BF16>(dk + c * 32, xk, p.scale);
+        const int64_t rbase = ((lse_b * p.Sk + t.sq.k_tok0 + j) * p.Hkv + t.g) * D + wg * kHalf;
+        elem_t *dv = reinterpret_cast<elem_t *>(p.dv) + rbase;
+        elem_t *dk = reinterpret_cast<elem_t *>(p.dk) + rbase;
+#pragma unroll
+        for (int c = 0; c < kHalf / 32; ++c) {
+          store_row32<BF16>(dv + c * 32, reinterpret_cast<const float *>(rv + 32 * c), 1.f);
+          store_row32<BF16>(dk + c * 32, reinterpret_cast<const float *>(rk + 32 * c), p.scale);
+        }
       }
     }
   }
@@ -958,8 +1025,9 @@ cudaError_t launch_bwd_t(const BwdLaunch &a) {
                                 : (int64_t)p.q_tiles * p.B * p.Hq;
   if (kv_ctas > 0x7fffffffll || q_ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
   if (kv_ctas > 0) {
-    kv<<<(unsigned)kv_ctas, kBwdThreads, L::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do,
-                                                               p);
+    // persistent: one CTA per SM walks the items
+    const unsigned kv_grid = (unsigned)(kv_ctas < a.sms ? kv_ctas : a.sms);
+    kv<<<kv_grid, kBwdThreads, L::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

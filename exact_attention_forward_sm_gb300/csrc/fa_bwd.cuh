@@ -39,6 +39,7 @@ struct BwdLaunch {
   BwdParams p;
   cudaStream_t stream;
   int device;
+  int sms;  // SM count of the device (persistent grids)
 };
 
 // Launches the three passes for head dim 64 or 128 (bf16 or fp16), dense or
