@@ -41,7 +41,7 @@ struct SmemBwd {
   static constexpr uint32_t kStOff = 2 * kTile;
   static constexpr uint32_t kVecOff = kStOff + 4 * kTile;  // [2][2][128] floats (key pass)
   static constexpr uint32_t kBarOff = kVecOff + 2048;
-  static constexpr int kNumBars = 14;
+  static constexpr int kNumBars = 15;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   // at least 120 KB, so that two CTAs never share an SM: each allocates all
@@ -381,8 +381,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::kBarOff;
-  const uint32_t kv_full = bar0, s_full = bar0 + 40, acc_ready = bar0 + 56,
-                 drain = bar0 + 64, kv_empty = bar0 + 96, acc_free = bar0 + 104;
+  const uint32_t kv_full = bar0, acc_ready = bar0 + 56, drain = bar0 + 64,
+                 kv_empty = bar0 + 96, acc_free = bar0 + 104;
+  // S^T / dP^T of queries 64h .. 64h + 63 computed (h = 0, 1)
+  auto s_full = [&](int h) { return h ? bar0 + 112u : bar0 + 40u; };
   auto st_full = [&](int s) { return bar0 + 8u + 8u * s; };
   auto st_empty = [&](int s) { return bar0 + 24u + 8u * s; };
   // P^T / dS^T of queries 64h .. 64h + 63 written (h = 0, 1)
@@ -410,7 +412,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(st_fixed(s), 1);
       mbar_init(p_half(s), 4);
     }
-    mbar_init(s_full, 1);
+    mbar_init(s_full(0), 1);
+    mbar_init(s_full(1), 1);
     mbar_init(acc_ready, 1);
     mbar_init(acc_free, 8);  // every elementwise warp, after reading dV / dK
     mbar_init(drain, 1);
@@ -506,7 +509,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // the whole warp walks the items (the packed decode is warp-collective);
     // lane 0 issues every MMA and commit
     {
-      constexpr uint32_t idesc_ss = make_idesc_f16(BF16, kBlockM, kBlockN, false);
+      constexpr uint32_t idesc_ss64 = make_idesc_f16(BF16, kBlockM, 64, false);
       constexpr uint32_t idesc_ts = make_idesc_f16(BF16, kBlockM, D, true);
       const uint64_t k_desc = make_sdesc_sw128(sbase + L::kResOff, 16, 1024);
       const uint64_t v_desc = make_sdesc_sw128(sbase + L::kResOff + L::kTile, 16, 1024);
@@ -519,27 +522,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const KvItem t = decode_kv_item<CAUSAL, VARLEN>(p, w, lane);
         if (!t.valid || t.n_it == 0) continue;
         if (lane == 0) {  // lanes 1-31 only follow the item sequence
-          ok = wait(kv_full, n_acc & 1);
+          // Query halves are software-pipelined: per step it and half h the
+          // issuer waits for P^T / dS^T of half h, issues dV += P^T dO and
+          // dK += dS^T Q of that half, then the next step's S^T / dP^T of the
+          // same half (N = 64), so one warpgroup's elementwise work overlaps
+          // the products of the other half.  S^T / dP^T of a half overwrite
+          // only that half's columns, whose packed P^T / dS^T the previous
+          // products (earlier in issue order) have read.
+          auto stage_ready = [&](int s_, int gs) {  // Q / dO of step s_ landed
+            const int s = gs & 1;
+            if (step_partial(t, s_)) {
+              const bool r = wait(st_fixed(s), (fixpar >> s) & 1u);
+              fixpar ^= 1u << s;
+              return r;
+            }
+            return wait(st_full(s), (gs >> 1) & 1);
+          };
+          auto issue_scores = [&](int gs, int h) {  // S^T, dP^T of half h of step gs
+            const uint32_t st = sbase + L::kStOff + (gs & 1) * 2 * L::kTile + h * 64 * 128;
+            issue_ss<D>(tmem + 64 * h, k_desc, make_sdesc_sw128(st, 16, 1024), idesc_ss64);
+            issue_ss<D>(tmem + 128 + 64 * h, v_desc,
+                        make_sdesc_sw128(st + L::kTile, 16, 1024), idesc_ss64);
+            tc_commit(s_full(h));
+          };
+          ok = wait(kv_full, n_acc & 1) && stage_ready(0, g_it);
+          if (ok) {
+            tc_fence_after();
+            issue_scores(g_it, 0);
+            issue_scores(g_it, 1);
+            if (t.n_it == 1) tc_commit(kv_empty);  // K / V read for the last time
+          }
           for (int s_ = 0; s_ < t.n_it && ok; ++s_, ++g_it) {
             const int s = g_it & 1;
             const uint32_t st = sbase + L::kStOff + s * 2 * L::kTile;
-            if (step_partial(t, s_)) {
-              ok = wait(st_fixed(s), (fixpar >> s) & 1u);
-              fixpar ^= 1u << s;
-            } else {
-              ok = wait(st_full(s), (g_it >> 1) & 1);
-            }
-            if (!ok) break;
-            tc_fence_after();
-            issue_ss<D>(tmem, k_desc, make_sdesc_sw128(st, 16, 1024), idesc_ss);  // S^T = K Q^T
-            issue_ss<D>(tmem + 128, v_desc, make_sdesc_sw128(st + L::kTile, 16, 1024),
-                        idesc_ss);  // dP^T = V dO^T
-            if (s_ == t.n_it - 1) tc_commit(kv_empty);  // K / V read for the last time
-            tc_commit(s_full);
-            // dV += P^T dO, dK += dS^T Q (B tiles MN-major: rows = queries), each
-            // half of the queries as soon as the elementwise warps have written it
             const uint64_t do_mn = make_sdesc_sw128(st + L::kTile, kChunkBytes, 1024);
             const uint64_t q_mn = make_sdesc_sw128(st, kChunkBytes, 1024);
+            const bool more = s_ + 1 < t.n_it;
             for (int hh = 0; hh < 2 && ok; ++hh) {
               ok = wait_bar_spin(p_half(hh), g_it & 1, abort_flag, limit, p.status);
               // the item's first product overwrites the accumulators: the
@@ -547,11 +565,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               if (ok && s_ == 0 && hh == 0 && n_acc > 0) ok = wait(acc_free, (n_acc - 1) & 1);
               if (!ok) break;
               tc_fence_after();
+              // dV += P^T dO, dK += dS^T Q (B tiles MN-major: rows = queries)
               issue_ts_half(tmem + 256, tmem, do_mn, idesc_ts, hh, s_ > 0);
               issue_ts_half(tmem + 256 + D, tmem + 128, q_mn, idesc_ts, hh, s_ > 0);
+              if (hh == 1) tc_commit(st_empty(s));  // Q / dO of this step read
+              if (more) {
+                if (hh == 0) {
+                  ok = stage_ready(s_ + 1, g_it + 1);
+                  if (!ok) break;
+                  tc_fence_after();
+                }
+                issue_scores(g_it + 1, hh);
+                if (hh == 1 && s_ + 2 == t.n_it) tc_commit(kv_empty);
+              }
             }
-            if (!ok) break;
-            tc_commit(st_empty(s));
           }
           if (ok) {
             tc_commit(acc_ready);
@@ -583,27 +610,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int j = k0 + row;
       const int64_t lse_b = VARLEN ? 0 : (int64_t)t.b;
       const int64_t lse_row0 = VARLEN ? (int64_t)t.sq.q_tok0 : 0;
-      // warpgroup 0 loads a query tile's lse / Delta one step ahead, so the
-      // global-memory latency overlaps the previous step's work
+      // each warpgroup keeps lse / Delta of its own 64 queries (threads 0-63
+      // of the warpgroup load them one step ahead, so the global-memory
+      // latency overlaps the previous step's work); the warpgroups meet only
+      // at their own named barrier, so their halves may run apart
       float n_lse = INFINITY, n_delta = 0.f;
       auto fetch = [&](int s_) {
-        const int qi = step_q0(t, s_) + row;
+        const int qi = step_q0(t, s_) + 64 * wg + row;
         const int64_t r = (lse_b * p.Hq + step_head(t, s_)) * p.Sq + lse_row0 + qi;
         n_lse = qi < lq ? p.lse_l2[r] : INFINITY;
         n_delta = qi < lq ? p.delta[r] : 0.f;
       };
-      if (wg == 0 && t.n_it > 0) fetch(0);
+      if (row < 64 && t.n_it > 0) fetch(0);
       for (int s_ = 0; s_ < t.n_it; ++s_, ++g_it) {
         const int s = g_it & 1;
         const int q0 = step_q0(t, s_);
-        float *v_lse = vec + s * 256, *v_delta = v_lse + 128;
-        if (wg == 0) {
-          v_lse[row] = n_lse;
-          v_delta[row] = n_delta;
+        float *v_mine = vec + (2 * wg + s) * 128;  // [64 lse][64 Delta] of this half
+        if (row < 64) {
+          v_mine[row] = n_lse;
+          v_mine[64 + row] = n_delta;
           if (s_ + 1 < t.n_it) fetch(s_ + 1);
         }
-        named_barrier_sync(1, 256);
-        if (ok) ok = __all_sync(0xffffffffu, wait(s_full, g_it & 1));
+        named_barrier_sync(1 + wg, 128);
+        // chunk c (32 queries) of this half reads entries (c - 2 wg) * 32 ..
+        float *v_lse = v_mine - 64 * wg, *v_delta = v_mine + 64 - 64 * wg;
+        if (ok) ok = __all_sync(0xffffffffu, wait(s_full(wg), g_it & 1));
         if (ok) {
           tc_fence_after();
           const bool interior = k0 + kBlockN <= lk && q0 + kBlockM <= lq &&
