@@ -724,21 +724,65 @@ struct SmemBwdQ {
   static constexpr uint32_t kVOff = 5 * kTile;  // 2 slots
   static constexpr uint32_t kBarOff = 7 * kTile;
   // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], sdp_full,
-  // ds_half[2], acc_ready, drain, k_fixed[3]
-  static constexpr int kNumBars = 19;
+  // ds_half[2], acc_ready, drain, k_fixed[3], q_empty, acc_free
+  static constexpr int kNumBars = 21;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024 > 120u * 1024 ? kBytes + 1024 : 120u * 1024;
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
 
-// One CTA per (query tile, batch, query head), heaviest (latest) query tiles
-// first under causal masking.  dQ of the tile's 128 rows accumulates in
-// tensor memory over the key tiles the rows see.  The scores alternate
-// between two tensor-memory buffers (columns 0-127 and 384-511; dP at
-// 128-255, dQ at 256-383): per key tile the MMA issuer runs dP(it + 1),
-// dQ += dS(it) K(it) and S(it + 2), so the elementwise work of tile it + 1
-// overlaps the last two.
+// Persistent: one CTA per SM walks a snake over the work items (query tile,
+// batch, query head; latest (heaviest) query tiles first under causal
+// masking; packed: every sequence's query tiles in order, query head
+// fastest).  dQ of an item's 128 rows accumulates in tensor memory over the
+// key tiles the rows see.  The scores alternate between two tensor-memory
+// buffers (columns 0-127 and 384-511; dP at 128-255, dQ at 256-383): per key
+// tile the MMA issuer runs dP(it + 1), dQ += dS(it) K(it) and S(it + 2), so
+// the elementwise work of tile it + 1 overlaps the last two.  Across items
+// the key-tile counter and the K / V rings run on; the next item's Q / dO
+// load starts once the item's last dP has read them, and its first dQ
+// product waits until the previous dQ is read out (acc_free).
+struct QItem {
+  int valid, b, h, q0, n_kt, off, k_tiles;
+  SeqRef sq;
+};
+
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ QItem decode_q_item(const BwdParams &p, int w, int lane) {
+  QItem t;
+  t.valid = 0;
+  t.sq = SeqRef{p.Sq, p.Sk, 0, 0, 0};
+  int qt;
+  if (VARLEN) {
+    t.h = w % p.Hq;
+    const int2 bt = packed_tile(p.cu_q, p.B, w / p.Hq, lane);
+    if (bt.x < 0) return t;
+    if (!packed_seq(p, bt.x, &t.sq)) {
+      if (lane == 0) record_status(p.status, 5);
+      return t;
+    }
+    t.b = bt.x;
+    qt = bt.y;
+  } else {
+    const int bh = w % (p.B * p.Hq);
+    qt = p.q_tiles - 1 - w / (p.B * p.Hq);  // latest (heaviest) first
+    t.b = bh / p.Hq;
+    t.h = bh % p.Hq;
+    t.sq.map_b = t.b;
+  }
+  t.q0 = qt * kBlockM;
+  t.off = t.sq.lk - t.sq.lq;
+  t.k_tiles = (t.sq.lk + kBlockN - 1) / kBlockN;
+  t.n_kt = t.k_tiles;
+  if (CAUSAL) {
+    const int last = min(t.q0 + kBlockM, t.sq.lq) - 1 + t.off;  // last key any row sees
+    t.n_kt = last < 0 ? 0 : min(t.k_tiles, last / kBlockN + 1);
+  }
+  t.valid = 1;
+  return t;
+}
+
 template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -753,7 +797,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::kBarOff;
   const uint32_t q_full = bar0, sdp_full = bar0 + 88, acc_ready = bar0 + 112,
-                 drain = bar0 + 120;
+                 drain = bar0 + 120, q_empty = bar0 + 152, acc_free = bar0 + 160;
   auto k_full = [&](int s) { return bar0 + 8u + 8u * s; };
   auto k_empty = [&](int s) { return bar0 + 32u + 8u * s; };
   auto v_full = [&](int s) { return bar0 + 56u + 8u * s; };
@@ -765,47 +809,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int b, h, qt;
-  SeqRef sq{p.Sq, p.Sk, 0, 0, 0};
-  if (VARLEN) {
-    // query tiles of all sequences in order, query head fastest
-    h = blockIdx.x % p.Hq;
-    const int2 bt = packed_tile(p.cu_q, p.B, blockIdx.x / p.Hq, lane);
-    b = bt.x;
-    qt = bt.y;
-    if (b < 0) return;
-    if (!packed_seq(p, b, &sq)) {
-      if (threadIdx.x == 0) record_status(p.status, 5);
-      return;
-    }
-  } else {
-    const int bh = blockIdx.x % (p.B * p.Hq);
-    qt = p.q_tiles - 1 - (int)(blockIdx.x / (p.B * p.Hq));  // latest (heaviest) first
-    b = bh / p.Hq;
-    h = bh % p.Hq;
-    sq.map_b = b;
-  }
-  const int g = h / p.group;
-  const int lq = sq.lq, lk = sq.lk;
-  const int q0 = qt * kBlockM;
-  const int off = lk - lq;
-  const int k_tiles = (lk + kBlockN - 1) / kBlockN;
-  int n_kt = k_tiles;
-  if (CAUSAL) {
-    const int last = min(q0 + kBlockM, lq) - 1 + off;  // last key any row sees
-    n_kt = last < 0 ? 0 : min(k_tiles, last / kBlockN + 1);
-  }
-  const int64_t lse_b = VARLEN ? 0 : (int64_t)b;
-  const int64_t lse_row0 = VARLEN ? (int64_t)sq.q_tok0 : 0;
-  // packed: key tile it reaches past the sequence's keys
-  auto k_partial = [&](int it) { return VARLEN && it * kBlockN + kBlockN > lk; };
+  const int n_items = VARLEN ? (p.q_tiles + p.B) * p.Hq : p.q_tiles * p.B * p.Hq;
+  const int G = gridDim.x;
+  auto item_of = [&](int i) {  // snake over the heavy-first item order
+    return i * G + ((i & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+  };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < 3; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
+      mbar_init(k_fixed(s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(v_full(s), 1);
@@ -814,8 +831,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(sdp_full, 1);
     mbar_init(acc_ready, 1);
+    mbar_init(acc_free, 8);  // every elementwise warp, after reading dQ
     mbar_init(drain, 1);
-    for (int s = 0; s < 3; ++s) mbar_init(k_fixed(s), 1);
     fence_barrier_init();
   }
   if (warp == kBwdMma) {
@@ -836,27 +853,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto wait = [&](uint32_t bar, uint32_t par) {
     return wait_bar(bar, par, abort_flag, limit, p.status);
   };
-  // score buffer of key tile it
-  auto s_buf = [&](int it) { return (it & 1) ? 384u : 0u; };
+  // score buffer of global key-tile step gs
+  auto s_buf = [&](int gs) { return (gs & 1) ? 384u : 0u; };
 
   if (warp == kBwdProducer) {
-    if (n_kt > 0) {
-      const uint64_t pol_res = policy_evict_first();
-      const uint64_t pol_st = policy_evict_last();
-      bool ok = true;
+    const uint64_t pol_res = policy_evict_first();
+    const uint64_t pol_st = policy_evict_last();
+    bool ok = true;
+    int gk = 0, n_acc = 0, k_issued = 0, v_issued = 0;
+    for (int i = 0; ok; ++i) {
+      const int w = item_of(i);
+      if (w >= n_items) break;
+      const QItem t = decode_q_item<CAUSAL, VARLEN>(p, w, lane);
+      if (!t.valid || t.n_kt == 0) continue;
+      // the previous item's last S and dP have read Q and dO
+      if (lane == 0 && n_acc > 0 && !wait(q_empty, (n_acc - 1) & 1)) ok = false;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full, 2 * L::kTile);
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(sbase + L::kQOff + c * kChunkBytes, &tm_q, q_full, c * 64, h,
-                      sq.q_tok0 + q0, sq.map_b, pol_res);
-          tma_load_4d(sbase + L::kDoOff + c * kChunkBytes, &tm_do, q_full, c * 64, h,
-                      sq.q_tok0 + q0, sq.map_b, pol_res);
+          tma_load_4d(sbase + L::kQOff + c * kChunkBytes, &tm_q, q_full, c * 64, t.h,
+                      t.sq.q_tok0 + t.q0, t.sq.map_b, pol_res);
+          tma_load_4d(sbase + L::kDoOff + c * kChunkBytes, &tm_do, q_full, c * 64, t.h,
+                      t.sq.q_tok0 + t.q0, t.sq.map_b, pol_res);
         }
       }
-      int k_issued = 0, v_issued = 0;
-      for (int it = 0; it < n_kt && ok; ++it) {
-        const int ks = it % 3, vs = it & 1;
-        if (lane == 0 && it >= 3 && !wait(k_empty(ks), ((it / 3) - 1) & 1)) ok = false;
+      ++n_acc;
+      const int g = t.h / p.group;
+      for (int it = 0; it < t.n_kt && ok; ++it, ++gk) {
+        const int ks = gk % 3, vs = gk & 1;
+        if (lane == 0 && gk >= 3 && !wait(k_empty(ks), ((gk / 3) - 1) & 1)) ok = false;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         const uint32_t kdst = sbase + L::kKOff + ks * L::kTile;
@@ -864,96 +891,124 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mbar_arrive_expect_tx(k_full(ks), L::kTile);
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(kdst + c * kChunkBytes, &tm_k, k_full(ks), c * 64, g,
-                        sq.k_tok0 + it * kBlockN, sq.map_b, pol_st);
+                        t.sq.k_tok0 + it * kBlockN, t.sq.map_b, pol_st);
         }
-        k_issued = it + 1;
-        if (k_partial(it)) {
+        k_issued = gk + 1;
+        if (VARLEN && it * kBlockN + kBlockN > t.sq.lk) {
           // rows past the sequence's keys belong to the next one: zero them
           // in K (the B operand of dQ += dS K) once the tile has landed
-          ok = __all_sync(0xffffffffu, wait(k_full(ks), (it / 3) & 1));
+          ok = __all_sync(0xffffffffu, wait(k_full(ks), (gk / 3) & 1));
           if (!ok) break;
-          zero_tail_rows<D>(kdst, lk - it * kBlockN, lane);
+          zero_tail_rows<D>(kdst, t.sq.lk - it * kBlockN, lane);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(k_fixed(ks));
         }
-        if (lane == 0 && it >= 2 && !wait(v_empty(vs), ((it >> 1) - 1) & 1)) ok = false;
+        if (lane == 0 && gk >= 2 && !wait(v_empty(vs), ((gk >> 1) - 1) & 1)) ok = false;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(v_full(vs), L::kTile);
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(sbase + L::kVOff + vs * L::kTile + c * kChunkBytes, &tm_v, v_full(vs),
-                        c * 64, g, sq.k_tok0 + it * kBlockN, sq.map_b, pol_st);
+                        c * 64, g, t.sq.k_tok0 + it * kBlockN, t.sq.map_b, pol_st);
         }
-        v_issued = it + 1;
-      }
-      // drain the copies still in flight before the CTA exits
-      if (lane == 0) {
-        wait_bar(q_full, 0, abort_flag, limit, p.status, false);
-        for (int it = max(0, k_issued - 3); it < k_issued; ++it)
-          wait_bar(k_full(it % 3), (it / 3) & 1, abort_flag, limit, p.status, false);
-        for (int it = max(0, v_issued - 2); it < v_issued; ++it)
-          wait_bar(v_full(it & 1), (it >> 1) & 1, abort_flag, limit, p.status, false);
+        v_issued = gk + 1;
       }
     }
+    // drain the copies still in flight before the CTA exits (Q / dO loads
+    // are serialised by q_empty, so only the last can be outstanding)
+    if (lane == 0 && n_acc > 0) {
+      wait_bar(q_full, (n_acc - 1) & 1, abort_flag, limit, p.status, false);
+      for (int it = max(0, k_issued - 3); it < k_issued; ++it)
+        wait_bar(k_full(it % 3), (it / 3) & 1, abort_flag, limit, p.status, false);
+      for (int it = max(0, v_issued - 2); it < v_issued; ++it)
+        wait_bar(v_full(it & 1), (it >> 1) & 1, abort_flag, limit, p.status, false);
+    }
   } else if (warp == kBwdMma) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_ss = make_idesc_f16(BF16, kBlockM, kBlockN, false);
-      constexpr uint32_t idesc_ts = make_idesc_f16(BF16, kBlockM, D, true);
-      const uint64_t q_desc = make_sdesc_sw128(sbase + L::kQOff, 16, 1024);
-      const uint64_t do_desc = make_sdesc_sw128(sbase + L::kDoOff, 16, 1024);
-      auto k_addr = [&](int it) { return sbase + L::kKOff + (it % 3) * L::kTile; };
-      auto v_addr = [&](int it) { return sbase + L::kVOff + (it & 1) * L::kTile; };
-      // S(it) = Q K(it)^T into its score buffer (tiles in increasing order);
-      // a partial packed tile is used once its tail rows are zeroed
-      uint32_t kfix = 0;  // bit s: phase of k_fixed(s), as the producer counts it
-      auto issue_s = [&](int it) {
-        const int ks = it % 3;
-        if (k_partial(it)) {
-          if (!wait(k_fixed(ks), (kfix >> ks) & 1u)) return false;
-          kfix ^= 1u << ks;
-        } else if (!wait(k_full(ks), (it / 3) & 1)) {
-          return false;
-        }
-        tc_fence_after();
-        issue_ss<D>(tmem + s_buf(it), q_desc, make_sdesc_sw128(k_addr(it), 16, 1024), idesc_ss);
-        return true;
-      };
-      // dP(it) = dO V(it)^T, then the V slot is released once it completes
-      auto issue_dp = [&](int it) {
-        if (!wait(v_full(it & 1), (it >> 1) & 1)) return false;
-        tc_fence_after();
-        issue_ss<D>(tmem + 128, do_desc, make_sdesc_sw128(v_addr(it), 16, 1024), idesc_ss);
-        tc_commit(v_empty(it & 1));
-        return true;
-      };
-      bool ok = n_kt == 0 || wait(q_full, 0);
-      if (ok && n_kt > 0) {
-        ok = issue_s(0) && issue_dp(0);
-        if (ok) tc_commit(sdp_full);
-        if (ok && n_kt > 1) ok = issue_s(1);
-      }
-      for (int it = 0; it < n_kt && ok; ++it) {
-        // dS(it) written by both warpgroups (and S(it), dP(it) read)
-        ok = wait_bar_spin(ds_half(0), it & 1, abort_flag, limit, p.status) &&
-             wait_bar_spin(ds_half(1), it & 1, abort_flag, limit, p.status);
-        if (!ok) break;
-        tc_fence_after();
-        if (it + 1 < n_kt) {  // the next tile's dP first: its elementwise waits on it
-          ok = issue_dp(it + 1);
-          if (!ok) break;
+    // the whole warp walks the items (the packed decode is warp-collective);
+    // lane 0 issues every MMA and commit
+    constexpr uint32_t idesc_ss = make_idesc_f16(BF16, kBlockM, kBlockN, false);
+    constexpr uint32_t idesc_ts = make_idesc_f16(BF16, kBlockM, D, true);
+    const uint64_t q_desc = make_sdesc_sw128(sbase + L::kQOff, 16, 1024);
+    const uint64_t do_desc = make_sdesc_sw128(sbase + L::kDoOff, 16, 1024);
+    auto k_addr = [&](int gs) { return sbase + L::kKOff + (gs % 3) * L::kTile; };
+    auto v_addr = [&](int gs) { return sbase + L::kVOff + (gs & 1) * L::kTile; };
+    bool ok = true;
+    int gk = 0, n_acc = 0;
+    uint32_t kfix = 0;  // bit s: phase of k_fixed(s), as the producer counts it
+    for (int i = 0; ok; ++i) {
+      const int w = item_of(i);
+      if (w >= n_items) break;
+      const QItem t = decode_q_item<CAUSAL, VARLEN>(p, w, lane);
+      if (!t.valid || t.n_kt == 0) continue;
+      if (lane == 0) {  // lanes 1-31 only follow the item sequence
+        const int n = t.n_kt, g0 = gk;
+        // S of item tile it (global step g0 + it) into its score buffer; a
+        // partial packed tile is used once its tail rows are zeroed
+        auto issue_s = [&](int it) {
+          const int gs = g0 + it, ks = gs % 3;
+          if (VARLEN && it * kBlockN + kBlockN > t.sq.lk) {
+            if (!wait(k_fixed(ks), (kfix >> ks) & 1u)) return false;
+            kfix ^= 1u << ks;
+          } else if (!wait(k_full(ks), (gs / 3) & 1)) {
+            return false;
+          }
+          tc_fence_after();
+          issue_ss<D>(tmem + s_buf(gs), q_desc, make_sdesc_sw128(k_addr(gs), 16, 1024),
+                      idesc_ss);
+          return true;
+        };
+        // dP of item tile it = dO V^T; the V slot is released once it completes
+        auto issue_dp = [&](int it) {
+          const int gs = g0 + it;
+          if (!wait(v_full(gs & 1), (gs >> 1) & 1)) return false;
+          tc_fence_after();
+          issue_ss<D>(tmem + 128, do_desc, make_sdesc_sw128(v_addr(gs), 16, 1024), idesc_ss);
+          tc_commit(v_empty(gs & 1));
+          return true;
+        };
+        ok = wait(q_full, n_acc & 1) && issue_s(0) && issue_dp(0);
+        if (ok) {
           tc_commit(sdp_full);
+          if (n == 1) tc_commit(q_empty);  // Q and dO read for the last time
+          if (n > 1) ok = issue_s(1);
         }
-        // dQ += dS(it) K(it) (K tile MN-major: rows = keys)
-        const uint64_t k_mn = make_sdesc_sw128(k_addr(it), kChunkBytes, 1024);
-        issue_ts_half(tmem + 256, tmem + s_buf(it), k_mn, idesc_ts, 0, it > 0);
-        issue_ts_half(tmem + 256, tmem + s_buf(it), k_mn, idesc_ts, 1, it > 0);
-        tc_commit(k_empty(it % 3));
-        // S(it + 2) into the buffer dQ(it) reads (the pipe keeps issue order)
-        if (it + 2 < n_kt) ok = issue_s(it + 2);
-      }
-      tc_commit(acc_ready);
+        for (int it = 0; it < n && ok; ++it, ++gk) {
+          // dS(it) written by both warpgroups (and S(it), dP(it) read)
+          ok = wait_bar_spin(ds_half(0), gk & 1, abort_flag, limit, p.status) &&
+               wait_bar_spin(ds_half(1), gk & 1, abort_flag, limit, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          if (it + 1 < n) {  // the next tile's dP first: its elementwise waits on it
+            ok = issue_dp(it + 1);
+            if (!ok) break;
+            tc_commit(sdp_full);
+            if (it + 2 == n) tc_commit(q_empty);  // the item's last dP (its last S is earlier)
+          }
+          // the item's first dQ product overwrites the accumulator: the
+          // previous item's epilogue must have read it
+          if (it == 0 && n_acc > 0) {
+            ok = wait(acc_free, (n_acc - 1) & 1);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          // dQ += dS(it) K(it) (K tile MN-major: rows = keys)
+          const uint64_t k_mn = make_sdesc_sw128(k_addr(gk), kChunkBytes, 1024);
+          issue_ts_half(tmem + 256, tmem + s_buf(gk), k_mn, idesc_ts, 0, it > 0);
+          issue_ts_half(tmem + 256, tmem + s_buf(gk), k_mn, idesc_ts, 1, it > 0);
+          tc_commit(k_empty(gk % 3));
+          // S(it + 2) into the buffer dQ(it) reads (the pipe keeps issue order)
+          if (it + 2 < n) ok = issue_s(it + 2);
+        }
+        if (ok) {
+          tc_commit(acc_ready);
+          ++n_acc;
+        }
+      }  // lane 0
+      ok = __shfl_sync(0xffffffffu, ok, 0);  // every lane, once per item
+    }
+    if (lane == 0) {
       tc_commit(drain);
       wait_bar(drain, 0, abort_flag, limit, p.status, false);
     }
@@ -961,57 +1016,78 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------ elementwise: one query row per thread
     const int quarter = warp & 3, wg = warp >> 2;  // TMEM lane quarter, column half
     const int row = quarter * 32 + lane;
-    const int qi = q0 + row;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
-    const int64_t r = (lse_b * p.Hq + h) * p.Sq + lse_row0 + qi;
-    const float lse2 = qi < lq ? p.lse_l2[r] : INFINITY;
-    const float dlt = qi < lq ? p.delta[r] : 0.f;
     bool ok = true;
-    for (int it = 0; it < n_kt; ++it) {
-      if (ok) ok = __all_sync(0xffffffffu, wait(sdp_full, it & 1));
-      if (ok) {
-        tc_fence_after();
-        const bool interior = (it + 1) * kBlockN <= lk && q0 + kBlockM <= lq &&
-                              (!CAUSAL || it * kBlockN + kBlockN - 1 <= q0 + off);
-        const uint32_t base = lane_base + s_buf(it);
-        const uint32_t dp_minus_s = 128u - s_buf(it);  // dP columns relative to base
+    int gk = 0, n_acc = 0;
+    for (int i = 0;; ++i) {
+      const int w = item_of(i);
+      if (w >= n_items) break;
+      const QItem t = decode_q_item<CAUSAL, VARLEN>(p, w, lane);
+      if (!t.valid) continue;
+      const int lq = t.sq.lq, lk = t.sq.lk, q0 = t.q0, off = t.off;
+      const int qi = q0 + row;
+      const int64_t lse_b = VARLEN ? 0 : (int64_t)t.b;
+      const int64_t lse_row0 = VARLEN ? (int64_t)t.sq.q_tok0 : 0;
+      const int64_t r = (lse_b * p.Hq + t.h) * p.Sq + lse_row0 + qi;
+      const float lse2 = qi < lq ? p.lse_l2[r] : INFINITY;
+      const float dlt = qi < lq ? p.delta[r] : 0.f;
+      for (int it = 0; it < t.n_kt; ++it, ++gk) {
+        if (ok) ok = __all_sync(0xffffffffu, wait(sdp_full, gk & 1));
+        if (ok) {
+          tc_fence_after();
+          const bool interior = (it + 1) * kBlockN <= lk && q0 + kBlockM <= lq &&
+                                (!CAUSAL || it * kBlockN + kBlockN - 1 <= q0 + off);
+          const uint32_t base = lane_base + s_buf(gk);
+          const uint32_t dp_minus_s = 128u - s_buf(gk);  // dP columns relative to base
 #pragma unroll 1
-        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-          if (interior)
-            q_chunk<BF16, false, CAUSAL>(base, dp_minus_s, c, sl2, lse2, dlt, qi, it, lq, lk,
-                                         off);
-          else
-            q_chunk<BF16, true, CAUSAL>(base, dp_minus_s, c, sl2, lse2, dlt, qi, it, lq, lk,
-                                        off);
+          for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
+            if (interior)
+              q_chunk<BF16, false, CAUSAL>(base, dp_minus_s, c, sl2, lse2, dlt, qi, it, lq, lk,
+                                           off);
+            else
+              q_chunk<BF16, true, CAUSAL>(base, dp_minus_s, c, sl2, lse2, dlt, qi, it, lq, lk,
+                                          off);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ds_half(wg));  // this half of the keys is written
         }
-        tmem_st_wait();
+        __syncwarp();
+      }
+      // ----------------------------------------------------------- epilogue
+      // warpgroup wg reads columns wg D / 2 .. (wg + 1) D / 2 - 1 of dQ out of
+      // tensor memory, releases the accumulator (acc_free), then stores
+      bool have = t.n_kt > 0 && ok;
+      if (have) have = __all_sync(0xffffffffu, wait(acc_ready, n_acc & 1));
+      if (t.n_kt > 0 && !have) ok = false;
+      constexpr int kHalf = D / 2;
+      uint32_t rq[kHalf];
+      if (have) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kHalf / 32; ++c)
+          tmem_ld32(lane_base + 256 + wg * kHalf + c * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(rq + 32 * c));
+#pragma unroll
+        for (int c = 0; c < kHalf / 32; ++c)
+          tmem_wait_ld32(*reinterpret_cast<uint32_t(*)[32]>(rq + 32 * c));
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(ds_half(wg));  // this half of the keys is written
-      }
-      __syncwarp();
-    }
-    bool have = n_kt > 0 && ok;
-    if (have) have = __all_sync(0xffffffffu, wait(acc_ready, 0));
-    if (n_kt > 0 && !have) ok = false;
-    if (have) tc_fence_after();
-    const bool store = qi < lq && (ok || n_kt == 0);
-    elem_t *dq = reinterpret_cast<elem_t *>(p.dq) +
-                 ((lse_b * p.Sq + sq.q_tok0 + (store ? qi : 0)) * p.Hq + h) * D;
-#pragma unroll 1
-    for (int c = wg * D / 64; c < (wg + 1) * D / 64; ++c) {
-      float x[32];
-      if (have) {
-        uint32_t rq[32];
-        tmem_ld32_wait(lane_base + 256 + c * 32, rq);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(rq[e]);
+        if (lane == 0) mbar_arrive(acc_free);
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = 0.f;  // the row sees no key
+        for (int e = 0; e < kHalf; ++e) rq[e] = 0u;  // the row sees no key
       }
-      if (store) store_row32<BF16>(dq + c * 32, x, p.scale);
+      if (t.n_kt > 0) ++n_acc;
+      if (qi < lq && (ok || t.n_kt == 0)) {
+        elem_t *dq = reinterpret_cast<elem_t *>(p.dq) +
+                     ((lse_b * p.Sq + t.sq.q_tok0 + qi) * p.Hq + t.h) * D + wg * kHalf;
+#pragma unroll
+        for (int c = 0; c < kHalf / 32; ++c)
+          store_row32<BF16>(dq + c * 32, reinterpret_cast<const float *>(rq + 32 * c), p.scale);
+      }
     }
   }
 
@@ -1063,8 +1139,8 @@ cudaError_t launch_bwd_t(const BwdLaunch &a) {
     if (e != cudaSuccess) return e;
   }
   if (q_ctas > 0) {
-    qk<<<(unsigned)q_ctas, kBwdThreads, LQ::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v,
-                                                               a.tm_do, p);
+    const unsigned q_grid = (unsigned)(q_ctas < a.sms ? q_ctas : a.sms);
+    qk<<<q_grid, kBwdThreads, LQ::kAlloc, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, p);
     e = cudaGetLastError();
   }
   return e;
