@@ -1,13 +1,17 @@
 // Backward pass of exact attention on sm_103a (see fa_bwd.cuh for the math).
 //
 // Both tile passes use the same two tcgen05 patterns as the forward kernel:
-//   SS, both operands K-major, M128 N128 K=D:  S^T = K Q^T, dP^T = V dO^T
-//                                              (key pass), S = Q K^T,
-//                                              dP = dO V^T (query pass);
-//   TS, A = 16-bit P / dS in tensor memory, B MN-major, M128 N=D K=128:
-//                                              dV += P^T dO, dK += dS^T Q
-//                                              (key pass), dQ += dS K
-//                                              (query pass).
+//   SS, both operands K-major, K = D:  S^T = K Q^T, dP^T = V dO^T (key pass,
+//                                      M128 N64 per half of the queries),
+//                                      S = Q K^T, dP = dO V^T (query pass,
+//                                      M128 N128);
+//   TS, A = 16-bit P / dS in tensor memory, B MN-major, M128 N=D, K = 64
+//                                      rows per half: dV += P^T dO,
+//                                      dK += dS^T Q (key pass), dQ += dS K
+//                                      (query pass).
+// Both tile passes are persistent: one CTA per SM walks a snake over the
+// heavy-first order of its work items, every barrier phase carried across
+// items.
 // A CTA has ten warps: warps 0-7 do the elementwise work (warp w owns tensor
 // memory lanes 32 (w % 4) .. 32 (w % 4) + 31 -- one key row per thread in the
 // key pass, one query row in the query pass -- and warpgroup w / 4 the column
