@@ -71,3 +71,20 @@ def test_visible_rows_match_flop_count():
         vis = bench._visible_per_row(case)
         assert vis.shape[0] == case.lse_rows()
         assert 4 * case.D * int(vis.sum()) == wl.attention_flops(case)
+
+
+def test_backward_workloads_and_oracle_sample():
+    """Every forward workload with head dim 64 / 128 has a backward twin, and
+    the backward CPU baseline times the oracle's gradients on a sub-problem
+    (batch 0, every head, a prefix of the positions) with 2.5x its forward
+    FLOPs."""
+    from exact_attention_forward_sm_gb300 import workloads as wl
+    names = {w.name for w in wl.WORKLOADS if w.D in (64, 128)}
+    assert {n[len(bench.BWD_PREFIX):] for n in bench.BWD_WORKLOADS} == names
+    case = wl.make_case(2, 4, 2, 300, 300, 64, "fp16", True, seed=3)
+    dout = torch.randn(tuple(case.q.shape)).to(case.q.dtype)
+    r = bench.oracle_sample_bwd(case, dout, seconds=0.05)
+    sp = r["rows"] // case.Hq
+    assert 1 <= sp <= 300 and r["rows_total"] == 2 * 4 * 300
+    assert r["flops"] == 2.5 * 4.0 * 64 * 4 * sp * (sp + 1) / 2
+    assert r["tflops"] > 0 and r["threads"] >= 1
