@@ -385,6 +385,7 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
   p.head_units = head_units;
   p.rows_per_unit = rows_per_unit;
   p.dense_row_units = (int)row_units;
+  p.rows_fastest = (!varlen && win_l < 0 && win_r < 0) ? 1 : 0;
   p.total_units = (int)units;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.threshold = FA_RESCALE_THRESHOLD;
@@ -517,6 +518,7 @@ int forward_kvcache(const void *q, const void *k_cache, const void *v_cache, voi
   p.head_units = Hkv;
   p.rows_per_unit = tok_per_tile;
   p.dense_row_units = (int)tok_blocks;
+  p.rows_fastest = 0;
   p.total_units = (int)units;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.threshold = FA_RESCALE_THRESHOLD;

@@ -118,6 +118,9 @@ struct FwdParams {
   int head_units;           // head slots per sequence: Hq / 2 or Hq
   int rows_per_unit;        // query rows per unit and head slot: 128 or 256
   int dense_row_units;      // dense problems: ceil(Sq / rows_per_unit)
+  int rows_fastest;         // dense, every unit the same work (no causal mask, no
+                            // window): the row unit varies fastest, so the
+                            // CTAs running together share one head's K / V in L2
   int total_units;          // units to process (packed: an upper bound)
   float scale_log2;         // scale * log2(e)
   float threshold;          // lazy-rescale threshold, log2 units
@@ -153,7 +156,7 @@ struct FwdParams {
   int tok_blocks;           // ceil(Sq / tok_per_tile)
   // the divisors of the unit index, set by set_divisors() once the fields
   // above are final
-  FastDiv div_splits, div_head_units, div_B, div_Hkv, div_tok_blocks;
+  FastDiv div_splits, div_head_units, div_B, div_Hkv, div_tok_blocks, div_ru;
   long long wait_limit;     // bounded-wait limit in SM clock cycles
   int *status;              // device status word (first error wins)
   unsigned long long *trace;  // clock64 pipeline trace (trace builds only)
@@ -165,6 +168,7 @@ inline void set_divisors(FwdParams &p) {
   p.div_B = make_fast_div(p.B > 0 ? p.B : 1);
   p.div_Hkv = make_fast_div(p.Hkv > 0 ? p.Hkv : 1);
   p.div_tok_blocks = make_fast_div(p.tok_blocks > 0 ? p.tok_blocks : 1);
+  p.div_ru = make_fast_div(p.dense_row_units > 0 ? p.dense_row_units : 1);
 }
 
 // Pipeline trace (compiled in with -DFA_TRACE): CTA 0 records SM clock stamps
@@ -382,14 +386,23 @@ __device__ Work decode_work(const FwdParams &p, int unit, int lane) {
     unit = u;
   }
   const int u_hu = fast_div(p.div_head_units, unit);  // unit / head_units
-  const int hu = unit - u_hu * p.head_units;
+  int hu = unit - u_hu * p.head_units;
   int b = 0, ru = 0, n_ru = 0;
   if (!VARLEN) {
-    // unit = (ru * B + b) * head_units + hu
-    ru = fast_div(p.div_B, u_hu);
-    b = u_hu - ru * p.B;
     n_ru = p.dense_row_units;
-    if (ru >= n_ru) return w;
+    if (p.rows_fastest) {
+      // unit = (b * head_units + hu) * n_ru + ru
+      const int bh = fast_div(p.div_ru, unit);
+      ru = unit - bh * n_ru;
+      b = fast_div(p.div_head_units, bh);
+      hu = bh - b * p.head_units;
+      if (b >= p.B) return w;
+    } else {
+      // unit = (ru * B + b) * head_units + hu: heavier rows first
+      ru = fast_div(p.div_B, u_hu);
+      b = u_hu - ru * p.B;
+      if (ru >= n_ru) return w;
+    }
     w.lq = p.Sq;
     w.lk = p.Sk;
     w.q_row0 = 0;
