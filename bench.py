@@ -596,6 +596,7 @@ def run_gpu_arm(args, rank, local_rank, world):
                             else f"{peak_src} {dense_key} (burst, cuBLAS bf16)"),
             "kernel": prob.kernel,
             "kernel_ms_mean": round(kernel_ms, 5),
+            "kernel_ms_median": round(statistics.median(times_ms), 5),
             "kernel_ms_min": round(min(times_ms), 5),
         },
         "e2e": {
