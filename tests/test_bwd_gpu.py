@@ -8,12 +8,19 @@ with ``oracle.attention_bwd`` (fp64, plain definition) on the same 16-bit
 inputs and upstream gradient.
 
 Gates per gradient tensor: cosine >= 0.9995 and max |g - ref| <= TOL *
-max(max |ref|, 1e-3) with TOL = 2e-2 (bf16) / 1e-2 (fp16).  The kernels round P and dS
-to the input type for the tensor-core products and the outputs to it (bf16
-keeps 8 significant bits: 2^-9 relative per rounding, 2^-8 per output
-element at worst); the row term rowsum(dO * O) reads the 16-bit O, and dS =
-P (dP - rowsum) cancels, so the gates sit a few output roundings above that.
+max(max |ref|, 1e-3) with TOL = 2e-2 (bf16) / 1e-2 (fp16).  The kernels
+round P and dS to the input type for the tensor-core products and the outputs
+to it (bf16 keeps 8 significant bits: 2^-9 relative per rounding, 2^-8 per
+output element at worst); the row term rowsum(dO * O) reads the 16-bit O, and
+dS = P (dP - rowsum) cancels, so the gates sit a few output roundings above
+that.
+
+With FA_PARITY_REPORT=<path> set, every comparison appends its metrics to
+that file as one JSON line.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -67,6 +74,12 @@ def _compare(name, got, ref, dtype):
     scale = max(np.max(np.abs(ref)), ABS_FLOOR)
     err = np.max(np.abs(g - ref)) / scale
     cos = float(np.sum(g * ref) / max(np.linalg.norm(g) * np.linalg.norm(ref), 1e-300))
+    report = os.environ.get("FA_PARITY_REPORT")
+    if report:
+        with open(report, "a") as f:
+            f.write(json.dumps({"case": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0],
+                                "grad": name, "dtype": dtype, "err_of_max": err,
+                                "cosine": cos}) + "\n")
     assert err <= TOL[dtype], f"{name}: max error {err:.3e} of max |ref|"
     if np.max(np.abs(ref)) > 0:
         assert cos >= COS_MIN, f"{name}: cosine {cos:.6f}"
@@ -139,6 +152,12 @@ def test_full_size_causal_benchmark_shape():
     release notes' backward finiteness check runs S = 2048 causal): every
     element of dq, dk, dv against the oracle."""
     _check(4, 16, 16, 2048, 2048, 128, "bf16", True, seed=2048)
+
+
+def test_short_benchmark_shape():
+    """B1 H2 S128 D64 fp16 non-causal, the short shape of the benchmark's
+    backward workloads: one tile each way."""
+    _check(1, 2, 2, 128, 128, 64, "fp16", False, seed=128)
 
 
 def test_full_size_gqa_rising_bias_workload():
@@ -228,3 +247,22 @@ def test_packed_neighbours_hold_inf_and_nan():
     clean = np.concatenate([np.arange(int(cu_q[b]), int(cu_q[b + 1])) for b in (0, 2, 4)])
     for n, t, r in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
         _compare(n, t[torch.as_tensor(clean, device=t.device)].contiguous(), r[clean], "bf16")
+
+
+def test_full_size_packed_workload():
+    """The packed benchmark workload at full size (16 sequences of 64 to 8192
+    tokens from its seeded recipe, H16, D64 fp16 causal) with a seeded
+    upstream gradient: every element of dq, dk, dv against the oracle (about
+    a minute and a half of fp64 work on 16 host cores)."""
+    from exact_attention_forward_sm_gb300 import workloads as wl
+    case = wl.make_workload(wl.BY_NAME["varlen16_l64to8192_h16_d64_fp16_causal"])
+    g = torch.Generator().manual_seed(8192)
+    do = torch.randn(tuple(case.q.shape), generator=g).to(case.q.dtype)
+    assert case.scale == case.D ** -0.5  # the binding's default scale
+    dq, dk, dv = _run_packed(case.q, case.k, case.v, do, case.cu_seqlens_q,
+                             case.cu_seqlens_k, True)
+    refs = oracle.attention_bwd(case.q, case.k, case.v, do, case.B, case.Hq, case.Hkv, case.Sq,
+                                case.Sk, case.D, case.scale, True, case.cu_seqlens_q,
+                                case.cu_seqlens_k)
+    for n, t, r in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        _compare(n, t, r, "fp16")
