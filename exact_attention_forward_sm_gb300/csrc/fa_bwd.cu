@@ -47,7 +47,9 @@ struct SmemBwd {
   static constexpr uint32_t kBarOff = kVecOff + 2048;
   static constexpr int kNumBars = 15;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr uint32_t kBytes = kMiscOff + 16;
+  // key pass: a 2 KB staging buffer per elementwise warp for the dV / dK rows
+  static constexpr uint32_t kEpiOff = (kMiscOff + 16 + 127) / 128 * 128;
+  static constexpr uint32_t kBytes = kEpiOff + 8 * 2048;
   // at least 120 KB, so that two CTAs never share an SM: each allocates all
   // 512 tensor-memory columns
   static constexpr uint32_t kAlloc = kBytes + 1024 > 120u * 1024 ? kBytes + 1024 : 120u * 1024;
@@ -662,9 +664,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // ----------------------------------------------------------- epilogue
       // Warpgroup wg owns columns wg D / 2 .. (wg + 1) D / 2 - 1 of dV and dK:
       // all of them are read out of tensor memory first and the accumulators
-      // released (acc_free), then converted and stored.  The loads are
-      // warp-wide (have, ok are warp-uniform); only the stores of keys inside
-      // the sequence are per lane.
+      // released (acc_free), then converted and stored through the warp's
+      // staging buffer.  The loads are warp-wide (have, ok are warp-uniform);
+      // only rows of keys inside the sequence are written.
       bool have = t.n_it > 0 && ok;
       if (have) have = __all_sync(0xffffffffu, wait(acc_ready, n_acc & 1));
       if (t.n_it > 0 && !have) ok = false;
@@ -692,15 +694,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int e = 0; e < kHalf; ++e) rv[e] = rk[e] = 0u;  // no query sees these keys
       }
       if (t.n_it > 0) ++n_acc;
-      const bool store = j < lk && (ok || t.n_it == 0);
-      if (store) {
-        const int64_t rbase = ((lse_b * p.Sk + t.sq.k_tok0 + j) * p.Hkv + t.g) * D + wg * kHalf;
-        elem_t *dv = reinterpret_cast<elem_t *>(p.dv) + rbase;
-        elem_t *dk = reinterpret_cast<elem_t *>(p.dk) + rbase;
+      if (ok || t.n_it == 0) {  // warp-uniform
+        // 32 columns of the warp's 32 key rows at a time: each lane packs its
+        // row into the warp's staging buffer (16-byte pieces XOR-swizzled by
+        // row, so neither side conflicts on banks), then the warp writes 8
+        // whole 64-byte row pieces per store instead of 32 half sectors
+        uint8_t *stg = smem + L::kEpiOff + warp * 2048;
+        const int kr0 = k0 + quarter * 32;  // key of the warp's row 0
+        const int64_t tok0 = lse_b * p.Sk + t.sq.k_tok0 + kr0;
 #pragma unroll
-        for (int c = 0; c < kHalf / 32; ++c) {
-          store_row32<BF16>(dv + c * 32, reinterpret_cast<const float *>(rv + 32 * c), 1.f);
-          store_row32<BF16>(dk + c * 32, reinterpret_cast<const float *>(rk + 32 * c), p.scale);
+        for (int which = 0; which < 2; ++which) {  // dV, then dK
+          const uint32_t *src = which ? rk : rv;
+          const float mul = which ? p.scale : 1.f;
+          elem_t *out = reinterpret_cast<elem_t *>(which ? p.dk : p.dv);
+#pragma unroll
+          for (int c = 0; c < kHalf / 32; ++c) {
+            const float *x = reinterpret_cast<const float *>(src + 32 * c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4 *>(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) * 16)) =
+                  make_uint4(pack_p<BF16>(x[8 * q] * mul, x[8 * q + 1] * mul),
+                             pack_p<BF16>(x[8 * q + 2] * mul, x[8 * q + 3] * mul),
+                             pack_p<BF16>(x[8 * q + 4] * mul, x[8 * q + 5] * mul),
+                             pack_p<BF16>(x[8 * q + 6] * mul, x[8 * q + 7] * mul));
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int r = (lane >> 2) + 8 * k, pc = lane & 3;
+              const uint4 v =
+                  *reinterpret_cast<const uint4 *>(stg + r * 64 + ((pc ^ ((r >> 1) & 3)) * 16));
+              if (kr0 + r < lk)
+                *reinterpret_cast<uint4 *>(out + ((tok0 + r) * p.Hkv + t.g) * D + wg * kHalf +
+                                           c * 32 + pc * 8) = v;
+            }
+            __syncwarp();
+          }
         }
       }
     }
