@@ -88,3 +88,25 @@ def test_backward_workloads_and_oracle_sample():
     assert 1 <= sp <= 300 and r["rows_total"] == 2 * 4 * 300
     assert r["flops"] == 2.5 * 4.0 * 64 * 4 * sp * (sp + 1) / 2
     assert r["tflops"] > 0 and r["threads"] >= 1
+
+
+def test_reference_arm_prints_one_json_line():
+    """`bench.py --impl reference` times the oracle on bounded samples of the
+    default workload and prints one JSON line: the shared keys, impl,
+    cpu_baseline and an end-to-end object with no host-device copies."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                        "--warmup", "3", "--reference-budget-s", "2"],
+                       cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["config"]["workload"] == "b4_h16_s2048_d128_bf16_causal"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
